@@ -223,7 +223,8 @@ WORKLOADS: Dict[str, Workload] = {
 }
 
 
-def make_inputs(wl: Workload, device="cpu", batches: Optional[List[int]] = None) -> Dict[str, torch.Tensor]:
+def make_inputs(wl: Workload, device="cpu", batches: Optional[List[int]] = None,
+                only: Optional[set] = None) -> Dict[str, torch.Tensor]:
     """Materialise the inputs of ``wl`` (optionally only sequences ``batches``).
 
     Returned keys depend on the mode:
@@ -231,12 +232,15 @@ def make_inputs(wl: Workload, device="cpu", batches: Optional[List[int]] = None)
       decode : q, q_idx, k_cmp, v_cmp, i_cmp, k_raw, v_raw, w, q_pos, raw_base
       hca    : q, k_raw, v_raw, g_k, g_v, q_pos, raw_base
     bf16 tensors are [B, ...] row-major; q_pos [B, Tq] int32; raw_base [B] int32;
-    w [H_I] fp32.
+    w [H_I] fp32.  ``only`` restricts the result to the named tensors.
     """
     bl = list(range(wl.B)) if batches is None else list(batches)
     s = wl.seed
     pos = torch.tensor(wl.q_positions, dtype=torch.int64, device=device)
     out: Dict[str, torch.Tensor] = {}
+
+    def want(name):
+        return only is None or name in only
 
     def heads(name, H, width):
         return torch.stack([rows_bf16_heads(s, TID[name], wl.T, H, width, b, pos) for b in bl])
@@ -252,24 +256,25 @@ def make_inputs(wl: Workload, device="cpu", batches: Optional[List[int]] = None)
         return torch.stack([normal_bf16(s, TID[name], (wl.N, width), device,
                                         offset=b * wl.N * width) for b in bl])
 
-    out["q"] = heads("q", wl.H, wl.d)
+    if want("q"):
+        out["q"] = heads("q", wl.H, wl.d)
     if wl.mode != "hca":
-        out["q_idx"] = heads("q_idx", wl.H_I, wl.d_I)
-        out["w"] = uniform_f32(s, TID["w"], (wl.H_I,), device)
+        if want("q_idx"):
+            out["q_idx"] = heads("q_idx", wl.H_I, wl.d_I)
+        if want("w"):
+            out["w"] = uniform_f32(s, TID["w"], (wl.H_I,), device)
     if wl.mode in ("prefill", "hca"):
-        out["k_raw"] = raw("k_raw", wl.d, 0, wl.T)
-        out["v_raw"] = raw("v_raw", wl.d, 0, wl.T)
-        out["g_k"] = raw("g_k", wl.d, 0, wl.T)
-        out["g_v"] = raw("g_v", wl.d, 0, wl.T)
-        if wl.mode == "prefill":
-            out["i_raw"] = raw("i_raw", wl.d_I, 0, wl.T)
-            out["g_i"] = raw("g_i", wl.d_I, 0, wl.T)
+        names = ["k_raw", "v_raw", "g_k", "g_v"] + (["i_raw", "g_i"] if wl.mode == "prefill" else [])
+        for name in names:
+            if want(name):
+                out[name] = raw(name, wl.d_I if name in ("i_raw", "g_i") else wl.d, 0, wl.T)
     else:
-        out["k_cmp"] = cache("k_cmp", wl.d)
-        out["v_cmp"] = cache("v_cmp", wl.d)
-        out["i_cmp"] = cache("i_cmp", wl.d_I)
-        out["k_raw"] = raw("k_raw", wl.d, wl.raw_base, wl.raw_len)
-        out["v_raw"] = raw("v_raw", wl.d, wl.raw_base, wl.raw_len)
+        for name, width in (("k_cmp", wl.d), ("v_cmp", wl.d), ("i_cmp", wl.d_I)):
+            if want(name):
+                out[name] = cache(name, width)
+        for name in ("k_raw", "v_raw"):
+            if want(name):
+                out[name] = raw(name, wl.d, wl.raw_base, wl.raw_len)
     out["q_pos"] = pos.to(torch.int32)[None, :].repeat(len(bl), 1).contiguous()
     out["raw_base"] = torch.full((len(bl),), wl.raw_base, dtype=torch.int32, device=device)
     return out

@@ -1,0 +1,220 @@
+/*
+ * csa.h -- C ABI of the B300 (sm_103a) Compressed Sparse Attention library.
+ *
+ * The library computes the CSA layer of the DeepSeek-V4 descriptions and its
+ * dense HCA mode on one GPU:
+ *   (1) block compression of the raw K / V / indexer-key streams,
+ *   (2) Lightning-Indexer scores of each query against the visible entries,
+ *   (3) per-query top-k of those scores,
+ *   (4) attention over the selected entries merged with a sliding window of
+ *       raw tokens (CSA), or over every visible entry (HCA).
+ *
+ * Sources: "DeepSeek V4: Compressed Sparse Attention and the Million-Token
+ * Context" (octagono.org), section "Hybrid Attention: CSA and HCA";
+ * "DeepSeek V4 technical review" (takeshell.com), sections 2.1 CSA and
+ * 2.2 HCA.  The accompanying workload specification fixes the compressor
+ * (per-channel softmax of given gate logits times the raw vectors), the score
+ * (sum_h w_h * ReLU(q_h . k)), the lowest-index tie rule, the visibility rule
+ * (block b visible to position t iff (b+1)*m - 1 <= t), the scale 1/sqrt(d)
+ * and the single shared K/V stream (MQA).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers named as tensors are DEVICE pointers owned by the caller; the
+ *   library never allocates, frees or keeps them.  Arrays of pointers and
+ *   size arrays (``x``, ``g``, ``out``, ``D`` of csa_compress, the args
+ *   struct of csa_layer) are HOST memory, read during the call only.
+ * - Tensors are dense row-major with the shapes given, bf16 unless stated.
+ *   Every bf16 / fp32 tensor must start on a 16-byte boundary.
+ * - ``stream`` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *   only enqueues work on it and returns; nothing synchronises except
+ *   csa_check_error.
+ * - Argument errors are found before anything is enqueued: a call that
+ *   returns an error has written nothing.  CSA_ERR_CUDA reports a failed
+ *   launch (cudaGetLastError).  Conditions found on the device (an index
+ *   outside its buffer, a bounded wait that ran out) set bits in the error
+ *   word at the start of the workspace; read them with csa_check_error.
+ * - ``ws`` / ``ws_bytes``: caller-owned device scratch of at least the size
+ *   the matching *_workspace call reports, 256-byte aligned, initialised once
+ *   with csa_workspace_init.  One workspace must not be used by two calls
+ *   that overlap on the GPU.
+ * - Results do not depend on the GPU's SM count or on timing: no floating-
+ *   point atomics are used and partial results are merged in a fixed order.
+ */
+#ifndef CSA_H_
+#define CSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum csa_status {
+    CSA_OK = 0,
+    CSA_ERR_INVALID = 1,      /* null pointer, bad size, misaligned tensor       */
+    CSA_ERR_UNSUPPORTED = 2,  /* valid, but a shape this build does not handle   */
+    CSA_ERR_WORKSPACE = 3,    /* workspace missing, misaligned or too small      */
+    CSA_ERR_CUDA = 4,         /* a CUDA call or kernel launch failed             */
+    CSA_ERR_TIMEOUT = 5,      /* device: a bounded wait ran out                  */
+    CSA_ERR_DEVICE_INDEX = 6  /* device: an index or window row outside its buffer */
+} csa_status;
+
+typedef enum csa_dtype { CSA_BF16 = 0, CSA_F32 = 1 } csa_dtype;
+
+/* Device error-word bits (csa_check_error's *flags). */
+#define CSA_FLAG_TIMEOUT 0x1u
+#define CSA_FLAG_INDEX 0x2u
+
+/* Bytes at the start of every workspace that hold the error word. */
+#define CSA_WS_HEADER_BYTES 256
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* csa_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int csa_version(void);
+
+/* Zero the error word at the start of ``ws`` (stream-ordered memset).
+ * Call once after allocating a workspace.  ws_bytes >= CSA_WS_HEADER_BYTES. */
+csa_status csa_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Wait for ``stream`` and read the workspace error word.  *flags (nullable)
+ * receives the raw bits; returns CSA_ERR_TIMEOUT / CSA_ERR_DEVICE_INDEX when a
+ * bit is set, else CSA_OK.  clear != 0 zeroes the word after reading it. */
+csa_status csa_check_error(const void* ws, uint32_t* flags, int clear, void* stream);
+
+/* --------------------------------------------------------------------------
+ * (1) Block compression.  "DeepSeek V4 technical review", section 2.1: each
+ * compressed entry is a weighted sum of m consecutive tokens (section 2.2:
+ * m' = 128 for HCA).  Entry b, channel c of stream i:
+ *     out_i[n, b, c] = sum_{j<m} softmax_j(g_i[n, b*m+j, c]) * x_i[n, b*m+j, c]
+ * n_streams (1..3) independent (x_i, g_i) -> out_i triples in one launch:
+ *   x[i], g[i] : [B, T, D[i]] bf16          out[i] : [B, T/m, D[i]] out_dtype
+ * T mod m trailing tokens are not compressed.  D[i] in {8, 16, ..., 512}
+ * (multiple of 8); 1 <= m <= 4096; out_dtype CSA_BF16 (round to nearest
+ * even) or CSA_F32.  Needs no workspace.
+ * ------------------------------------------------------------------------ */
+csa_status csa_compress(int n_streams, const void* const* x, const void* const* g,
+                        void* const* out, const int* D, int B, int T, int m,
+                        int out_dtype, void* stream);
+
+/* --------------------------------------------------------------------------
+ * (2) Lightning Indexer scores.  Octagono "Hybrid Attention: CSA and HCA" and
+ * the technical review, section 2.1: every query gets indexer queries that
+ * are scored against the compressed entries; 64 heads of width 128.
+ *     S[n, j, b] = sum_h w[h] * ReLU(q_idx[n, j, h, :] . k_idx[n, b, :])
+ * for the visible blocks b < n_vis = min(N, floor((q_pos[n, j] + 1) / m)).
+ *   q_idx  [B, Tq, H_I, d_I] bf16     k_idx [B, N, d_I] bf16
+ *   w      [H_I] fp32                 q_pos [B, Tq] int32 (absolute positions)
+ *   scores [B, Tq, ld_scores] fp32, ld_scores >= N and a multiple of 4;
+ *          entries b >= n_vis are left untouched.
+ * Computed on the tcgen05 tensor cores (bf16 products, fp32 accumulation).
+ * H_I in {4, 8, 16, 32, 64, 128}; d_I in {32, 64, 128}.  Workspace:
+ * CSA_WS_HEADER_BYTES.
+ * ------------------------------------------------------------------------ */
+csa_status csa_index_scores(const void* q_idx, const void* k_idx, const float* w,
+                            const int32_t* q_pos, int B, int Tq, int N, int H_I, int d_I,
+                            int m, float* scores, int64_t ld_scores,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
+ * (3) Top-k.  Technical review, section 2.1: keep the top-k compressed blocks
+ * per query (k = 1024).  Among the n_vis visible scores of each query keep
+ * the min(k, n_vis) largest; equal scores go to the lower block index.
+ *   scores    [B, Tq, ld_scores] fp32 (only b < n_vis is read; -0 == +0)
+ *   idx_out   [B, Tq, k] int32: kept block indices ascending, then -1
+ *   score_out [B, Tq, k] fp32 (nullable): the kept scores, 0 in padding
+ * Integer radix selection on order-preserving keys: exact, no tolerance.
+ * 1 <= k <= 4096; N <= 262144 * 3.  Workspace: CSA_WS_HEADER_BYTES.
+ * ------------------------------------------------------------------------ */
+csa_status csa_topk(const float* scores, int64_t ld_scores, const int32_t* q_pos,
+                    int B, int Tq, int N, int m, int k, int32_t* idx_out, float* score_out,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/* (2)+(3) in one call; the scores live in the workspace. */
+csa_status csa_index_topk_workspace(int B, int Tq, int N, int H_I, int d_I, int k,
+                                    size_t* bytes);
+csa_status csa_index_topk(const void* q_idx, const void* k_idx, const float* w,
+                          const int32_t* q_pos, int B, int Tq, int N, int H_I, int d_I,
+                          int m, int k, int32_t* idx_out, float* score_out,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
+ * (4) Sparse attention + sliding window (CSA).  Technical review, section
+ * 2.1: attention runs only over the selected compressed blocks; octagono
+ * "Hybrid Attention": a window over the most recent 128 raw tokens supplies
+ * local context.  For query (n, j) at position t = q_pos[n, j] and head h:
+ *     keys  J = { k_cmp[n, idx[n, j, i]] : idx >= 0 }
+ *             ++ { k_raw[n, u - raw_base[n]] : max(0, t-W+1) <= u <= t }
+ *     out[n, j, h] = sum_{x in J} softmax_x(scale * q[n, j, h] . K_x) V_x
+ * one softmax over both parts (not de-duplicated); empty J gives 0 / -inf.
+ *   q [B, Tq, H, d]; k_cmp, v_cmp [B, N, d]; idx [B, Tq, k] int32 (-1 = skip)
+ *   k_raw, v_raw [B, T_raw, d] (row r holds token raw_base[n] + r)
+ *   raw_base [B], q_pos [B, Tq] int32
+ *   out [B, Tq, H, d] out_dtype;  lse [B, Tq, H] fp32 natural log (nullable)
+ * scale <= 0 selects 1/sqrt(d).  d in {64, 128}; 1 <= H <= 64; W >= 0.
+ * Indices >= N and window rows outside [0, T_raw) are skipped and flagged
+ * with CSA_FLAG_INDEX.  bf16 MMAs, fp32 softmax and accumulation.
+ * ------------------------------------------------------------------------ */
+csa_status csa_attend_workspace(int B, int Tq, int H, int d, int k, int W, size_t* bytes);
+csa_status csa_attend(const void* q, const void* k_cmp, const void* v_cmp, const int32_t* idx,
+                      const void* k_raw, const void* v_raw, const int32_t* raw_base,
+                      const int32_t* q_pos, int B, int Tq, int N, int T_raw, int H, int d,
+                      int k, int W, float scale, void* out, int out_dtype, float* lse,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
+ * HCA mode.  Octagono "Hybrid Attention: CSA and HCA" and the technical
+ * review, section 2.2: entries compressed every m' (= 128) tokens, attended
+ * densely with no selection, plus the same sliding window.  As csa_attend
+ * with J's first part = every visible entry b < min(N, floor((t+1)/m)).
+ * ------------------------------------------------------------------------ */
+csa_status hca_attend_workspace(int B, int Tq, int N, int H, int d, int W, size_t* bytes);
+csa_status hca_attend(const void* q, const void* k_cmp, const void* v_cmp,
+                      const void* k_raw, const void* v_raw, const int32_t* raw_base,
+                      const int32_t* q_pos, int B, int Tq, int N, int T_raw, int H, int d,
+                      int m, int W, float scale, void* out, int out_dtype, float* lse,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
+ * The whole CSA layer, steps (1) -> (2) -> (3) -> (4), enqueued on one stream.
+ * If g_k, g_v and g_i are all non-NULL, step (1) compresses x_k, x_v, x_i
+ * ([B, T, d], [B, T, d], [B, T, d_I]) at m into k_cmp, v_cmp, i_cmp
+ * ([B, N, .] bf16, N = T / m); if all three are NULL the caches are read as
+ * given (decode).  Steps (2)-(4) are csa_index_topk and csa_attend.
+ * ------------------------------------------------------------------------ */
+typedef struct csa_layer_args {
+    int B, Tq, N, m, H, d, H_I, d_I, k, W;
+    int T;                  /* raw tokens compressed (step 1 only)              */
+    int T_raw;              /* rows of the window buffer k_win / v_win          */
+    float scale;            /* <= 0: 1/sqrt(d)                                  */
+    const void *x_k, *x_v, *x_i;   /* raw streams for step (1), or NULL         */
+    const void *g_k, *g_v, *g_i;   /* gate logits for step (1), or NULL         */
+    void *k_cmp, *v_cmp, *i_cmp;   /* compressed caches (written by step 1)     */
+    const void *k_win, *v_win;     /* raw window buffer [B, T_raw, d]           */
+    const int32_t* raw_base;       /* [B]                                       */
+    const void* q;                 /* [B, Tq, H, d]                             */
+    const void* q_idx;             /* [B, Tq, H_I, d_I]                         */
+    const float* w;                /* [H_I]                                     */
+    const int32_t* q_pos;          /* [B, Tq]                                   */
+    int32_t* idx_out;              /* [B, Tq, k] or NULL (kept in workspace)    */
+    void* out;                     /* [B, Tq, H, d]                             */
+    int out_dtype;
+    float* lse;                    /* [B, Tq, H] or NULL                        */
+} csa_layer_args;
+
+csa_status csa_layer_workspace(const csa_layer_args* a, size_t* bytes);
+csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* stream);
+
+/* Test hook: the clock64 budget of every bounded device-side wait issued by
+ * later calls in this process (default ~2^31 cycles, about one second).
+ * cycles <= 0 restores the default. */
+void csa_set_wait_budget(long long cycles);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_H_ */

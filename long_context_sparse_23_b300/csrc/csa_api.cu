@@ -1,0 +1,406 @@
+// C ABI of the CSA library (declared in include/csa.h): argument checks that
+// run before anything is enqueued, workspace layout, and kernel dispatch.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/csa.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+long long g_wait_budget = 1LL << 31;  // clock64 cycles, about one second
+
+constexpr size_t kAlignWs = 256;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool al4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+inline csa_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return CSA_OK;
+  if (e == cudaErrorNotSupported) return CSA_ERR_UNSUPPORTED;
+  return CSA_ERR_CUDA;
+}
+
+inline csa_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) % kAlignWs) != 0) return CSA_ERR_WORKSPACE;
+  if (ws_bytes < need) return CSA_ERR_WORKSPACE;
+  return CSA_OK;
+}
+
+inline uint32_t* err_word(void* ws) { return static_cast<uint32_t*>(ws); }
+
+inline long long scores_ld(int N) { return (static_cast<long long>(N) + 3) / 4 * 4; }
+
+inline size_t scores_bytes(int B, int Tq, int N) {
+  return align_up(static_cast<size_t>(B) * Tq * scores_ld(N) * sizeof(float), kAlignWs);
+}
+
+bool hi_ok(int H_I) {
+  return H_I == 4 || H_I == 8 || H_I == 16 || H_I == 32 || H_I == 64 || H_I == 128;
+}
+bool di_ok(int d_I) { return d_I == 32 || d_I == 64 || d_I == 128; }
+
+csa_status check_index_args(const void* q_idx, const void* k_idx, const float* w,
+                            const int32_t* q_pos, int B, int Tq, int N, int H_I, int d_I, int m) {
+  if (!q_idx || !k_idx || !w || !q_pos) return CSA_ERR_INVALID;
+  if (!al16(q_idx) || !al16(k_idx) || !al4(w) || !al4(q_pos)) return CSA_ERR_INVALID;
+  if (B <= 0 || Tq <= 0 || N <= 0 || H_I <= 0 || d_I <= 0 || m <= 0) return CSA_ERR_INVALID;
+  if (!hi_ok(H_I) || !di_ok(d_I)) return CSA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Tq * H_I >= (1LL << 31)) return CSA_ERR_UNSUPPORTED;
+  return CSA_OK;
+}
+
+csa_status check_topk_shape(const int32_t* q_pos, int B, int Tq, int N, int m, int k) {
+  if (!q_pos || !al4(q_pos)) return CSA_ERR_INVALID;
+  if (B <= 0 || Tq <= 0 || N <= 0 || m <= 0 || k <= 0) return CSA_ERR_INVALID;
+  if (k > 4096) return CSA_ERR_UNSUPPORTED;
+  if (!csa::topk_supported(N)) return CSA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Tq >= (1LL << 31)) return CSA_ERR_UNSUPPORTED;
+  return CSA_OK;
+}
+
+csa_status check_topk_args(const int32_t* q_pos, int B, int Tq, int N, int m, int k,
+                           const int32_t* idx_out, const float* score_out) {
+  if (!idx_out || !al4(idx_out) || (score_out && !al4(score_out))) return CSA_ERR_INVALID;
+  return check_topk_shape(q_pos, B, Tq, N, m, k);
+}
+
+csa_status check_attend_args(const void* q, const void* k_cmp, const void* v_cmp, const void* k_raw,
+                             const void* v_raw, const int32_t* raw_base, const int32_t* q_pos,
+                             int B, int Tq, int N, int T_raw, int H, int d, int W, const void* out,
+                             int out_dtype, const float* lse) {
+  if (!q || !q_pos || !out) return CSA_ERR_INVALID;
+  if (B <= 0 || Tq <= 0 || N < 0 || T_raw < 0 || H <= 0 || d <= 0 || W < 0) return CSA_ERR_INVALID;
+  if (N > 0 && (!k_cmp || !v_cmp)) return CSA_ERR_INVALID;
+  if (W > 0 && (!k_raw || !v_raw || !raw_base || T_raw <= 0)) return CSA_ERR_INVALID;
+  if (!al16(q) || !al16(out) || (k_cmp && !al16(k_cmp)) || (v_cmp && !al16(v_cmp)) ||
+      (k_raw && !al16(k_raw)) || (v_raw && !al16(v_raw)) || !al4(q_pos) ||
+      (raw_base && !al4(raw_base)) || (lse && !al4(lse)))
+    return CSA_ERR_INVALID;
+  if (out_dtype != CSA_BF16 && out_dtype != CSA_F32) return CSA_ERR_INVALID;
+  if (d != 64 && d != 128) return CSA_ERR_UNSUPPORTED;
+  if (H > 64) return CSA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Tq >= 65536LL * 1024) return CSA_ERR_UNSUPPORTED;
+  return CSA_OK;
+}
+
+size_t attend_part_bytes(int B, int Tq, int n_keys_max, int H, int d) {
+  const csa::AttendPlan p = csa::plan_attend(Tq, static_cast<long long>(B) * Tq, n_keys_max, H, d);
+  return align_up(p.part_bytes, kAlignWs);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* csa_status_string(int s) {
+  switch (s) {
+    case CSA_OK: return "CSA_OK";
+    case CSA_ERR_INVALID: return "CSA_ERR_INVALID";
+    case CSA_ERR_UNSUPPORTED: return "CSA_ERR_UNSUPPORTED";
+    case CSA_ERR_WORKSPACE: return "CSA_ERR_WORKSPACE";
+    case CSA_ERR_CUDA: return "CSA_ERR_CUDA";
+    case CSA_ERR_TIMEOUT: return "CSA_ERR_TIMEOUT";
+    case CSA_ERR_DEVICE_INDEX: return "CSA_ERR_DEVICE_INDEX";
+    default: return "CSA_ERR_UNKNOWN";
+  }
+}
+
+int csa_version(void) { return 100; }
+
+void csa_set_wait_budget(long long cycles) { g_wait_budget = cycles > 0 ? cycles : (1LL << 31); }
+
+csa_status csa_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES) != CSA_OK) return CSA_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(ws, 0, CSA_WS_HEADER_BYTES, static_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_check_error(const void* ws, uint32_t* flags, int clear, void* stream) {
+  if (check_ws(ws, CSA_WS_HEADER_BYTES, CSA_WS_HEADER_BYTES) != CSA_OK) return CSA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t f = 0;
+  cudaError_t e = cudaMemcpyAsync(&f, ws, sizeof(f), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(const_cast<void*>(ws), 0, sizeof(f), s);
+  if (e == cudaSuccess && clear) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return CSA_ERR_CUDA;
+  if (flags) *flags = f;
+  if (f & CSA_FLAG_TIMEOUT) return CSA_ERR_TIMEOUT;
+  if (f & CSA_FLAG_INDEX) return CSA_ERR_DEVICE_INDEX;
+  return CSA_OK;
+}
+
+// ---------------------------------------------------------------- (1)
+csa_status csa_compress(int n_streams, const void* const* x, const void* const* g, void* const* out,
+                        const int* D, int B, int T, int m, int out_dtype, void* stream) {
+  if (n_streams < 1 || n_streams > 3 || !x || !g || !out || !D) return CSA_ERR_INVALID;
+  if (B <= 0 || T < 0 || m < 1 || m > 4096) return CSA_ERR_INVALID;
+  if (out_dtype != CSA_BF16 && out_dtype != CSA_F32) return CSA_ERR_INVALID;
+  csa::CompressArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int i = 0; i < n_streams; ++i) {
+    if (!x[i] || !g[i] || !out[i]) return CSA_ERR_INVALID;
+    if (!al16(x[i]) || !al16(g[i]) || !al16(out[i])) return CSA_ERR_INVALID;
+    if (D[i] <= 0 || D[i] % 8 != 0 || D[i] > 512) return CSA_ERR_INVALID;
+    a.x[i] = x[i];
+    a.g[i] = g[i];
+    a.out[i] = out[i];
+    a.D[i] = D[i];
+  }
+  a.n_streams = n_streams;
+  a.B = B;
+  a.T = T;
+  a.m = m;
+  a.out_f32 = out_dtype == CSA_F32;
+  if (T / m == 0) return CSA_OK;
+  return cuda_status(csa::launch_compress(a, static_cast<cudaStream_t>(stream)));
+}
+
+// ---------------------------------------------------------------- (2)
+csa_status csa_index_scores(const void* q_idx, const void* k_idx, const float* w,
+                            const int32_t* q_pos, int B, int Tq, int N, int H_I, int d_I, int m,
+                            float* scores, int64_t ld_scores, void* ws, size_t ws_bytes,
+                            void* stream) {
+  csa_status st = check_index_args(q_idx, k_idx, w, q_pos, B, Tq, N, H_I, d_I, m);
+  if (st != CSA_OK) return st;
+  if (!scores || !al16(scores) || ld_scores < N || ld_scores % 4 != 0) return CSA_ERR_INVALID;
+  st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES);
+  if (st != CSA_OK) return st;
+  csa::IndexerArgs a{q_idx, k_idx, w, q_pos, scores, ld_scores, B, Tq, N, H_I, d_I, m,
+                     err_word(ws), g_wait_budget};
+  return cuda_status(csa::launch_indexer(a, static_cast<cudaStream_t>(stream)));
+}
+
+// ---------------------------------------------------------------- (3)
+csa_status csa_topk(const float* scores, int64_t ld_scores, const int32_t* q_pos, int B, int Tq,
+                    int N, int m, int k, int32_t* idx_out, float* score_out, void* ws,
+                    size_t ws_bytes, void* stream) {
+  csa_status st = check_topk_args(q_pos, B, Tq, N, m, k, idx_out, score_out);
+  if (st != CSA_OK) return st;
+  if (!scores || !al16(scores) || ld_scores < N || ld_scores % 4 != 0) return CSA_ERR_INVALID;
+  st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES);
+  if (st != CSA_OK) return st;
+  csa::TopkArgs a{scores, ld_scores, q_pos, B, Tq, N, m, k, idx_out, score_out};
+  return cuda_status(csa::launch_topk(a, static_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_index_topk_workspace(int B, int Tq, int N, int H_I, int d_I, int k, size_t* bytes) {
+  (void)H_I;
+  (void)d_I;
+  (void)k;
+  if (!bytes || B <= 0 || Tq <= 0 || N <= 0) return CSA_ERR_INVALID;
+  *bytes = CSA_WS_HEADER_BYTES + scores_bytes(B, Tq, N);
+  return CSA_OK;
+}
+
+csa_status csa_index_topk(const void* q_idx, const void* k_idx, const float* w,
+                          const int32_t* q_pos, int B, int Tq, int N, int H_I, int d_I, int m,
+                          int k, int32_t* idx_out, float* score_out, void* ws, size_t ws_bytes,
+                          void* stream) {
+  csa_status st = check_index_args(q_idx, k_idx, w, q_pos, B, Tq, N, H_I, d_I, m);
+  if (st != CSA_OK) return st;
+  st = check_topk_args(q_pos, B, Tq, N, m, k, idx_out, score_out);
+  if (st != CSA_OK) return st;
+  size_t need = 0;
+  csa_index_topk_workspace(B, Tq, N, H_I, d_I, k, &need);
+  st = check_ws(ws, ws_bytes, need);
+  if (st != CSA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* S = reinterpret_cast<float*>(static_cast<char*>(ws) + CSA_WS_HEADER_BYTES);
+  const long long ld = scores_ld(N);
+  csa::IndexerArgs ia{q_idx, k_idx, w, q_pos, S, ld, B, Tq, N, H_I, d_I, m, err_word(ws), g_wait_budget};
+  st = cuda_status(csa::launch_indexer(ia, s));
+  if (st != CSA_OK) return st;
+  csa::TopkArgs ta{S, ld, q_pos, B, Tq, N, m, k, idx_out, score_out};
+  return cuda_status(csa::launch_topk(ta, s));
+}
+
+// ---------------------------------------------------------------- (4)
+csa_status csa_attend_workspace(int B, int Tq, int H, int d, int k, int W, size_t* bytes) {
+  if (!bytes || B <= 0 || Tq <= 0 || H <= 0 || d <= 0 || k < 0 || W < 0) return CSA_ERR_INVALID;
+  *bytes = CSA_WS_HEADER_BYTES + attend_part_bytes(B, Tq, k + W, H, d);
+  return CSA_OK;
+}
+
+static csa_status attend_common(const void* q, const void* k_cmp, const void* v_cmp,
+                                const int32_t* idx, const void* k_raw, const void* v_raw,
+                                const int32_t* raw_base, const int32_t* q_pos, int B, int Tq, int N,
+                                int T_raw, int H, int d, int k, int m, int W, float scale, void* out,
+                                int out_dtype, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  const int n_keys_max = (idx ? k : N) + W;
+  const size_t need = CSA_WS_HEADER_BYTES + attend_part_bytes(B, Tq, n_keys_max, H, d);
+  csa_status st = check_ws(ws, ws_bytes, need);
+  if (st != CSA_OK) return st;
+  const csa::AttendPlan plan = csa::plan_attend(Tq, static_cast<long long>(B) * Tq, n_keys_max, H, d);
+  csa::AttendArgs a;
+  a.q = q;
+  a.k_cmp = k_cmp;
+  a.v_cmp = v_cmp;
+  a.idx = idx;
+  a.k_raw = k_raw;
+  a.v_raw = v_raw;
+  a.raw_base = raw_base;
+  a.q_pos = q_pos;
+  a.B = B;
+  a.Tq = Tq;
+  a.N = N;
+  a.T_raw = T_raw;
+  a.H = H;
+  a.d = d;
+  a.k = k;
+  a.W = W;
+  a.m = m;
+  a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(d));
+  a.out = out;
+  a.out_f32 = out_dtype == CSA_F32;
+  a.lse = lse;
+  a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + CSA_WS_HEADER_BYTES);
+  a.errw = err_word(ws);
+  return cuda_status(csa::launch_attend(a, plan, static_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_attend(const void* q, const void* k_cmp, const void* v_cmp, const int32_t* idx,
+                      const void* k_raw, const void* v_raw, const int32_t* raw_base,
+                      const int32_t* q_pos, int B, int Tq, int N, int T_raw, int H, int d, int k,
+                      int W, float scale, void* out, int out_dtype, float* lse, void* ws,
+                      size_t ws_bytes, void* stream) {
+  csa_status st = check_attend_args(q, k_cmp, v_cmp, k_raw, v_raw, raw_base, q_pos, B, Tq, N, T_raw,
+                                    H, d, W, out, out_dtype, lse);
+  if (st != CSA_OK) return st;
+  if (k < 0 || (k > 0 && (!idx || !al4(idx)))) return CSA_ERR_INVALID;
+  if (k > 0 && N <= 0) return CSA_ERR_INVALID;
+  // k == 0 leaves only the window; any non-null pointer keeps the call in CSA
+  // mode (the index list is empty and never read)
+  return attend_common(q, k_cmp, v_cmp, idx ? idx : q_pos, k_raw,
+                       v_raw, raw_base, q_pos, B, Tq, N, T_raw, H, d, k, 1, W, scale, out,
+                       out_dtype, lse, ws, ws_bytes, stream);
+}
+
+csa_status hca_attend_workspace(int B, int Tq, int N, int H, int d, int W, size_t* bytes) {
+  if (!bytes || B <= 0 || Tq <= 0 || N < 0 || H <= 0 || d <= 0 || W < 0) return CSA_ERR_INVALID;
+  *bytes = CSA_WS_HEADER_BYTES + attend_part_bytes(B, Tq, N + W, H, d);
+  return CSA_OK;
+}
+
+csa_status hca_attend(const void* q, const void* k_cmp, const void* v_cmp, const void* k_raw,
+                      const void* v_raw, const int32_t* raw_base, const int32_t* q_pos, int B,
+                      int Tq, int N, int T_raw, int H, int d, int m, int W, float scale, void* out,
+                      int out_dtype, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  csa_status st = check_attend_args(q, k_cmp, v_cmp, k_raw, v_raw, raw_base, q_pos, B, Tq, N, T_raw,
+                                    H, d, W, out, out_dtype, lse);
+  if (st != CSA_OK) return st;
+  if (m <= 0) return CSA_ERR_INVALID;
+  return attend_common(q, k_cmp, v_cmp, nullptr, k_raw, v_raw, raw_base, q_pos, B, Tq, N, T_raw, H,
+                       d, 0, m, W, scale, out, out_dtype, lse, ws, ws_bytes, stream);
+}
+
+// ---------------------------------------------------------------- layer
+csa_status csa_layer_workspace(const csa_layer_args* a, size_t* bytes) {
+  if (!a || !bytes || a->B <= 0 || a->Tq <= 0 || a->N <= 0 || a->k <= 0) return CSA_ERR_INVALID;
+  size_t total = CSA_WS_HEADER_BYTES + scores_bytes(a->B, a->Tq, a->N);
+  if (!a->idx_out) total += align_up(static_cast<size_t>(a->B) * a->Tq * a->k * 4, kAlignWs);
+  total += attend_part_bytes(a->B, a->Tq, a->k + a->W, a->H, a->d);
+  *bytes = total;
+  return CSA_OK;
+}
+
+csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* stream) {
+  if (!a) return CSA_ERR_INVALID;
+  const bool do_compress = a->g_k || a->g_v || a->g_i;
+  if (do_compress) {
+    if (!a->g_k || !a->g_v || !a->g_i || !a->x_k || !a->x_v || !a->x_i) return CSA_ERR_INVALID;
+    if (a->m <= 0 || a->T < 0 || a->T / a->m != a->N) return CSA_ERR_INVALID;
+    if (!a->k_cmp || !a->v_cmp || !a->i_cmp) return CSA_ERR_INVALID;
+  }
+  csa_status st = check_index_args(a->q_idx, a->i_cmp, a->w, a->q_pos, a->B, a->Tq, a->N, a->H_I,
+                                   a->d_I, a->m);
+  if (st != CSA_OK) return st;
+  int32_t* idx = a->idx_out;
+  st = idx ? check_topk_args(a->q_pos, a->B, a->Tq, a->N, a->m, a->k, idx, nullptr)
+           : check_topk_shape(a->q_pos, a->B, a->Tq, a->N, a->m, a->k);
+  if (st != CSA_OK) return st;
+  st = check_attend_args(a->q, a->k_cmp, a->v_cmp, a->k_win, a->v_win, a->raw_base, a->q_pos, a->B,
+                         a->Tq, a->N, a->T_raw, a->H, a->d, a->W, a->out, a->out_dtype, a->lse);
+  if (st != CSA_OK) return st;
+  if (do_compress && (a->d % 8 != 0 || a->d_I % 8 != 0 || !al16(a->x_k) || !al16(a->x_v) ||
+                      !al16(a->x_i) || !al16(a->g_k) || !al16(a->g_v) || !al16(a->g_i) ||
+                      !al16(a->k_cmp) || !al16(a->v_cmp) || !al16(a->i_cmp)))
+    return CSA_ERR_INVALID;
+  size_t need = 0;
+  csa_layer_workspace(a, &need);
+  st = check_ws(ws, ws_bytes, need);
+  if (st != CSA_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(ws) + CSA_WS_HEADER_BYTES;
+  float* S = reinterpret_cast<float*>(base);
+  base += scores_bytes(a->B, a->Tq, a->N);
+  if (!idx) {
+    idx = reinterpret_cast<int32_t*>(base);
+    base += align_up(static_cast<size_t>(a->B) * a->Tq * a->k * 4, kAlignWs);
+  }
+  if (do_compress) {
+    csa::CompressArgs c;
+    std::memset(&c, 0, sizeof(c));
+    c.x[0] = a->x_k;
+    c.x[1] = a->x_v;
+    c.x[2] = a->x_i;
+    c.g[0] = a->g_k;
+    c.g[1] = a->g_v;
+    c.g[2] = a->g_i;
+    c.out[0] = a->k_cmp;
+    c.out[1] = a->v_cmp;
+    c.out[2] = a->i_cmp;
+    c.D[0] = a->d;
+    c.D[1] = a->d;
+    c.D[2] = a->d_I;
+    c.n_streams = 3;
+    c.B = a->B;
+    c.T = a->T;
+    c.m = a->m;
+    c.out_f32 = 0;
+    st = cuda_status(csa::launch_compress(c, s));
+    if (st != CSA_OK) return st;
+  }
+  const long long ld = scores_ld(a->N);
+  csa::IndexerArgs ia{a->q_idx, a->i_cmp, a->w, a->q_pos, S, ld, a->B, a->Tq, a->N, a->H_I, a->d_I,
+                      a->m, err_word(ws), g_wait_budget};
+  st = cuda_status(csa::launch_indexer(ia, s));
+  if (st != CSA_OK) return st;
+  csa::TopkArgs ta{S, ld, a->q_pos, a->B, a->Tq, a->N, a->m, a->k, idx, nullptr};
+  st = cuda_status(csa::launch_topk(ta, s));
+  if (st != CSA_OK) return st;
+  const int n_keys_max = a->k + a->W;
+  const csa::AttendPlan plan =
+      csa::plan_attend(a->Tq, static_cast<long long>(a->B) * a->Tq, n_keys_max, a->H, a->d);
+  csa::AttendArgs at;
+  at.q = a->q;
+  at.k_cmp = a->k_cmp;
+  at.v_cmp = a->v_cmp;
+  at.idx = idx;
+  at.k_raw = a->k_win;
+  at.v_raw = a->v_win;
+  at.raw_base = a->raw_base;
+  at.q_pos = a->q_pos;
+  at.B = a->B;
+  at.Tq = a->Tq;
+  at.N = a->N;
+  at.T_raw = a->T_raw;
+  at.H = a->H;
+  at.d = a->d;
+  at.k = a->k;
+  at.W = a->W;
+  at.m = a->m;
+  at.scale = a->scale > 0.f ? a->scale : 1.0f / std::sqrt(static_cast<float>(a->d));
+  at.out = a->out;
+  at.out_f32 = a->out_dtype == CSA_F32;
+  at.lse = a->lse;
+  at.part = reinterpret_cast<float*>(base);
+  at.errw = err_word(ws);
+  return cuda_status(csa::launch_attend(at, plan, s));
+}
+
+}  // extern "C"

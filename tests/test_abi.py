@@ -1,0 +1,125 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/csa.h declares, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from long_context_sparse_23_b300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "csa.h")
+
+A16 = 1 << 20  # a fake, 16-byte aligned "device pointer" (never dereferenced on these paths)
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|csa_status|int|void)\s+(\w+)\s*\(", src, re.M)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from long_context_sparse_23_b300 import build
+    build.build()
+    return _lib.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert len(names) >= 15, names
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(_lib.SIGNATURES), set(names) ^ set(_lib.SIGNATURES)
+
+
+def test_status_strings_and_version(L):
+    for code, name in enumerate(["CSA_OK", "CSA_ERR_INVALID", "CSA_ERR_UNSUPPORTED", "CSA_ERR_WORKSPACE",
+                                 "CSA_ERR_CUDA", "CSA_ERR_TIMEOUT", "CSA_ERR_DEVICE_INDEX"]):
+        assert L.csa_status_string(code).decode() == name
+    assert L.csa_status_string(99).decode() == "CSA_ERR_UNKNOWN"
+    assert L.csa_version() >= 100
+
+
+def test_workspace_sizes(L):
+    need = ctypes.c_size_t(0)
+    assert L.csa_index_topk_workspace(4, 1, 262144, 64, 128, 1024, ctypes.byref(need)) == 0
+    assert need.value == 256 + 4 * 262144 * 4
+    assert L.csa_index_topk_workspace(1, 1, 5, 64, 128, 4, ctypes.byref(need)) == 0
+    assert need.value == 256 + 256                # 8 floats rounded up to 256 bytes
+    assert L.csa_attend_workspace(64, 1, 64, 128, 1024, 128, ctypes.byref(need)) == 0
+    splits = (1152 // 64 + 3) // 4                 # 4 tiles of 64 keys per split
+    assert need.value == 256 + 64 * splits * 64 * 129 * 4
+    assert L.csa_attend_workspace(1, 8192, 16, 128, 1024, 128, ctypes.byref(need)) == 0
+    assert need.value == 256                       # prefill: no split partials
+    # batch-invariant split plan: per-sequence bytes scale linearly with B
+    a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    L.hca_attend_workspace(1, 1, 8192, 64, 128, 128, ctypes.byref(a))
+    L.hca_attend_workspace(8, 1, 8192, 64, 128, 128, ctypes.byref(b))
+    assert b.value - 256 == 8 * (a.value - 256)
+    assert L.csa_attend_workspace(0, 1, 64, 128, 16, 8, ctypes.byref(need)) == _lib.CSA_ERR_INVALID
+
+
+def test_validation_before_any_launch(L):
+    P3 = ctypes.c_void_p * 3
+    D = (ctypes.c_int * 3)(64, 64, 32)
+    ok = P3(A16, A16, A16)
+    # compress: stream count, null pointer, misalignment, channel count, dtype
+    assert L.csa_compress(0, ok, ok, ok, D, 1, 256, 4, 0, None) == _lib.CSA_ERR_INVALID
+    assert L.csa_compress(1, P3(None, A16, A16), ok, ok, D, 1, 256, 4, 0, None) == _lib.CSA_ERR_INVALID
+    assert L.csa_compress(1, P3(A16 + 2, 0, 0), ok, ok, D, 1, 256, 4, 0, None) == _lib.CSA_ERR_INVALID
+    assert L.csa_compress(1, ok, ok, ok, (ctypes.c_int * 3)(12, 0, 0), 1, 256, 4, 0, None) == _lib.CSA_ERR_INVALID
+    assert L.csa_compress(1, ok, ok, ok, D, 1, 256, 4, 7, None) == _lib.CSA_ERR_INVALID
+    assert L.csa_compress(1, ok, ok, ok, D, 1, 256, 0, 0, None) == _lib.CSA_ERR_INVALID
+    # indexer: unsupported head count / width, bad leading dimension, workspace
+    args = [A16, A16, A16, A16, 1, 4, 64, 64, 128, 4, A16, 64, A16, 256, None]
+    a = list(args); a[7] = 48
+    assert L.csa_index_scores(*a) == _lib.CSA_ERR_UNSUPPORTED
+    a = list(args); a[8] = 96
+    assert L.csa_index_scores(*a) == _lib.CSA_ERR_UNSUPPORTED
+    a = list(args); a[11] = 62
+    assert L.csa_index_scores(*a) == _lib.CSA_ERR_INVALID
+    a = list(args); a[13] = 100
+    assert L.csa_index_scores(*a) == _lib.CSA_ERR_WORKSPACE
+    a = list(args); a[12] = A16 + 16
+    assert L.csa_index_scores(*a) == _lib.CSA_ERR_WORKSPACE
+    a = list(args); a[0] = None
+    assert L.csa_index_scores(*a) == _lib.CSA_ERR_INVALID
+    # top-k: k range, too many entries
+    targs = [A16, 64, A16, 1, 1, 64, 4, 16, A16, None, A16, 256, None]
+    t = list(targs); t[7] = 5000
+    assert L.csa_topk(*t) == _lib.CSA_ERR_UNSUPPORTED
+    t = list(targs); t[5] = 16 * 49152 + 1; t[1] = 16 * 49152 + 4
+    assert L.csa_topk(*t) == _lib.CSA_ERR_UNSUPPORTED
+    t = list(targs); t[7] = 0
+    assert L.csa_topk(*t) == _lib.CSA_ERR_INVALID
+    # attention: head width, head count, window buffer, workspace
+    at = [A16, A16, A16, A16, A16, A16, A16, A16, 1, 1, 64, 256, 64, 128, 16, 32, 0.0, A16, 0, None,
+          A16, 1 << 20, None]
+    x = list(at); x[13] = 96
+    assert L.csa_attend(*x) == _lib.CSA_ERR_UNSUPPORTED
+    x = list(at); x[12] = 65
+    assert L.csa_attend(*x) == _lib.CSA_ERR_UNSUPPORTED
+    x = list(at); x[4] = None
+    assert L.csa_attend(*x) == _lib.CSA_ERR_INVALID
+    x = list(at); x[21] = 100
+    assert L.csa_attend(*x) == _lib.CSA_ERR_WORKSPACE
+    x = list(at); x[18] = 3
+    assert L.csa_attend(*x) == _lib.CSA_ERR_INVALID
+    # layer: missing struct, partial gate set
+    assert L.csa_layer(None, A16, 1 << 20, None) == _lib.CSA_ERR_INVALID
+    la = _lib.csa_layer_args()
+    la.g_k = A16
+    assert L.csa_layer(ctypes.byref(la), A16, 1 << 20, None) == _lib.CSA_ERR_INVALID
+    # workspace init / check with a bad pointer
+    assert L.csa_workspace_init(None, 1024, None) == _lib.CSA_ERR_WORKSPACE
+    assert L.csa_check_error(A16 + 8, None, 0, None) == _lib.CSA_ERR_WORKSPACE
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(ImportError):
+        _lib.lib()
