@@ -1,0 +1,415 @@
+"""Benchmark: CSA decode queries/s at 1M-token context (and 128K), with the
+dominant kernel's fraction of its roofline and the CPU oracle beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--all]
+
+One step = one pass of the decode hot path over one batch: Lightning-Indexer
+scores -> top-k -> window-merged sparse attention (+ split combine), for the
+B=4 sequences of the 1M-token workload (262144 compressed entries each, one
+query at position 1048575).  Steps are replayed from a CUDA graph; the device
+time is taken with CUDA events on the launching stream.  Under torchrun every
+rank runs its own replica (independent sequences: weak scaling, no data-path
+collective); the reported time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import csa_synth as S  # noqa: E402
+
+HEADLINE = "decode_1m"
+PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+# DRAM bytes per launch of the indexer on the 1M decode workload, from an ncu
+# capture (profiles/indexer_decode_1m.md); valid only for the source it was
+# measured on.
+TRAFFIC = {"indexer": {"src_sha": None, "bytes": None}}
+
+
+def _src_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "long_context_sparse_23_b300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 8:
+                continue
+            try:
+                sm.append(float(r[0]))
+                smax = float(r[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, r[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workload
+
+class DecodeStep:
+    """Device buffers and the three enqueue calls of one decode step."""
+
+    def __init__(self, name: str, device):
+        import long_context_sparse_23_b300 as csa
+        from long_context_sparse_23_b300 import _lib
+        self.csa, self.L = csa, _lib.lib()
+        self.wl = wl = S.WORKLOADS[name]
+        self.inp = S.make_inputs(wl, device)
+        B, Tq = self.inp["q_pos"].shape
+        self.B, self.Tq = B, Tq
+        self.ld = csa.scores_ld(wl.N)
+        self.scores = torch.empty(B, Tq, self.ld, dtype=torch.float32, device=device)
+        self.idx = torch.empty(B, Tq, wl.k, dtype=torch.int32, device=device)
+        self.out = torch.empty(B, Tq, wl.H, wl.d, dtype=torch.bfloat16, device=device)
+        need = ctypes.c_size_t(0)
+        self.L.csa_attend_workspace(B, Tq, wl.H, wl.d, wl.k, wl.W, ctypes.byref(need))
+        self.ws = csa.Workspace(need.value + (1 << 20), device)
+        self.st = torch.cuda.current_stream().cuda_stream
+
+    def indexer(self, st):
+        i, wl = self.inp, self.wl
+        r = self.L.csa_index_scores(i["q_idx"].data_ptr(), i["i_cmp"].data_ptr(), i["w"].data_ptr(),
+                                    i["q_pos"].data_ptr(), self.B, self.Tq, wl.N, wl.H_I, wl.d_I, wl.m,
+                                    self.scores.data_ptr(), self.ld, self.ws.ptr, self.ws.nbytes, st)
+        assert r == 0, r
+
+    def topk(self, st):
+        wl = self.wl
+        r = self.L.csa_topk(self.scores.data_ptr(), self.ld, self.inp["q_pos"].data_ptr(), self.B, self.Tq,
+                            wl.N, wl.m, wl.k, self.idx.data_ptr(), None, self.ws.ptr, self.ws.nbytes, st)
+        assert r == 0, r
+
+    def attend(self, st):
+        i, wl = self.inp, self.wl
+        r = self.L.csa_attend(i["q"].data_ptr(), i["k_cmp"].data_ptr(), i["v_cmp"].data_ptr(),
+                              self.idx.data_ptr(), i["k_raw"].data_ptr(), i["v_raw"].data_ptr(),
+                              i["raw_base"].data_ptr(), i["q_pos"].data_ptr(), self.B, self.Tq, wl.N,
+                              wl.raw_len, wl.H, wl.d, wl.k, wl.W, 0.0, self.out.data_ptr(), 0, None,
+                              self.ws.ptr, self.ws.nbytes, st)
+        assert r == 0, r
+
+    def step(self, st):
+        self.indexer(st)
+        self.topk(st)
+        self.attend(st)
+
+    def kernels_per_step(self):
+        """indexer + top-k + attention, + the split combine when keys are split"""
+        need = ctypes.c_size_t(0)
+        self.L.csa_attend_workspace(1, self.Tq, self.wl.H, self.wl.d, self.wl.k, self.wl.W, ctypes.byref(need))
+        combine = 1 if need.value > 256 else 0
+        return 3 + combine
+
+    # algorithmic work of the indexer launch (per visible entry: its d_I-wide bf16
+    # key read once + one fp32 score written; per query: its H_I x d_I bf16 queries)
+    def indexer_bytes(self):
+        wl = self.wl
+        n_vis = sum(min(wl.N, (int(t) + 1) // wl.m) for t in self.inp["q_pos"].flatten().tolist())
+        return n_vis * (wl.d_I * 2 + 4) + self.B * self.Tq * wl.H_I * wl.d_I * 2, n_vis
+
+
+def graph_of(fn, st_torch):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st_torch):
+        fn(st_torch.cuda_stream)
+    return g
+
+
+def time_graph(g, steps, warmup, stream):
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+        e1.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def stage_breakdown(ds: DecodeStep, steps: int, warmup: int, stream):
+    """Average device time of each stage (plain launches, CUDA events between
+    the stage calls on the launching stream)."""
+    names = ("indexer", "topk", "attend")
+    fns = (ds.indexer, ds.topk, ds.attend)
+    st = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            ds.step(st)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        for i in range(steps):
+            ev[i][0].record(stream)
+            for j, f in enumerate(fns):
+                f(st)
+                ev[i][j + 1].record(stream)
+        stream.synchronize()
+    return {n: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps
+            for j, n in enumerate(names)}
+
+
+def e2e_decode(ds: DecodeStep, steps: int, warmup: int):
+    """Queries/s through csa_layer with pinned host inputs (q, q_idx) copied in
+    and the output copied back every step; the caches stay resident."""
+    csa, wl = ds.csa, ds.wl
+    i = ds.inp
+    hq = i["q"].cpu().pin_memory()
+    hqi = i["q_idx"].cpu().pin_memory()
+    hout = torch.empty(ds.out.shape, dtype=ds.out.dtype).pin_memory()
+    dq, dqi = torch.empty_like(i["q"]), torch.empty_like(i["q_idx"])
+    a = csa.layer_args(B=ds.B, Tq=ds.Tq, N=wl.N, m=wl.m, H=wl.H, d=wl.d, H_I=wl.H_I, d_I=wl.d_I, k=wl.k,
+                       W=wl.W, T_raw=wl.raw_len, k_cmp=i["k_cmp"], v_cmp=i["v_cmp"], i_cmp=i["i_cmp"],
+                       k_win=i["k_raw"], v_win=i["v_raw"], raw_base=i["raw_base"], q=dq, q_idx=dqi,
+                       w=i["w"], q_pos=i["q_pos"], idx_out=ds.idx, out=ds.out)
+    need = ctypes.c_size_t(0)
+    ds.L.csa_layer_workspace(ctypes.byref(a), ctypes.byref(need))
+    ws = csa.Workspace(need.value)
+    st = torch.cuda.current_stream()
+
+    def one():
+        dq.copy_(hq, non_blocking=True)
+        dqi.copy_(hqi, non_blocking=True)
+        r = ds.L.csa_layer(ctypes.byref(a), ws.ptr, ws.nbytes, st.cuda_stream)
+        assert r == 0, r
+        hout.copy_(ds.out, non_blocking=True)
+        st.synchronize()
+
+    for _ in range(warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = (time.perf_counter() - t0) / steps
+    h2d = hq.numel() * 2 + hqi.numel() * 2
+    d2h = hout.numel() * 2
+    return ds.B * ds.Tq / dt, h2d, d2h
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_rate(name: str, budget_s: float, steps: int = 0, warmup: int = 0):
+    """The oracle on the host: queries/s on a bounded sample of the workload.
+
+    One query of sequence 0: indexer scores over its most recent ``n`` visible
+    entries, top-k of those scores, window-merged attention over the kept
+    entries.  With steps = 0 every sample is a whole query (n = n_vis) and
+    samples repeat until ``budget_s`` is spent; with steps = K each of the
+    W + K samples is sized so that they fit the budget together, and the rate
+    is scaled by n / n_vis (the indexer dominates the oracle's work).
+    Input generation is outside the timed calls."""
+    import numpy as np  # noqa: F401
+    import oracle as O
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([d.get("num_threads", 1) for d in threadpool_info()] + [1])
+    except Exception:  # pragma: no cover
+        threads = 1
+    threads = max(threads, torch.get_num_threads())  # the generator / oracle's torch ops
+    wl = S.WORKLOADS[name]
+    t = wl.q_positions[0]
+    n_vis = O.n_visible(t, wl.m, wl.N)
+    c = S.make_inputs(wl.replace(B=1), "cpu", only={"q", "q_idx", "w", "q_pos", "k_raw", "v_raw"})
+    q_bits, qi_bits = S.bf16_bits(c["q"]), S.bf16_bits(c["q_idx"])
+    kr_bits, vr_bits = S.bf16_bits(c["k_raw"]), S.bf16_bits(c["v_raw"])
+    w = c["w"].numpy()
+    rows = torch.arange(0, n_vis, dtype=torch.int64)
+    ki_bits = S.bf16_bits(S.rows_bf16(wl.seed, S.TID["i_cmp"], wl.N, wl.d_I, 0, rows))[None]
+    kc_bits = S.bf16_bits(S.rows_bf16(wl.seed, S.TID["k_cmp"], wl.N, wl.d, 0, rows))[None]
+    vc_bits = S.bf16_bits(S.rows_bf16(wl.seed, S.TID["v_cmp"], wl.N, wl.d, 0, rows))[None]
+    base = [wl.raw_base]
+
+    def sample(n):
+        # the oracle's own batched calls: (2)+(3) over the newest n entries, then (4)
+        t0 = time.perf_counter()
+        lo = n_vis - n
+        idx, _ = O.csa_index_topk(qi_bits, ki_bits[:, lo:], w, [[n * wl.m - 1]], wl.m, wl.k)
+        O.csa_attend(q_bits, kc_bits[:, lo:], vc_bits[:, lo:], idx, kr_bits, vr_bits, base, [[t]],
+                     wl.W, 1 / math.sqrt(wl.d))
+        return time.perf_counter() - t0
+
+    if steps <= 0:
+        done, tot = 0, 0.0
+        while done == 0 or tot < budget_s:
+            tot += sample(n_vis)
+            done += 1
+        return done / tot, threads, (f"{done} whole queries of {name} (sequence 0, t={t}, "
+                                     f"{n_vis} visible entries), inputs generated outside the timing")
+    probe = sample(min(n_vis, 16384))
+    per_step = budget_s / (steps + warmup)
+    n = int(min(n_vis, max(1024, min(n_vis, 16384) * per_step / max(probe, 1e-6))))
+    for _ in range(warmup):
+        sample(n)
+    tot = sum(sample(n) for _ in range(steps))
+    return steps * (n / n_vis) / tot, threads, (f"per step: 1 query of {name} with its indexer over the most "
+                                                 f"recent {n} of {n_vis} visible entries, scaled by n/n_vis")
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--all", action="store_true", help="also time the 8K prefill and the 1M HCA decode")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = S.WORKLOADS[HEADLINE]
+    metric = "CSA decode queries/s @1M ctx (B=4, 262144 compressed entries, top-1024, W=128)"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        rate, threads, what = oracle_rate(HEADLINE, budget_s=90.0, steps=args.steps, warmup=args.warmup)
+        line = {"impl": "reference", "metric": metric, "value": rate, "unit": "queries/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / rate,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": HEADLINE},
+                "cpu_baseline": {"value": rate, "unit": "queries/s", "cores": threads, "kind": "oracle", "sample": what},
+                "e2e": {"value": rate, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+
+    ds = DecodeStep(HEADLINE, dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        ds.step(stream.cuda_stream)      # first calls outside capture (one-time set-up)
+        stream.synchronize()
+        g_step = graph_of(ds.step, stream)
+    assert ds.ws.check_error() == 0
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clk = ClockSampler(local)
+    clk.start()
+    ms = time_graph(g_step, args.steps, args.warmup, stream)
+    clocks = clk.stop()
+    stages = stage_breakdown(ds, max(20, min(args.steps, 400)), 5, stream)
+    ms_idx = stages["indexer"]
+    torch.cuda.synchronize()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+        ms = float(t.item())
+    qps = ds.B * ds.Tq * world / (ms * 1e-3)
+
+    launches = args.steps * ds.kernels_per_step()
+    e2e_qps, h2d, d2h = e2e_decode(ds, max(20, min(args.steps, 500)), 10)
+
+    peaks, src = _peaks()
+    ibytes, n_vis = ds.indexer_bytes()
+    achieved = ibytes / (ms_idx * 1e-3) / 1e9
+    sha = _src_sha("indexer.cu", "common.cuh")
+    traffic = TRAFFIC["indexer"]["bytes"] if TRAFFIC["indexer"]["src_sha"] == sha else None
+    roof = {"kernel": "indexer_kernel (tcgen05)", "bound": "hbm", "achieved": round(achieved, 1),
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": traffic, "algorithmic_bytes": ibytes, "launch_us": round(ms_idx * 1e3, 2),
+            "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.4 TB/s"}
+
+    extra = {}
+    del ds, g_step
+    torch.cuda.empty_cache()
+    ds2 = DecodeStep("decode_128k", dev)
+    with torch.cuda.stream(stream):
+        ds2.step(stream.cuda_stream)
+        stream.synchronize()
+        g2 = graph_of(ds2.step, stream)
+    ms2 = time_graph(g2, max(10, args.steps // 4), 10, stream)
+    extra["decode_128k"] = {"queries_per_s": ds2.B * ds2.Tq / (ms2 * 1e-3), "ms_per_step": ms2}
+    del ds2, g2
+    torch.cuda.empty_cache()
+
+    line = {"metric": metric, "value": qps, "unit": "queries/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": HEADLINE, "B": wl.B, "context": wl.T, "entries": wl.N, "m": wl.m,
+                       "H": wl.H, "d": wl.d, "H_I": wl.H_I, "d_I": wl.d_I, "k": wl.k, "W": wl.W,
+                       "l2": "inputs exceed L2: 268 MB of indexer keys streamed per step",
+                       "launch": "CUDA graph replay of csa_index_scores + csa_topk + csa_attend"},
+            "clocks": clocks, "gpu_launches": launches, "roofline": roof,
+            "e2e": {"value": e2e_qps, "unit": "queries/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "stages_ms": {k: round(v, 5) for k, v in stages.items()}, "also": extra}
+    if rank == 0:
+        rate, threads, what = oracle_rate(HEADLINE, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": rate, "unit": "queries/s", "cores": threads, "kind": "oracle", "sample": what}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -390,8 +390,7 @@ cudaError_t launch_impl(const AttendArgs& a, const AttendPlan& p, cudaStream_t s
     const size_t need = 4 * 16 * D * 4 + 2 * 4 * 16 * 4;
     smem = smem > need ? smem : need;
   }
-  cudaError_t e = cudaFuncSetAttribute(attend_kernel<D, HG>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dyn_smem<attend_kernel<D, HG>>(static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long nq = static_cast<long long>(a.B) * a.Tq;
   dim3 grid(p.nsplit, static_cast<unsigned>(nq));

@@ -245,4 +245,18 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   return r;
 }
 
+// Raise a kernel's dynamic shared-memory limit, once per device and size:
+// later calls (for example inside a CUDA-graph capture) touch no driver state.
+template <auto Kern>
+inline cudaError_t ensure_dyn_smem(int bytes) {
+  static int done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev] >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = bytes;
+  return e;
+}
+
 }  // namespace csa

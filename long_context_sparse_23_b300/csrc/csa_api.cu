@@ -139,23 +139,25 @@ csa_status csa_compress(int n_streams, const void* const* x, const void* const* 
   if (n_streams < 1 || n_streams > 3 || !x || !g || !out || !D) return CSA_ERR_INVALID;
   if (B <= 0 || T < 0 || m < 1 || m > 4096) return CSA_ERR_INVALID;
   if (out_dtype != CSA_BF16 && out_dtype != CSA_F32) return CSA_ERR_INVALID;
+  const bool empty = T / m == 0;  // no complete block: nothing is read or written
   csa::CompressArgs a;
   std::memset(&a, 0, sizeof(a));
   for (int i = 0; i < n_streams; ++i) {
+    if (D[i] <= 0 || D[i] % 8 != 0 || D[i] > 512) return CSA_ERR_INVALID;
+    if (empty) continue;
     if (!x[i] || !g[i] || !out[i]) return CSA_ERR_INVALID;
     if (!al16(x[i]) || !al16(g[i]) || !al16(out[i])) return CSA_ERR_INVALID;
-    if (D[i] <= 0 || D[i] % 8 != 0 || D[i] > 512) return CSA_ERR_INVALID;
     a.x[i] = x[i];
     a.g[i] = g[i];
     a.out[i] = out[i];
     a.D[i] = D[i];
   }
+  if (empty) return CSA_OK;
   a.n_streams = n_streams;
   a.B = B;
   a.T = T;
   a.m = m;
   a.out_f32 = out_dtype == CSA_F32;
-  if (T / m == 0) return CSA_OK;
   return cuda_status(csa::launch_compress(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -339,8 +339,7 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
       return cudaErrorInvalidValue;
   }
   const size_t smem = 1024 + q_bytes + static_cast<size_t>(stages) * stage_bytes + sizeof(Bars);
-  cudaError_t e = cudaFuncSetAttribute(indexer_kernel<HI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = ensure_dyn_smem<indexer_kernel<HI>>(static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   indexer_kernel<HI><<<static_cast<unsigned>(items), kThreads, smem, s>>>(tmk, tmq, p);
   return cudaGetLastError();

@@ -262,13 +262,9 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
   chunk = (chunk + 31) & ~31;
   if (chunk > kMaxChunk) return cudaErrorNotSupported;
   const size_t smem = static_cast<size_t>(chunk > 0 ? chunk : 32) * 4;
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kMaxChunk * 4);
+  // (the cluster-size attribute was set once by max_cluster_for_device)
+  cudaError_t e = ensure_dyn_smem<topk_kernel>(kMaxChunk * 4);
   if (e != cudaSuccess) return e;
-  if (C > 8) {
-    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
   cudaLaunchConfig_t lc = {};
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;

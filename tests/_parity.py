@@ -2,8 +2,10 @@
 
 * compressed entries, fp32 output: |gpu - ref| <= 1e-3 * sum_j p_j |x_j| (the
   softmax-weighted magnitude, which bounds |ref| and avoids blow-ups where the
-  pooled value cancels);  bf16 output: within one bf16 ulp of the oracle's
-  bf16-rounded value everywhere and bit-equal on >= 99.9% of entries;
+  pooled value cancels);  bf16 output: the same budget plus the final
+  rounding, |gpu - ref| <= 1e-3 * sum_j p_j |x_j| + ulp_bf16(ref) / 2, and
+  bit-equal to the oracle's bf16 rounding on >= 99.9% of entries (one bf16 ulp
+  everywhere cannot hold where the pooled value cancels towards zero);
 * top-k indices: bit-exact, except at near-ties -- the valid counts match and
   every index in the symmetric difference has an oracle score within 1e-3 of
   the oracle's k-th largest score (relative);
@@ -36,15 +38,18 @@ def assert_compressed_f32(gpu: np.ndarray, ref: np.ndarray, scale: np.ndarray, w
     assert not bad.any(), f"{what}: {bad.sum()} entries beyond 1e-3 * sum p|x| (max rel {np.max(err / (scale + 1e-30)):.3g})"
 
 
-def assert_compressed_bf16(gpu_bits: np.ndarray, ref_f64: np.ndarray, what: str = "") -> None:
-    ref_bits = O.round_bf16(ref_f64)
-    g = gpu_bits.astype(np.int32)
-    r = ref_bits.astype(np.int32)
-    same_sign = (g >> 15) == (r >> 15)
-    ulps = np.where(same_sign, np.abs(g - r), np.abs((g & 0x7FFF) + (r & 0x7FFF)))
-    assert ulps.max() <= 1, f"{what}: {np.sum(ulps > 1)} entries more than one bf16 ulp away"
-    frac = np.mean(g == r)
-    assert frac >= 0.999, f"{what}: only {frac:.5f} bit-equal"
+def assert_compressed_bf16(gpu_bits: np.ndarray, ref_f64: np.ndarray, scale: np.ndarray, what: str = "") -> None:
+    g = O.bf16_to_f64(gpu_bits)
+    half_ulp = np.ldexp(1.0, np.frexp(np.abs(ref_f64))[1] - 9)
+    err = np.abs(g - ref_f64)
+    lim = 1e-3 * scale + half_ulp
+    bad = err > lim
+    if bad.any():
+        i = np.argmax(err / lim)
+        raise AssertionError(f"{what}: {bad.sum()} entries beyond 1e-3*sum p|x| + ulp/2 (worst: gpu "
+                             f"{g.flat[i]:.6g}, ref {ref_f64.flat[i]:.6g}, sum p|x| {scale.flat[i]:.4g})")
+    frac = np.mean(gpu_bits == O.round_bf16(ref_f64))
+    assert frac >= 0.999, f"{what}: only {frac:.5f} bit-equal to the oracle's bf16 rounding"
 
 
 def check_topk_near_tie(gpu_idx: np.ndarray, ref_idx: np.ndarray, ref_scores: np.ndarray, k: int,

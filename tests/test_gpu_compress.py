@@ -42,7 +42,7 @@ def test_compress_parity(B, T, m, Ds):
         if T // m == 0:
             continue
         assert_compressed_f32(out32[i].cpu().numpy(), ref, scale, f"stream {i}")
-        assert_compressed_bf16(bits(out16[i]), ref, f"stream {i}")
+        assert_compressed_bf16(bits(out16[i]), ref, scale, f"stream {i}")
         if m == 1:
             assert torch.equal(out16[i].cpu(), xc[i])
 
@@ -56,13 +56,14 @@ def test_compress_full_1m_hca_sampled():
     kc, vc = csa.csa_compress([inp["k_raw"], inp["v_raw"]], [inp["g_k"], inp["g_v"]], wl.m)
     torch.cuda.synchronize()
     rng = np.random.default_rng(3)
-    got_all, ref_all = [], []
+    got_all, ref_all, scale_all = [], [], []
     for b, blk in zip(rng.integers(0, wl.B, 256), rng.integers(0, wl.N, 256)):
         rows = torch.arange(blk * wl.m, (blk + 1) * wl.m, dtype=torch.int64)
         for name, gname, got in (("k_raw", "g_k", kc), ("v_raw", "g_v", vc)):
             x = O.bf16_to_f64(bits(S.rows_bf16(wl.seed, S.TID[name], wl.T, wl.d, int(b), rows)))
             g = O.bf16_to_f64(bits(S.rows_bf16(wl.seed, S.TID[gname], wl.T, wl.d, int(b), rows)))
             ref_all.append(O.compress(x, g, wl.m)[0])
+            scale_all.append(O.compress(np.abs(x), g, wl.m)[0])
             got_all.append(bits(got[b, blk]))
-    assert_compressed_bf16(np.stack(got_all), np.stack(ref_all), "1M HCA sampled entries")
+    assert_compressed_bf16(np.stack(got_all), np.stack(ref_all), np.stack(scale_all), "1M HCA sampled entries")
     del inp

@@ -39,8 +39,10 @@ def _prefill_case(name, rows=None):
     kc = O.csa_compress(c["k_raw"], c["g_k"], wl.m)
     vc = O.csa_compress(c["v_raw"], c["g_v"], wl.m)
     ic = O.csa_compress(c["i_raw"], c["g_i"], wl.m)
-    for ref, key in ((kc, "k_cmp"), (vc, "v_cmp"), (ic, "i_cmp")):
-        assert_compressed_bf16(bits(res[key]), ref, key)
+    for ref, key, xk, gk in ((kc, "k_cmp", "k_raw", "g_k"), (vc, "v_cmp", "v_raw", "g_v"),
+                             (ic, "i_cmp", "i_raw", "g_i")):
+        absx = O.round_bf16(np.abs(O.bf16_to_f64(c[xk])))  # |x| is exact in bf16
+        assert_compressed_bf16(bits(res[key]), ref, O.csa_compress(absx, c[gk], wl.m), key)
     # downstream steps on the oracle's own bf16 caches
     kcb, vcb, icb = O.round_bf16(kc), O.round_bf16(vc), O.round_bf16(ic)
     q64 = O.bf16_to_f64(c["q"])
