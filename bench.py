@@ -187,23 +187,35 @@ def time_graph(g, steps, warmup, stream):
 
 
 def stage_breakdown(ds: DecodeStep, steps: int, warmup: int, stream):
-    """Average device time of each stage (plain launches, CUDA events between
-    the stage calls on the launching stream)."""
+    """Average device time of each stage: plain launches with CUDA events
+    between the stage calls on the launching stream.  Each batch of steps is
+    queued behind a GPU-side sleep, so the host has enqueued the whole batch
+    before the first kernel starts and the events time kernels back to back
+    (not host launch latency)."""
     names = ("indexer", "topk", "attend")
     fns = (ds.indexer, ds.topk, ds.attend)
     st = stream.cuda_stream
+    batch = 50
+    tot = {n: 0.0 for n in names}
+    done = 0
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             ds.step(st)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
-        for i in range(steps):
-            ev[i][0].record(stream)
-            for j, f in enumerate(fns):
-                f(st)
-                ev[i][j + 1].record(stream)
-        stream.synchronize()
-    return {n: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps
-            for j, n in enumerate(names)}
+        while done < steps:
+            nb = min(batch, steps - done)
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nb)]
+            torch.cuda._sleep(20_000_000)       # ~10 ms of GPU time to queue behind
+            for i in range(nb):
+                ev[i][0].record(stream)
+                for j, f in enumerate(fns):
+                    f(st)
+                    ev[i][j + 1].record(stream)
+            stream.synchronize()
+            for i in range(nb):
+                for j, n in enumerate(names):
+                    tot[n] += ev[i][j].elapsed_time(ev[i][j + 1])
+            done += nb
+    return {n: tot[n] / steps for n in names}
 
 
 def e2e_decode(ds: DecodeStep, steps: int, warmup: int):
@@ -291,7 +303,8 @@ def oracle_rate(name: str, budget_s: float, steps: int = 0, warmup: int = 0):
             tot += sample(n_vis)
             done += 1
         return done / tot, threads, (f"{done} whole queries of {name} (sequence 0, t={t}, "
-                                     f"{n_vis} visible entries), inputs generated outside the timing")
+                                     f"{n_vis} visible entries), inputs generated outside the timing; "
+                                     f"host has {os.cpu_count()} logical CPUs")
     probe = sample(min(n_vis, 16384))
     per_step = budget_s / (steps + warmup)
     n = int(min(n_vis, max(1024, min(n_vis, 16384) * per_step / max(probe, 1e-6))))

@@ -27,45 +27,33 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kTile = 64;  // keys per tile
+constexpr int kMaxTilesPerCta = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-struct Src {
-  const char* k;
-  const char* v;
-  bool valid;
-  bool bad;  // an out-of-range index (flagged once, by the bias thread)
-};
-
-template <int D>
-__device__ __forceinline__ Src key_source(const AttendArgs& a, long long qi, int b, int t,
-                                          int n_c, int vk) {
-  Src s{static_cast<const char*>(a.k_cmp), static_cast<const char*>(a.v_cmp), false, false};
+// Row code of virtual key slot vk of query (qi, b, t): >= 0 a compressed row,
+// <= -2 the raw-window row (-code - 2), -1 no key.  *bad is set for an index
+// or window row outside its buffer (the slot is then skipped).
+__device__ __forceinline__ int slot_code(const AttendArgs& a, long long qi, int b, int t, int n_c,
+                                         int raw_base, int vk, bool* bad) {
   if (vk < n_c) {
     const int row = a.idx ? a.idx[qi * a.k + vk] : vk;
-    if (row < 0) return s;
+    if (row < 0) return -1;
     if (row >= a.N) {
-      s.bad = true;
-      return s;
+      *bad = true;
+      return -1;
     }
-    const size_t off = (static_cast<size_t>(b) * a.N + row) * D * 2;
-    s.k += off;
-    s.v += off;
-    s.valid = true;
-    return s;
+    return row;
   }
-  const int u = t - a.W + 1 + (vk - n_c);
-  if (vk - n_c >= a.W || u < 0) return s;
-  const int r = u - a.raw_base[b];
+  const int w = vk - n_c;
+  const int u = t - a.W + 1 + w;
+  if (w >= a.W || u < 0) return -1;
+  const int r = u - raw_base;
   if (r < 0 || r >= a.T_raw) {
-    s.bad = true;
-    return s;
+    *bad = true;
+    return -1;
   }
-  const size_t off = (static_cast<size_t>(b) * a.T_raw + r) * D * 2;
-  s.k = static_cast<const char*>(a.k_raw) + off;
-  s.v = static_cast<const char*>(a.v_raw) + off;
-  s.valid = true;
-  return s;
+  return -r - 2;
 }
 
 // byte offset of 16-byte chunk ch of row r in a swizzled [rows][D] bf16 tile
@@ -84,9 +72,9 @@ __global__ void __launch_bounds__(kThreads) attend_kernel(AttendArgs a, int nspl
   constexpr int TILE_BYTES = kTile * D * 2;
 
   extern __shared__ __align__(128) char smem[];
-  char* Ks = smem;                      // [2][kTile][D]
-  char* Vs = smem + 2 * TILE_BYTES;     // [2][kTile][D]
-  float* bias = reinterpret_cast<float*>(smem + 4 * TILE_BYTES);  // [2][kTile]
+  char* Ks = smem;                    // [2][kTile][D]
+  char* Vs = smem + 2 * TILE_BYTES;   // [2][kTile][D]
+  int* codes = reinterpret_cast<int*>(smem + 4 * TILE_BYTES);  // [tps * kTile] slot row codes
 
   const int split = blockIdx.x;
   const long long qi = blockIdx.y;
@@ -131,20 +119,36 @@ __global__ void __launch_bounds__(kThreads) attend_kernel(AttendArgs a, int nspl
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   const float sl2 = a.scale * kLog2e;
 
+  // resolve every key slot of this CTA's tile range once (one coalesced pass
+  // over the index list), so the gathers below need no dependent loads
+  {
+    const int raw_base = a.W > 0 ? a.raw_base[b] : 0;
+    bool bad = false;
+    const int nslots = (tile1 - tile0) * kTile;
+    for (int i = tid; i < nslots; i += kThreads)
+      codes[i] = slot_code(a, qi, b, t, n_c, raw_base, tile0 * kTile + i, &bad);
+    if (bad) raise_flag(a.errw, kFlagIndex);
+  }
+  __syncthreads();
+  const char* kc_base = static_cast<const char*>(a.k_cmp) + static_cast<size_t>(b) * a.N * D * 2;
+  const char* vc_base = static_cast<const char*>(a.v_cmp) + static_cast<size_t>(b) * a.N * D * 2;
+  const char* kr_base = static_cast<const char*>(a.k_raw) + static_cast<size_t>(b) * a.T_raw * D * 2;
+  const char* vr_base = static_cast<const char*>(a.v_raw) + static_cast<size_t>(b) * a.T_raw * D * 2;
+
   auto load_tile = [&](int stage, int tile) {
-    const int v0 = tile * kTile;
+    const int* cs = codes + (tile - tile0) * kTile;
 #pragma unroll
     for (int rr = 0; rr < kTile * CH / kThreads; ++rr) {
       const int i = tid + rr * kThreads;
       const int r = i / CH, ch = i % CH;
-      const Src s = key_source<D>(a, qi, b, t, n_c, v0 + r);
-      cp_async16(Ks + stage * TILE_BYTES + swz<D>(r, ch), s.k + ch * 16, s.valid);
-      cp_async16(Vs + stage * TILE_BYTES + swz<D>(r, ch), s.v + ch * 16, s.valid);
-    }
-    if (tid < kTile) {
-      const Src s = key_source<D>(a, qi, b, t, n_c, v0 + tid);
-      bias[stage * kTile + tid] = s.valid ? 0.f : -INFINITY;
-      if (s.bad) raise_flag(a.errw, kFlagIndex);
+      const int code = cs[r];
+      const char* ks = code >= 0 ? kc_base + static_cast<size_t>(code) * D * 2
+                                 : kr_base + static_cast<size_t>(code <= -2 ? -code - 2 : 0) * D * 2;
+      const char* vs = code >= 0 ? vc_base + static_cast<size_t>(code) * D * 2
+                                 : vr_base + static_cast<size_t>(code <= -2 ? -code - 2 : 0) * D * 2;
+      const bool valid = code != -1;
+      cp_async16(Ks + stage * TILE_BYTES + swz<D>(r, ch), valid ? ks + ch * 16 : kc_base, valid);
+      cp_async16(Vs + stage * TILE_BYTES + swz<D>(r, ch), valid ? vs + ch * 16 : vc_base, valid);
     }
     cp_async_commit();
   };
@@ -160,10 +164,10 @@ __global__ void __launch_bounds__(kThreads) attend_kernel(AttendArgs a, int nspl
     }
     __syncthreads();
 
-    const float* bs = bias + stage * kTile + ks * KW;
+    const int* cs = codes + (tile - tile0) * kTile + ks * KW;
     bool any = false;
 #pragma unroll
-    for (int i = 0; i < KW; i += 32) any |= __any_sync(0xffffffffu, bs[min(i + lane, KW - 1)] == 0.f);
+    for (int i = 0; i < KW; i += 32) any |= __any_sync(0xffffffffu, cs[min(i + lane, KW - 1)] != -1);
     if (any) {
       const char* Kt = Ks + stage * TILE_BYTES;
       const char* Vt = Vs + stage * TILE_BYTES;
@@ -187,7 +191,8 @@ __global__ void __launch_bounds__(kThreads) attend_kernel(AttendArgs a, int nspl
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        const float b0 = bs[8 * j + 2 * c], b1 = bs[8 * j + 2 * c + 1];
+        const float b0 = cs[8 * j + 2 * c] != -1 ? 0.f : -INFINITY;
+        const float b1 = cs[8 * j + 2 * c + 1] != -1 ? 0.f : -INFINITY;
         s[j][0] = fmaf(s[j][0], sl2, b0);
         s[j][1] = fmaf(s[j][1], sl2, b1);
         s[j][2] = fmaf(s[j][2], sl2, b0);
@@ -385,7 +390,7 @@ template <int D, int HG>
 cudaError_t launch_impl(const AttendArgs& a, const AttendPlan& p, cudaStream_t s) {
   constexpr int TILE_BYTES = kTile * D * 2;
   constexpr int KS = 4 / HG;
-  size_t smem = 4 * TILE_BYTES + 2 * kTile * sizeof(float);
+  size_t smem = 4 * TILE_BYTES + static_cast<size_t>(p.tiles_per_split) * kTile * sizeof(int);
   if (KS > 1) {
     const size_t need = 4 * 16 * D * 4 + 2 * 4 * 16 * 4;
     smem = smem > need ? smem : need;
@@ -415,16 +420,17 @@ AttendPlan plan_attend(int Tq, long long nq, int n_keys_max, int H, int d) {
   // The split depends only on the queries per sequence and the key count, never
   // on the batch size or the GPU, so a sequence gives bit-identical results
   // alone or inside any batch.  Prefill-like calls (many queries per sequence)
-  // fill the GPU without splitting; decode-like calls split every query's keys
-  // into ranges of at least four 64-key tiles (at most 32 ranges).
+  // fill the GPU without splitting (up to 128 tiles per CTA); decode-like calls
+  // split every query's keys into ranges of at least two 64-key tiles (at most
+  // 32 ranges).
   AttendPlan p;
   const int n_tiles = (n_keys_max + kTile - 1) / kTile;
   int tps;
   if (Tq >= 16) {
-    tps = n_tiles;
+    tps = n_tiles < kMaxTilesPerCta ? n_tiles : kMaxTilesPerCta;
   } else {
     tps = (n_tiles + 31) / 32;
-    tps = tps < 4 ? 4 : tps;
+    tps = tps < 2 ? 2 : tps;
   }
   if (tps > n_tiles) tps = n_tiles;
   if (tps < 1) tps = 1;

@@ -50,7 +50,7 @@ def test_workspace_sizes(L):
     assert L.csa_index_topk_workspace(1, 1, 5, 64, 128, 4, ctypes.byref(need)) == 0
     assert need.value == 256 + 256                # 8 floats rounded up to 256 bytes
     assert L.csa_attend_workspace(64, 1, 64, 128, 1024, 128, ctypes.byref(need)) == 0
-    splits = (1152 // 64 + 3) // 4                 # 4 tiles of 64 keys per split
+    splits = (1152 // 64 + 1) // 2                 # decode: 2 tiles of 64 keys per split
     assert need.value == 256 + 64 * splits * 64 * 129 * 4
     assert L.csa_attend_workspace(1, 8192, 16, 128, 1024, 128, ctypes.byref(need)) == 0
     assert need.value == 256                       # prefill: no split partials

@@ -80,3 +80,21 @@ def test_topk_signs_small_k_and_short_rows():
     q_pos = np.array([[0, 2, 3, 7, 4 * N - 1, 4 * N + 100]])        # n_vis 0, 0, 1, 2, N, N
     for k in (1, 2, 7, 1024, 4096):
         _check(s, q_pos, N, m, k)
+
+
+def test_topk_bucket_path_with_quantised_ties():
+    """Long rows take the 12-bit bucket path; scores on a 1/4 grid put many
+    exact ties inside the bucket that holds the k-th score."""
+    rng = np.random.default_rng(4)
+    N, m, k = 262144, 4, 1024
+    s = np.round((rng.standard_normal((3, 1, N)) * 30 + 150) * 4) / 4
+    q_pos = np.array([[4 * N - 1], [4 * N - 1], [4 * N - 9]])
+    _check(s.astype(np.float32), q_pos, N, m, k)
+
+
+def test_topk_bucket_overflow_falls_back():
+    """A bucket too full to gather (a narrow score range) takes the digit path."""
+    rng = np.random.default_rng(5)
+    N, m, k = 100000, 4, 1024
+    s = (1000.0 + rng.integers(0, 512, (2, 1, N)) / 4096.0).astype(np.float32)
+    _check(s, np.array([[4 * N - 1], [4 * N - 1]]), N, m, k)
