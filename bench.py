@@ -172,11 +172,19 @@ def graph_of(fn, st_torch):
     return g
 
 
-def time_graph(g, steps, warmup, stream):
+def time_graph(g, steps, warmup, stream, min_warm_s=0.3):
+    """Average ms per replay over exactly ``steps`` timed replays, after
+    ``warmup`` replays and at least ``min_warm_s`` seconds of untimed replays
+    (so that clocks and caches have settled whatever ``warmup`` is)."""
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             g.replay()
         stream.synchronize()
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < min_warm_s:
+            for _ in range(20):
+                g.replay()
+            stream.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(steps):
@@ -325,13 +333,19 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--all", action="store_true", help="also time the 8K prefill and the 1M HCA decode")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--workload", default=HEADLINE, choices=["decode_1m", "decode_128k", "decode_1m_tail"],
+                    help="decode workload to time (the headline is decode_1m)")
+    ap.add_argument("--quick", action="store_true",
+                    help="time the device step only: no stage breakdown, e2e, 128K line or CPU baseline "
+                         "(the form used for kernel profiles)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    wl = S.WORKLOADS[HEADLINE]
-    metric = "CSA decode queries/s @1M ctx (B=4, 262144 compressed entries, top-1024, W=128)"
+    wl = S.WORKLOADS[args.workload]
+    metric = (f"CSA decode queries/s @{'1M' if wl.T == 1 << 20 else '128K'} ctx (B={wl.B}, {wl.N} compressed "
+              f"entries, top-{wl.k}, W={wl.W})")
 
     if args.impl == "reference":
         if rank != 0:
@@ -354,7 +368,7 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
 
-    ds = DecodeStep(HEADLINE, dev)
+    ds = DecodeStep(args.workload, dev)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         ds.step(stream.cuda_stream)      # first calls outside capture (one-time set-up)
@@ -369,6 +383,11 @@ def main():
     clk.start()
     ms = time_graph(g_step, args.steps, args.warmup, stream)
     clocks = clk.stop()
+    if args.quick:
+        if rank == 0:
+            print(json.dumps({"workload": args.workload, "ms_per_step": ms, "steps": args.steps,
+                              "queries_per_s": ds.B * ds.Tq * world / (ms * 1e-3), "clocks": clocks}))
+        return
     stages = stage_breakdown(ds, max(20, min(args.steps, 400)), 5, stream)
     ms_idx = stages["indexer"]
     torch.cuda.synchronize()
@@ -408,7 +427,7 @@ def main():
     line = {"metric": metric, "value": qps, "unit": "queries/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": HEADLINE, "B": wl.B, "context": wl.T, "entries": wl.N, "m": wl.m,
+            "config": {"workload": args.workload, "B": wl.B, "context": wl.T, "entries": wl.N, "m": wl.m,
                        "H": wl.H, "d": wl.d, "H_I": wl.H_I, "d_I": wl.d_I, "k": wl.k, "W": wl.W,
                        "l2": "inputs exceed L2: 268 MB of indexer keys streamed per step",
                        "launch": "CUDA graph replay of csa_index_scores + csa_topk + csa_attend"},
