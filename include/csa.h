@@ -166,6 +166,41 @@ csa_status csa_attend(const void* q, const void* k_cmp, const void* v_cmp, const
                       void* ws, size_t ws_bytes, void* stream);
 
 /* --------------------------------------------------------------------------
+ * csa_attend without a workspace, for callers that cannot allocate device
+ * memory: operators hosted by a framework whose memory planner owns the
+ * device and hands an operator only its inputs and outputs, and latency-bound
+ * callers that must never reach cudaMalloc / cudaFree (both can synchronise
+ * the device).  The pages describe no such call; it has no counterpart there.
+ *
+ * Arguments, layouts, results and the argument errors are those of
+ * csa_attend; inputs and outputs are still caller-owned device memory.  The
+ * split-KV partials go to one fixed device array of CSA_NOALLOC_SCRATCH_BYTES
+ * inside the library instead of a workspace; every GPU that loads the library
+ * holds that array until the process exits, and no call allocates or frees
+ * anything.
+ * - Returns CSA_ERR_WORKSPACE when the call's partials would exceed
+ *   CSA_NOALLOC_SCRATCH_BYTES.  With n_tiles = ceil((k + W) / 64), a call
+ *   splits every query's keys into n_split = ceil(n_tiles / tiles) ranges,
+ *   tiles = max(2, ceil(n_tiles / 32)) when Tq < 16, else min(n_tiles, 128);
+ *   n_split > 1 needs B * Tq * n_split * H * (d + 1) * 4 bytes.  For example
+ *   B = 64, Tq = 1, H = 64, d = 128, k = 1024, W = 128 needs 19 MB.
+ * - The first call on a device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ * - Every call on a device shares the one array, which keeps the last call's
+ *   contents (each call writes every partial it reads, so nothing needs to
+ *   start at zero).  Calls that overlap on the GPU -- on different streams,
+ *   or from different host threads -- race on it: order them on one stream.
+ * - There is no error word: indices >= N and window rows outside the buffer
+ *   are skipped, as in csa_attend, but not reported.
+ * ------------------------------------------------------------------------ */
+#define CSA_NOALLOC_SCRATCH_BYTES (32u << 20)
+csa_status csa_attend_noalloc(const void* q, const void* k_cmp, const void* v_cmp,
+                              const int32_t* idx, const void* k_raw, const void* v_raw,
+                              const int32_t* raw_base, const int32_t* q_pos, int B, int Tq,
+                              int N, int T_raw, int H, int d, int k, int W, float scale,
+                              void* out, int out_dtype, float* lse, void* stream);
+
+/* --------------------------------------------------------------------------
  * HCA mode.  Octagono "Hybrid Attention: CSA and HCA" and the technical
  * review, section 2.2: entries compressed every m' (= 128) tokens, attended
  * densely with no selection, plus the same sliding window.  As csa_attend

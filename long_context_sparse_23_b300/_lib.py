@@ -52,6 +52,8 @@ SIGNATURES = {
     "csa_attend_workspace": (c_int, [c_int, c_int, c_int, c_int, c_int, c_int, c_sizep]),
     "csa_attend": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int,
                            c_int, c_int, c_int, c_int, c_float, c_vp, c_int, c_vp, c_vp, c_size, c_vp]),
+    "csa_attend_noalloc": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int,
+                                   c_int, c_int, c_int, c_int, c_float, c_vp, c_int, c_vp, c_vp]),
     "hca_attend_workspace": (c_int, [c_int, c_int, c_int, c_int, c_int, c_int, c_sizep]),
     "hca_attend": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int,
                            c_int, c_int, c_int, c_float, c_vp, c_int, c_vp, c_vp, c_size, c_vp]),
