@@ -104,7 +104,9 @@ class ClockSampler:
 # ---------------------------------------------------------------- workload
 
 class DecodeStep:
-    """Device buffers and the three enqueue calls of one decode step."""
+    """Device buffers and the two library calls of one decode step:
+    csa_index_topk (indexer scores + top-k) and csa_attend (selected entries
+    + window)."""
 
     def __init__(self, name: str, device):
         import long_context_sparse_23_b300 as csa
@@ -114,26 +116,18 @@ class DecodeStep:
         self.inp = S.make_inputs(wl, device)
         B, Tq = self.inp["q_pos"].shape
         self.B, self.Tq = B, Tq
-        self.ld = csa.scores_ld(wl.N)
-        self.scores = torch.empty(B, Tq, self.ld, dtype=torch.float32, device=device)
         self.idx = torch.empty(B, Tq, wl.k, dtype=torch.int32, device=device)
         self.out = torch.empty(B, Tq, wl.H, wl.d, dtype=torch.bfloat16, device=device)
-        need = ctypes.c_size_t(0)
-        self.L.csa_attend_workspace(B, Tq, wl.H, wl.d, wl.k, wl.W, ctypes.byref(need))
-        self.ws = csa.Workspace(need.value + (1 << 20), device)
-        self.st = torch.cuda.current_stream().cuda_stream
+        n1, n2 = ctypes.c_size_t(0), ctypes.c_size_t(0)
+        self.L.csa_index_topk_workspace(B, Tq, wl.N, wl.H_I, wl.d_I, wl.k, ctypes.byref(n1))
+        self.L.csa_attend_workspace(B, Tq, wl.H, wl.d, wl.k, wl.W, ctypes.byref(n2))
+        self.ws = csa.Workspace(max(n1.value, n2.value), device)
 
-    def indexer(self, st):
+    def index_topk(self, st):
         i, wl = self.inp, self.wl
-        r = self.L.csa_index_scores(i["q_idx"].data_ptr(), i["i_cmp"].data_ptr(), i["w"].data_ptr(),
-                                    i["q_pos"].data_ptr(), self.B, self.Tq, wl.N, wl.H_I, wl.d_I, wl.m,
-                                    self.scores.data_ptr(), self.ld, self.ws.ptr, self.ws.nbytes, st)
-        assert r == 0, r
-
-    def topk(self, st):
-        wl = self.wl
-        r = self.L.csa_topk(self.scores.data_ptr(), self.ld, self.inp["q_pos"].data_ptr(), self.B, self.Tq,
-                            wl.N, wl.m, wl.k, self.idx.data_ptr(), None, self.ws.ptr, self.ws.nbytes, st)
+        r = self.L.csa_index_topk(i["q_idx"].data_ptr(), i["i_cmp"].data_ptr(), i["w"].data_ptr(),
+                                  i["q_pos"].data_ptr(), self.B, self.Tq, wl.N, wl.H_I, wl.d_I, wl.m, wl.k,
+                                  self.idx.data_ptr(), None, self.ws.ptr, self.ws.nbytes, st)
         assert r == 0, r
 
     def attend(self, st):
@@ -146,16 +140,22 @@ class DecodeStep:
         assert r == 0, r
 
     def step(self, st):
-        self.indexer(st)
-        self.topk(st)
+        self.index_topk(st)
         self.attend(st)
 
     def kernels_per_step(self):
-        """indexer + top-k + attention, + the split combine when keys are split"""
+        """Our kernel launches in one step: the indexer, top-k (select + finish
+        for long rows, + the histogram pass when the indexer does not build
+        it; one kernel for short rows), attention (+ the split combine)."""
+        wl = self.wl
+        if wl.N > 16384:
+            topk = 2 + (0 if self.Tq == 1 and wl.H_I >= 16 else 1)
+        else:
+            topk = 1
         need = ctypes.c_size_t(0)
-        self.L.csa_attend_workspace(1, self.Tq, self.wl.H, self.wl.d, self.wl.k, self.wl.W, ctypes.byref(need))
+        self.L.csa_attend_workspace(1, self.Tq, wl.H, wl.d, wl.k, wl.W, ctypes.byref(need))
         combine = 1 if need.value > 256 else 0
-        return 3 + combine
+        return 1 + topk + 1 + combine
 
     # algorithmic work of the indexer launch (per visible entry: its d_I-wide bf16
     # key read once + one fp32 score written; per query: its H_I x d_I bf16 queries)
@@ -165,43 +165,65 @@ class DecodeStep:
         return n_vis * (wl.d_I * 2 + 4) + self.B * self.Tq * wl.H_I * wl.d_I * 2, n_vis
 
 
-def graph_of(fn, st_torch):
+def graph_of(fn, st_torch, n=1, marks=None, L=None):
+    """CUDA graph of ``n`` consecutive steps; with ``marks`` = (begin events,
+    end events), step i records marks[0][i] / marks[1][i] around its indexer
+    launch (csa_set_indexer_events), so the indexer is timed inside the graph."""
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=st_torch):
-        fn(st_torch.cuda_stream)
+        for i in range(n):
+            if marks is not None:
+                L.csa_set_indexer_events(marks[0][i].cuda_event, marks[1][i].cuda_event)
+            fn(st_torch.cuda_stream)
+        if marks is not None:
+            L.csa_set_indexer_events(None, None)
     return g
 
 
-def time_graph(g, steps, warmup, stream, min_warm_s=0.3):
-    """Average ms per replay over exactly ``steps`` timed replays, after
-    ``warmup`` replays and at least ``min_warm_s`` seconds of untimed replays
-    (so that clocks and caches have settled whatever ``warmup`` is)."""
+def timing_events(n, stream):
+    """n timing events, each recorded once so that its handle exists."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in ev:
+        e.record(stream)
+    stream.synchronize()
+    return ev
+
+
+def warm(g1, warmup, stream, min_warm_s=0.3):
+    """``warmup`` replays of the one-step graph, then at least ``min_warm_s``
+    seconds more of them (clocks and caches settle whatever ``warmup`` is)."""
     with torch.cuda.stream(stream):
         for _ in range(warmup):
-            g.replay()
+            g1.replay()
         stream.synchronize()
         t0 = time.perf_counter()
         while time.perf_counter() - t0 < min_warm_s:
             for _ in range(20):
-                g.replay()
+                g1.replay()
             stream.synchronize()
+
+
+def time_steps(gk, steps, stream):
+    """Device time of one replay of the ``steps``-step graph (CUDA events on
+    the launching stream, synchronised on both sides): ms per step."""
+    with torch.cuda.stream(stream):
+        stream.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(steps):
-            g.replay()
+        gk.replay()
         e1.record(stream)
         e1.synchronize()
     return e0.elapsed_time(e1) / steps
 
 
 def stage_breakdown(ds: DecodeStep, steps: int, warmup: int, stream):
-    """Average device time of each stage: plain launches with CUDA events
-    between the stage calls on the launching stream.  Each batch of steps is
+    """Average device time of each library call: plain launches with CUDA
+    events between the calls on the launching stream.  Each batch of steps is
     queued behind a GPU-side sleep, so the host has enqueued the whole batch
     before the first kernel starts and the events time kernels back to back
     (not host launch latency)."""
-    names = ("indexer", "topk", "attend")
-    fns = (ds.indexer, ds.topk, ds.attend)
+    names = ("index_topk", "attend")
+    fns = (ds.index_topk, ds.attend)
     st = stream.cuda_stream
     batch = 50
     tot = {n: 0.0 for n in names}
@@ -211,7 +233,7 @@ def stage_breakdown(ds: DecodeStep, steps: int, warmup: int, stream):
             ds.step(st)
         while done < steps:
             nb = min(batch, steps - done)
-            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nb)]
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nb)]
             torch.cuda._sleep(20_000_000)       # ~10 ms of GPU time to queue behind
             for i in range(nb):
                 ev[i][0].record(stream)
@@ -370,26 +392,33 @@ def main():
 
     ds = DecodeStep(args.workload, dev)
     stream = torch.cuda.Stream(device=dev)
+    K = args.steps
+    ev_b, ev_e = timing_events(K, stream), timing_events(K, stream)
     with torch.cuda.stream(stream):
         ds.step(stream.cuda_stream)      # first calls outside capture (one-time set-up)
         stream.synchronize()
-        g_step = graph_of(ds.step, stream)
+        g1 = graph_of(ds.step, stream)
+        gk = graph_of(ds.step, stream, n=K, marks=(ev_b, ev_e), L=ds.L)
     assert ds.ws.check_error() == 0
 
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    warm(g1, args.warmup, stream)
     clk = ClockSampler(local)
     clk.start()
-    ms = time_graph(g_step, args.steps, args.warmup, stream)
+    ms = time_steps(gk, K, stream)
     clocks = clk.stop()
+    # the indexer's own launches inside the timed region
+    ms_idx = sum(b.elapsed_time(e) for b, e in zip(ev_b, ev_e)) / K
     if args.quick:
+        stages = stage_breakdown(ds, 50, 5, stream)
         if rank == 0:
-            print(json.dumps({"workload": args.workload, "ms_per_step": ms, "steps": args.steps,
-                              "queries_per_s": ds.B * ds.Tq * world / (ms * 1e-3), "clocks": clocks}))
+            print(json.dumps({"workload": args.workload, "ms_per_step": ms, "steps": K, "indexer_ms": ms_idx,
+                              "stages_ms": stages, "queries_per_s": ds.B * ds.Tq * world / (ms * 1e-3),
+                              "clocks": clocks}))
         return
     stages = stage_breakdown(ds, max(20, min(args.steps, 400)), 5, stream)
-    ms_idx = stages["indexer"]
     torch.cuda.synchronize()
     if world > 1:
         t = torch.tensor([ms], device=dev)
@@ -412,16 +441,19 @@ def main():
             "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.4 TB/s"}
 
     extra = {}
-    del ds, g_step
+    del ds, g1, gk
     torch.cuda.empty_cache()
     ds2 = DecodeStep("decode_128k", dev)
+    K2 = max(10, args.steps // 4)
     with torch.cuda.stream(stream):
         ds2.step(stream.cuda_stream)
         stream.synchronize()
-        g2 = graph_of(ds2.step, stream)
-    ms2 = time_graph(g2, max(10, args.steps // 4), 10, stream)
+        g1 = graph_of(ds2.step, stream)
+        gk = graph_of(ds2.step, stream, n=K2)
+    warm(g1, 10, stream)
+    ms2 = time_steps(gk, K2, stream)
     extra["decode_128k"] = {"queries_per_s": ds2.B * ds2.Tq / (ms2 * 1e-3), "ms_per_step": ms2}
-    del ds2, g2
+    del ds2, g1, gk
     torch.cuda.empty_cache()
 
     line = {"metric": metric, "value": qps, "unit": "queries/s", "n_gpus": world, "steps": args.steps,
@@ -429,8 +461,8 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "B": wl.B, "context": wl.T, "entries": wl.N, "m": wl.m,
                        "H": wl.H, "d": wl.d, "H_I": wl.H_I, "d_I": wl.d_I, "k": wl.k, "W": wl.W,
-                       "l2": "inputs exceed L2: 268 MB of indexer keys streamed per step",
-                       "launch": "CUDA graph replay of csa_index_scores + csa_topk + csa_attend"},
+                       "l2": f"inputs exceed L2: {ibytes / 1e6:.0f} MB of indexer keys streamed per step",
+                       "launch": "one CUDA graph of K unrolled steps (csa_index_topk + csa_attend)"},
             "clocks": clocks, "gpu_launches": launches, "roofline": roof,
             "e2e": {"value": e2e_qps, "unit": "queries/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "stages_ms": {k: round(v, 5) for k, v in stages.items()}, "also": extra}

@@ -127,13 +127,18 @@ csa_status csa_index_scores(const void* q_idx, const void* k_idx, const float* w
  *   idx_out   [B, Tq, k] int32: kept block indices ascending, then -1
  *   score_out [B, Tq, k] fp32 (nullable): the kept scores, 0 in padding
  * Integer radix selection on order-preserving keys: exact, no tolerance.
- * 1 <= k <= 4096; N <= 262144 * 3.  Workspace: CSA_WS_HEADER_BYTES.
+ * 1 <= k <= 4096; N <= 2^24.  Rows longer than 16384 entries use a bucket
+ * histogram and candidate list in the workspace: size from
+ * csa_topk_workspace (CSA_WS_HEADER_BYTES alone when N <= 16384).
  * ------------------------------------------------------------------------ */
+csa_status csa_topk_workspace(int B, int Tq, int N, int k, size_t* bytes);
 csa_status csa_topk(const float* scores, int64_t ld_scores, const int32_t* q_pos,
                     int B, int Tq, int N, int m, int k, int32_t* idx_out, float* score_out,
                     void* ws, size_t ws_bytes, void* stream);
 
-/* (2)+(3) in one call; the scores live in the workspace. */
+/* (2)+(3) in one call; the scores (and the long-row top-k scratch) live in
+ * the workspace.  With Tq == 1 the indexer also accumulates the top-k bucket
+ * histogram as it writes the scores. */
 csa_status csa_index_topk_workspace(int B, int Tq, int N, int H_I, int d_I, int k,
                                     size_t* bytes);
 csa_status csa_index_topk(const void* q_idx, const void* k_idx, const float* w,
@@ -173,17 +178,18 @@ csa_status csa_attend(const void* q, const void* k_cmp, const void* v_cmp, const
  * the device).  The pages describe no such call; it has no counterpart there.
  *
  * Arguments, layouts, results and the argument errors are those of
- * csa_attend; inputs and outputs are still caller-owned device memory.  The
- * split-KV partials go to one fixed device array of CSA_NOALLOC_SCRATCH_BYTES
- * inside the library instead of a workspace; every GPU that loads the library
- * holds that array until the process exits, and no call allocates or frees
- * anything.
+ * csa_attend; inputs and outputs are still caller-owned device memory.  Key
+ * lists of up to 16 * 128 tiles of 64 keys (k + W <= 131072) merge their
+ * split partials inside a thread-block cluster and need no scratch at all;
+ * longer lists keep their split partials in one fixed device array of
+ * CSA_NOALLOC_SCRATCH_BYTES inside the library instead of a workspace.
+ * Every GPU that loads the library holds that array until the process exits,
+ * and no call allocates or frees anything.
  * - Returns CSA_ERR_WORKSPACE when the call's partials would exceed
- *   CSA_NOALLOC_SCRATCH_BYTES.  With n_tiles = ceil((k + W) / 64), a call
- *   splits every query's keys into n_split = ceil(n_tiles / tiles) ranges,
- *   tiles = max(2, ceil(n_tiles / 32)) when Tq < 16, else min(n_tiles, 128);
- *   n_split > 1 needs B * Tq * n_split * H * (d + 1) * 4 bytes.  For example
- *   B = 64, Tq = 1, H = 64, d = 128, k = 1024, W = 128 needs 19 MB.
+ *   CSA_NOALLOC_SCRATCH_BYTES: with n_tiles = ceil((k + W) / 64) > 2048, a
+ *   call splits every query's keys into n_split = ceil(n_tiles / 128)
+ *   ranges and needs B * Tq * n_split * H * (d + 1) * 4 bytes (for example
+ *   k + W = 139392, H = 64, d = 128: 594 KB per query, at most 56 queries).
  * - The first call on a device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
  * - Every call on a device shares the one array, which keeps the last call's
@@ -247,6 +253,14 @@ csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* s
  * later calls in this process (default ~2^31 cycles, about one second).
  * cycles <= 0 restores the default. */
 void csa_set_wait_budget(long long cycles);
+
+/* Instrumentation: until called again with NULLs, every call made from this
+ * host thread that launches the indexer kernel (csa_index_scores,
+ * csa_index_topk, csa_layer) records cudaEvent_t ev_begin on the call's
+ * stream just before that launch and ev_end just after it, so the indexer can
+ * be timed inside the fused calls (also inside a stream capture, where the
+ * records become graph nodes).  Either may be NULL. */
+void csa_set_indexer_events(void* ev_begin, void* ev_end);
 
 #ifdef __cplusplus
 }

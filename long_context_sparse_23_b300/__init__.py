@@ -141,7 +141,9 @@ def csa_topk(scores: torch.Tensor, q_pos: torch.Tensor, N: int, m: int, k: int,
     B, Tq, ld = scores.shape
     idx = torch.empty(B, Tq, k, dtype=torch.int32, device=scores.device)
     sel = torch.empty(B, Tq, k, dtype=torch.float32, device=scores.device) if with_scores else None
-    w_ = _ws(_lib.CSA_WS_HEADER_BYTES, ws)
+    need = ctypes.c_size_t(0)
+    check("csa_topk_workspace", _lib.lib().csa_topk_workspace(B, Tq, N, k, ctypes.byref(need)))
+    w_ = _ws(need.value, ws)
     st = _lib.lib().csa_topk(_ptr(scores), ld, _ptr(q_pos), B, Tq, N, m, k, _ptr(idx), _ptr(sel),
                              w_.ptr, w_.nbytes, _stream())
     check("csa_topk", st)

@@ -46,6 +46,7 @@ SIGNATURES = {
                                  c_vp, ctypes.c_int64, c_vp, c_size, c_vp]),
     "csa_topk": (c_int, [c_vp, ctypes.c_int64, c_vp, c_int, c_int, c_int, c_int, c_int, c_vp, c_vp,
                          c_vp, c_size, c_vp]),
+    "csa_topk_workspace": (c_int, [c_int, c_int, c_int, c_int, c_sizep]),
     "csa_index_topk_workspace": (c_int, [c_int, c_int, c_int, c_int, c_int, c_int, c_sizep]),
     "csa_index_topk": (c_int, [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                                c_vp, c_vp, c_vp, c_size, c_vp]),
@@ -60,6 +61,7 @@ SIGNATURES = {
     "csa_layer_workspace": (c_int, [ctypes.POINTER(csa_layer_args), c_sizep]),
     "csa_layer": (c_int, [ctypes.POINTER(csa_layer_args), c_vp, c_size, c_vp]),
     "csa_set_wait_budget": (None, [c_ll]),
+    "csa_set_indexer_events": (None, [c_vp, c_vp]),
 }
 
 _lib = None

@@ -15,11 +15,18 @@
 // (double-buffered; invalid slots are zero-filled and masked with -inf).
 // Warps are (head group of 16) x (key sub-range of the tile): S = Q K^T and
 // O += P V run on mma.sync m16n8k16 (bf16 in, fp32 out) with an online
-// softmax in the log2 domain.  Sub-range partials merge in shared memory, and
-// split partials (normalised O, log2-sum-exp) merge in a second kernel in
-// split order, so results never depend on scheduling.
+// softmax in the log2 domain.  Sub-range partials merge in shared memory.
+// The key-range splits of one query (up to 16) form a thread-block cluster:
+// each CTA publishes its (O, max, sum) in shared memory and then folds every
+// split's partial into its slice of the output through distributed shared
+// memory, in split order, so results never depend on scheduling.  Longer key
+// lists keep split partials in the workspace and merge in a second kernel.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
+
+namespace cg = cooperative_groups;
 
 namespace csa {
 
@@ -28,6 +35,7 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kTile = 64;  // keys per tile
 constexpr int kMaxTilesPerCta = 128;
+constexpr int kMaxCluster = 16;  // CTAs of one query merged through distributed shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -62,8 +70,12 @@ __device__ __forceinline__ int swz(int r, int ch) {
   return r * (D * 2) + ((ch ^ (r & 7)) << 4);
 }
 
+// mode: 0 = one split (write the output), 1 = split partials to global
+// memory (merged by attend_combine_kernel), 2 = the splits of a query form a
+// thread-block cluster and merge through distributed shared memory.
 template <int D, int HG>
-__global__ void __launch_bounds__(kThreads) attend_kernel(AttendArgs a, int nsplit, int tps) {
+__global__ void __launch_bounds__(kThreads) attend_kernel(AttendArgs a, int nsplit, int tps, int mode) {
+  pdl_wait_then_release();
   constexpr int KS = 4 / HG;      // key sub-ranges per tile
   constexpr int KW = kTile / KS;  // keys per warp per tile: 64, 32, 16
   constexpr int CH = D / 8;       // 16-byte chunks per row
@@ -305,14 +317,101 @@ __global__ void __launch_bounds__(kThreads) attend_kernel(AttendArgs a, int nspl
       l1 = L1;
     }
   }
+  const int h0 = hg * 16 + g, h1 = h0 + 8;
+  if (mode == 2) {
+    // ---- cluster merge: every CTA publishes (o, m, l) in its shared memory,
+    // then owns a slice of the (head, column) outputs and folds the cluster's
+    // partials into it in split order
+    float* po = reinterpret_cast<float*>(smem);   // [H][D] unnormalised
+    float* pm = po + a.H * D;                      // [H] running max (log2 domain)
+    float* pl = pm + a.H;                          // [H] sum of exponentials
+    __syncthreads();                               // the merge above is done with smem
+    if (ks == 0) {
+#pragma unroll
+      for (int i = 0; i < DT; ++i) {
+        const int col = 8 * i + 2 * c;
+        if (h0 < a.H) *reinterpret_cast<float2*>(po + h0 * D + col) = make_float2(o[i][0], o[i][1]);
+        if (h1 < a.H) *reinterpret_cast<float2*>(po + h1 * D + col) = make_float2(o[i][2], o[i][3]);
+      }
+      if (c == 0) {
+        if (h0 < a.H) {
+          pm[h0] = m0;
+          pl[h0] = l0;
+        }
+        if (h1 < a.H) {
+          pm[h1] = m1;
+          pl[h1] = l1;
+        }
+      }
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    const int C = static_cast<int>(cluster.num_blocks());
+    const int rank = static_cast<int>(cluster.block_rank());
+    // every split's (max, sum) of every head, fetched once into local shared
+    // memory (after the partial o, which nothing overwrites)
+    float* wgt = pl + a.H;  // [kMaxCluster][H] weights 2^(m_r - M) / L
+    for (int i = tid; i < C * a.H; i += kThreads) {
+      const int r = i / a.H, h = i % a.H;
+      wgt[i] = *cluster.map_shared_rank(pm + h, r);
+      wgt[kMaxCluster * a.H + i] = *cluster.map_shared_rank(pl + h, r);
+    }
+    __syncthreads();
+    if (tid < a.H) {
+      const int h = tid;
+      float M = -INFINITY;
+      for (int r = 0; r < C; ++r) M = fmaxf(M, wgt[r * a.H + h]);
+      float den = 0.f;
+      for (int r = 0; r < C; ++r) {
+        const float f = M == -INFINITY ? 0.f : ex2(wgt[r * a.H + h] - M);
+        wgt[r * a.H + h] = f;
+        den = fmaf(f, wgt[kMaxCluster * a.H + r * a.H + h], den);
+      }
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      for (int r = 0; r < C; ++r) wgt[r * a.H + h] *= inv;
+      if (a.lse && rank == 0) a.lse[qi * a.H + h] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
+    }
+    __syncthreads();
+    // this CTA's slice of the output, four columns per thread, all splits'
+    // partials requested before any is used
+    const int n4 = a.H * D / 4;
+    for (int e4 = rank * kThreads + tid; e4 < n4; e4 += C * kThreads) {
+      const int h = (4 * e4) / D;
+      float4 v[kMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < C) v[r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(po + 4 * e4, r));
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) {
+        if (r < C) {
+          const float f = wgt[r * a.H + h];
+          acc.x = fmaf(f, v[r].x, acc.x);
+          acc.y = fmaf(f, v[r].y, acc.y);
+          acc.z = fmaf(f, v[r].z, acc.z);
+          acc.w = fmaf(f, v[r].w, acc.w);
+        }
+      }
+      const long long o0 = qi * static_cast<long long>(a.H) * D + 4 * e4;
+      if (a.out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + o0) = acc;
+      } else {
+        uint2 pk;
+        pk.x = pack_bf16x2(acc.x, acc.y);
+        pk.y = pack_bf16x2(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + o0) = pk;
+      }
+    }
+    cluster.sync();  // peers may still read this CTA's partials until here
+    return;
+  }
   if (ks != 0) return;
 
   // ---- write: final output (single split) or the split partial
-  const int h0 = hg * 16 + g, h1 = h0 + 8;
   const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
   const float lse0 = l0 > 0.f ? m0 + __log2f(l0) : -INFINITY;
   const float lse1 = l1 > 0.f ? m1 + __log2f(l1) : -INFINITY;
-  if (nsplit == 1) {
+  if (mode == 0) {
 #pragma unroll
     for (int i = 0; i < DT; ++i) {
       const int col = 8 * i + 2 * c;
@@ -362,6 +461,7 @@ __global__ void __launch_bounds__(kThreads) attend_kernel(AttendArgs a, int nspl
 // Merge split partials of one (query, head) in split order.
 template <int D>
 __global__ void __launch_bounds__(D) attend_combine_kernel(AttendArgs a, int nsplit) {
+  pdl_wait_then_release();
   const long long qh = blockIdx.x;  // qi * H + h
   const long long qi = qh / a.H;
   const int h = static_cast<int>(qh % a.H);
@@ -395,15 +495,30 @@ cudaError_t launch_impl(const AttendArgs& a, const AttendPlan& p, cudaStream_t s
     const size_t need = 4 * 16 * D * 4 + 2 * 4 * 16 * 4;
     smem = smem > need ? smem : need;
   }
+  if (p.mode == 2) {
+    // the CTA's partial (o, m, l), then every split's (m, l) of every head
+    const size_t need = static_cast<size_t>(a.H) * (D + 2 + 2 * kMaxCluster) * 4;
+    smem = smem > need ? smem : need;
+  }
   cudaError_t e = ensure_dyn_smem<attend_kernel<D, HG>>(static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long nq = static_cast<long long>(a.B) * a.Tq;
-  dim3 grid(p.nsplit, static_cast<unsigned>(nq));
-  attend_kernel<D, HG><<<grid, kThreads, smem, s>>>(a, p.nsplit, p.tiles_per_split);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || p.nsplit == 1) return e;
-  attend_combine_kernel<D><<<static_cast<unsigned>(nq * a.H), D, 0, s>>>(a, p.nsplit);
-  return cudaGetLastError();
+  const dim3 grid(p.nsplit, static_cast<unsigned>(nq));
+  if (p.mode == 2 && p.nsplit > 8) {
+    static bool nonportable_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!nonportable_set[dev]) {
+      e = cudaFuncSetAttribute(attend_kernel<D, HG>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      nonportable_set[dev] = true;
+    }
+  }
+  e = launch_k(attend_kernel<D, HG>, grid, dim3(kThreads), smem, s, p.mode == 2 ? p.nsplit : 1, a, p.nsplit,
+               p.tiles_per_split, p.mode);
+  if (e != cudaSuccess || p.mode != 1) return e;
+  return launch_k(attend_combine_kernel<D>, dim3(static_cast<unsigned>(nq * a.H)), dim3(D), 0, s, 1, a,
+                  p.nsplit);
 }
 
 template <int D>
@@ -421,22 +536,25 @@ AttendPlan plan_attend(int Tq, long long nq, int n_keys_max, int H, int d) {
   // on the batch size or the GPU, so a sequence gives bit-identical results
   // alone or inside any batch.  Prefill-like calls (many queries per sequence)
   // fill the GPU without splitting (up to 128 tiles per CTA); decode-like calls
-  // split every query's keys into ranges of at least two 64-key tiles (at most
-  // 32 ranges).
+  // split every query's keys over up to kMaxCluster CTAs.  Up to kMaxCluster
+  // splits of a query run as one thread-block cluster and merge through
+  // distributed shared memory; more splits (over kMaxCluster * 128 tiles) keep
+  // their partials in the workspace and merge in a second kernel.
   AttendPlan p;
   const int n_tiles = (n_keys_max + kTile - 1) / kTile;
   int tps;
   if (Tq >= 16) {
     tps = n_tiles < kMaxTilesPerCta ? n_tiles : kMaxTilesPerCta;
   } else {
-    tps = (n_tiles + 31) / 32;
-    tps = tps < 2 ? 2 : tps;
+    tps = (n_tiles + kMaxCluster - 1) / kMaxCluster;
+    tps = tps > kMaxTilesPerCta ? kMaxTilesPerCta : tps;
   }
   if (tps > n_tiles) tps = n_tiles;
   if (tps < 1) tps = 1;
   p.tiles_per_split = tps;
   p.nsplit = n_tiles > 0 ? (n_tiles + tps - 1) / tps : 1;
-  p.part_bytes = p.nsplit > 1 ? static_cast<size_t>(nq) * p.nsplit * H * (d + 1) * sizeof(float) : 0;
+  p.mode = p.nsplit == 1 ? 0 : (p.nsplit <= kMaxCluster ? 2 : 1);
+  p.part_bytes = p.mode == 1 ? static_cast<size_t>(nq) * p.nsplit * H * (d + 1) * sizeof(float) : 0;
   return p;
 }
 

@@ -237,6 +237,46 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 }
 
 // ----------------------------------------------------------------------------
+// programmatic dependent launch: every kernel of the library is launched so
+// that it may start while the previous kernel on the stream finishes; it
+// waits for that kernel's completion (and memory) before touching any data,
+// then lets its own dependent start launching.  Because each kernel triggers
+// only after its own wait, the predecessor of a running kernel has always
+// completed as well.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait_then_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch ``kern`` with programmatic stream serialisation and, for
+// cluster_x > 1, thread-block clusters of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            int cluster_x, Args... args) {
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute at[2];
+  int n = 0;
+  at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  lc.attrs = at;
+  lc.numAttrs = n;
+  return cudaLaunchKernelEx(&lc, kern, args...);
+}
+
+// ----------------------------------------------------------------------------
 // small block-wide helpers
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ unsigned lanemask_lt() {

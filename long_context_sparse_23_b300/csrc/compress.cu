@@ -65,6 +65,7 @@ __device__ __forceinline__ void fold_rows(const char* xp, const char* gp, size_t
 
 template <int R, bool kF32Out>
 __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
+  pdl_wait_then_release();
   const int sidx = blockIdx.y;
   // select with constant indices so the argument block stays in param space
   const int D = sidx == 0 ? a.D[0] : (sidx == 1 ? a.D[1] : a.D[2]);
@@ -118,11 +119,9 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
 }
 
 template <int R>
-void launch_r(const CompressArgs& a, dim3 grid, cudaStream_t s) {
-  if (a.out_f32)
-    compress_kernel<R, true><<<grid, kThreads, 0, s>>>(a);
-  else
-    compress_kernel<R, false><<<grid, kThreads, 0, s>>>(a);
+cudaError_t launch_r(const CompressArgs& a, dim3 grid, cudaStream_t s) {
+  if (a.out_f32) return launch_k(compress_kernel<R, true>, grid, dim3(kThreads), 0, s, 1, a);
+  return launch_k(compress_kernel<R, false>, grid, dim3(kThreads), 0, s, 1, a);
 }
 
 }  // namespace
@@ -138,15 +137,10 @@ cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s) {
   const long long cap = 148LL * 8;  // grid-stride beyond eight resident blocks per SM
   if (blocks > cap) blocks = cap;
   dim3 grid(static_cast<unsigned>(blocks), a.n_streams);
-  if (a.m % 8 == 0)
-    launch_r<8>(a, grid, s);
-  else if (a.m % 4 == 0)
-    launch_r<4>(a, grid, s);
-  else if (a.m % 2 == 0)
-    launch_r<2>(a, grid, s);
-  else
-    launch_r<1>(a, grid, s);
-  return cudaGetLastError();
+  if (a.m % 8 == 0) return launch_r<8>(a, grid, s);
+  if (a.m % 4 == 0) return launch_r<4>(a, grid, s);
+  if (a.m % 2 == 0) return launch_r<2>(a, grid, s);
+  return launch_r<1>(a, grid, s);
 }
 
 }  // namespace csa

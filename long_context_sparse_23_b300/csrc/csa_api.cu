@@ -12,6 +12,23 @@ namespace {
 
 long long g_wait_budget = 1LL << 31;  // clock64 cycles, about one second
 
+// Instrumentation: events recorded around the next indexer launches of this
+// host thread (csa_set_indexer_events).
+thread_local cudaEvent_t t_idx_ev_begin = nullptr;
+thread_local cudaEvent_t t_idx_ev_end = nullptr;
+
+// (cudaEventRecordExternal: inside a stream capture the record becomes an
+// event-record node of the graph, not a capture-internal dependency)
+cudaError_t launch_indexer_marked(const csa::IndexerArgs& a, cudaStream_t s) {
+  if (t_idx_ev_begin) {
+    cudaError_t e = cudaEventRecordWithFlags(t_idx_ev_begin, s, cudaEventRecordExternal);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = csa::launch_indexer(a, s);
+  if (e == cudaSuccess && t_idx_ev_end) e = cudaEventRecordWithFlags(t_idx_ev_end, s, cudaEventRecordExternal);
+  return e;
+}
+
 constexpr size_t kAlignWs = 256;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -87,6 +104,32 @@ csa_status check_attend_args(const void* q, const void* k_cmp, const void* v_cmp
   return CSA_OK;
 }
 
+size_t topk_bytes(int B, int Tq, int N) {
+  return align_up(csa::topk_scratch_bytes(static_cast<long long>(B) * Tq, N), kAlignWs);
+}
+
+// Indexer (optionally filling the top-k histogram) then top-k, with the
+// long-row scratch at ``tk``.
+csa_status index_then_topk(const csa::IndexerArgs& ia_in, const csa::TopkArgs& ta_in, void* tk,
+                           cudaStream_t s) {
+  csa::IndexerArgs ia = ia_in;
+  csa::TopkArgs ta = ta_in;
+  const long long nq = static_cast<long long>(ta.B) * ta.Tq;
+  bool fused = false;
+  if (csa::topk_long_rows(ta.N)) {
+    csa::topk_scratch_carve(ta, tk, nq);
+    fused = csa::indexer_fills_hist(ia.Tq, ia.H_I);
+    if (fused) {
+      cudaError_t e = csa::launch_topk_zero(ta, nq, s);
+      if (e != cudaSuccess) return CSA_ERR_CUDA;
+      ia.hist = ta.hist;
+    }
+  }
+  csa_status st = cuda_status(launch_indexer_marked(ia, s));
+  if (st != CSA_OK) return st;
+  return cuda_status(csa::launch_topk(ta, fused, s));
+}
+
 size_t attend_part_bytes(int B, int Tq, int n_keys_max, int H, int d) {
   const csa::AttendPlan p = csa::plan_attend(Tq, static_cast<long long>(B) * Tq, n_keys_max, H, d);
   return align_up(p.part_bytes, kAlignWs);
@@ -112,6 +155,11 @@ const char* csa_status_string(int s) {
 int csa_version(void) { return 100; }
 
 void csa_set_wait_budget(long long cycles) { g_wait_budget = cycles > 0 ? cycles : (1LL << 31); }
+
+void csa_set_indexer_events(void* ev_begin, void* ev_end) {
+  t_idx_ev_begin = static_cast<cudaEvent_t>(ev_begin);
+  t_idx_ev_end = static_cast<cudaEvent_t>(ev_end);
+}
 
 csa_status csa_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   if (check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES) != CSA_OK) return CSA_ERR_WORKSPACE;
@@ -172,8 +220,8 @@ csa_status csa_index_scores(const void* q_idx, const void* k_idx, const float* w
   st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES);
   if (st != CSA_OK) return st;
   csa::IndexerArgs a{q_idx, k_idx, w, q_pos, scores, ld_scores, B, Tq, N, H_I, d_I, m,
-                     err_word(ws), g_wait_budget};
-  return cuda_status(csa::launch_indexer(a, static_cast<cudaStream_t>(stream)));
+                     err_word(ws), g_wait_budget, nullptr};
+  return cuda_status(launch_indexer_marked(a, static_cast<cudaStream_t>(stream)));
 }
 
 // ---------------------------------------------------------------- (3)
@@ -183,10 +231,19 @@ csa_status csa_topk(const float* scores, int64_t ld_scores, const int32_t* q_pos
   csa_status st = check_topk_args(q_pos, B, Tq, N, m, k, idx_out, score_out);
   if (st != CSA_OK) return st;
   if (!scores || !al16(scores) || ld_scores < N || ld_scores % 4 != 0) return CSA_ERR_INVALID;
-  st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES);
+  st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES + topk_bytes(B, Tq, N));
   if (st != CSA_OK) return st;
-  csa::TopkArgs a{scores, ld_scores, q_pos, B, Tq, N, m, k, idx_out, score_out};
-  return cuda_status(csa::launch_topk(a, static_cast<cudaStream_t>(stream)));
+  csa::TopkArgs a{scores, ld_scores, q_pos, B, Tq, N, m, k, idx_out, score_out, nullptr, nullptr, nullptr, nullptr};
+  if (csa::topk_long_rows(N))
+    csa::topk_scratch_carve(a, static_cast<char*>(ws) + CSA_WS_HEADER_BYTES, static_cast<long long>(B) * Tq);
+  return cuda_status(csa::launch_topk(a, false, static_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_topk_workspace(int B, int Tq, int N, int k, size_t* bytes) {
+  (void)k;
+  if (!bytes || B <= 0 || Tq <= 0 || N <= 0) return CSA_ERR_INVALID;
+  *bytes = CSA_WS_HEADER_BYTES + topk_bytes(B, Tq, N);
+  return CSA_OK;
 }
 
 csa_status csa_index_topk_workspace(int B, int Tq, int N, int H_I, int d_I, int k, size_t* bytes) {
@@ -194,7 +251,7 @@ csa_status csa_index_topk_workspace(int B, int Tq, int N, int H_I, int d_I, int 
   (void)d_I;
   (void)k;
   if (!bytes || B <= 0 || Tq <= 0 || N <= 0) return CSA_ERR_INVALID;
-  *bytes = CSA_WS_HEADER_BYTES + scores_bytes(B, Tq, N);
+  *bytes = CSA_WS_HEADER_BYTES + scores_bytes(B, Tq, N) + topk_bytes(B, Tq, N);
   return CSA_OK;
 }
 
@@ -213,11 +270,9 @@ csa_status csa_index_topk(const void* q_idx, const void* k_idx, const float* w,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* S = reinterpret_cast<float*>(static_cast<char*>(ws) + CSA_WS_HEADER_BYTES);
   const long long ld = scores_ld(N);
-  csa::IndexerArgs ia{q_idx, k_idx, w, q_pos, S, ld, B, Tq, N, H_I, d_I, m, err_word(ws), g_wait_budget};
-  st = cuda_status(csa::launch_indexer(ia, s));
-  if (st != CSA_OK) return st;
-  csa::TopkArgs ta{S, ld, q_pos, B, Tq, N, m, k, idx_out, score_out};
-  return cuda_status(csa::launch_topk(ta, s));
+  csa::IndexerArgs ia{q_idx, k_idx, w, q_pos, S, ld, B, Tq, N, H_I, d_I, m, err_word(ws), g_wait_budget, nullptr};
+  csa::TopkArgs ta{S, ld, q_pos, B, Tq, N, m, k, idx_out, score_out, nullptr, nullptr, nullptr, nullptr};
+  return index_then_topk(ia, ta, reinterpret_cast<char*>(S) + scores_bytes(B, Tq, N), s);
 }
 
 // ---------------------------------------------------------------- (4)
@@ -302,7 +357,7 @@ csa_status hca_attend(const void* q, const void* k_cmp, const void* v_cmp, const
 // ---------------------------------------------------------------- layer
 csa_status csa_layer_workspace(const csa_layer_args* a, size_t* bytes) {
   if (!a || !bytes || a->B <= 0 || a->Tq <= 0 || a->N <= 0 || a->k <= 0) return CSA_ERR_INVALID;
-  size_t total = CSA_WS_HEADER_BYTES + scores_bytes(a->B, a->Tq, a->N);
+  size_t total = CSA_WS_HEADER_BYTES + scores_bytes(a->B, a->Tq, a->N) + topk_bytes(a->B, a->Tq, a->N);
   if (!a->idx_out) total += align_up(static_cast<size_t>(a->B) * a->Tq * a->k * 4, kAlignWs);
   total += attend_part_bytes(a->B, a->Tq, a->k + a->W, a->H, a->d);
   *bytes = total;
@@ -340,6 +395,8 @@ csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* s
   char* base = static_cast<char*>(ws) + CSA_WS_HEADER_BYTES;
   float* S = reinterpret_cast<float*>(base);
   base += scores_bytes(a->B, a->Tq, a->N);
+  void* tk = base;
+  base += topk_bytes(a->B, a->Tq, a->N);
   if (!idx) {
     idx = reinterpret_cast<int32_t*>(base);
     base += align_up(static_cast<size_t>(a->B) * a->Tq * a->k * 4, kAlignWs);
@@ -369,11 +426,9 @@ csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* s
   }
   const long long ld = scores_ld(a->N);
   csa::IndexerArgs ia{a->q_idx, a->i_cmp, a->w, a->q_pos, S, ld, a->B, a->Tq, a->N, a->H_I, a->d_I,
-                      a->m, err_word(ws), g_wait_budget};
-  st = cuda_status(csa::launch_indexer(ia, s));
-  if (st != CSA_OK) return st;
-  csa::TopkArgs ta{S, ld, a->q_pos, a->B, a->Tq, a->N, a->m, a->k, idx, nullptr};
-  st = cuda_status(csa::launch_topk(ta, s));
+                      a->m, err_word(ws), g_wait_budget, nullptr};
+  csa::TopkArgs ta{S, ld, a->q_pos, a->B, a->Tq, a->N, a->m, a->k, idx, nullptr, nullptr, nullptr, nullptr, nullptr};
+  st = index_then_topk(ia, ta, tk, s);
   if (st != CSA_OK) return st;
   const int n_keys_max = a->k + a->W;
   const csa::AttendPlan plan =

@@ -48,6 +48,7 @@ struct KParams {
   int tmem_cols;
   uint32_t* errw;
   long long budget;
+  uint32_t* hist;  // [B*Tq][kTopkBins] (G == 1 only), or nullptr
 };
 
 struct __align__(8) Bars {
@@ -62,12 +63,15 @@ template <int HI>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
                    KParams p) {
+  pdl_wait_then_release();
   extern __shared__ __align__(1024) char smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle atoms
   char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   char* qs = smem;                                      // [kh][NC][128 B]
   char* ks = qs + p.kh * p.NC * 128;                    // [stages][kh][128][128 B]
   Bars* bars = reinterpret_cast<Bars*>(ks + p.stages * p.kh * kHalfBytes);
+  // top-k bucket histogram of this CTA's scores (one query per group)
+  uint32_t* hist_s = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(bars) + sizeof(Bars));
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ float w_s[HI];
@@ -93,6 +97,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     nvis_s[jj] = nv;
   }
   for (int h = tid; h < HI; h += kThreads) w_s[h] = p.w[h];
+  if (p.hist)
+    for (int i = tid; i < kTopkBins; i += kThreads) hist_s[i] = 0u;
   if (tid == 0) {
     abort_flag = 0;
     for (int s = 0; s < p.stages; ++s) {
@@ -212,17 +218,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t col0 = lane_addr + static_cast<uint32_t>(acc * p.NC);
       if constexpr (HI >= 16) {
         for (int jj = 0; jj < p.G; ++jj) {
+          // all of the query's head columns in flight at once, one wait
+          uint32_t r[HI / 16][16];
+#pragma unroll
+          for (int hc = 0; hc < HI / 16; ++hc) tmem_ld16(col0 + jj * HI + hc * 16, r[hc]);
+          tmem_ld_wait();
           float sum = 0.f;
 #pragma unroll
-          for (int hc = 0; hc < HI / 16; ++hc) {
-            uint32_t r[16];
-            tmem_ld16(col0 + jj * HI + hc * 16, r);
-            tmem_ld_wait();
+          for (int hc = 0; hc < HI / 16; ++hc)
 #pragma unroll
-            for (int e = 0; e < 16; ++e) sum = fmaf(w_s[hc * 16 + e], fmaxf(__uint_as_float(r[e]), 0.f), sum);
+            for (int e = 0; e < 16; ++e) sum = fmaf(w_s[hc * 16 + e], fmaxf(__uint_as_float(r[hc][e]), 0.f), sum);
+          const bool vis = key < nvis_s[jj];
+          if (vis) p.S[(static_cast<long long>(b) * p.Tq + j0 + jj) * p.ld + key] = sum;
+          if (p.hist) {
+            // bucket = top 12 bits of the order-preserving key of sum (sum >= 0 unless w < 0)
+            uint32_t u = __float_as_uint(sum);
+            u = u == 0x80000000u ? 0u : u;
+            u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+            const unsigned am = __ballot_sync(0xffffffffu, vis);
+            if (vis) {
+              const unsigned peers = __match_any_sync(am, u >> 20);
+              if (lane == __ffs(peers) - 1) atomicAdd(&hist_s[u >> 20], static_cast<uint32_t>(__popc(peers)));
+            }
           }
-          if (key < nvis_s[jj])
-            p.S[(static_cast<long long>(b) * p.Tq + j0 + jj) * p.ld + key] = sum;
         }
       } else {
         constexpr int QPC = 16 / HI;  // queries per 16-column chunk
@@ -253,6 +271,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tbase, p.tmem_cols);
+  }
+  if (p.hist) {
+    uint32_t* g = p.hist + (static_cast<long long>(b) * p.Tq + j0) * kTopkBins;
+    for (int i = tid; i < kTopkBins; i += kThreads)
+      if (hist_s[i]) atomicAdd(g + i, hist_s[i]);
   }
 }
 
@@ -295,7 +318,8 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   p.tmem_cols = cols;
   const int q_bytes = p.kh * p.NC * 128;
   const int stage_bytes = p.kh * kHalfBytes;
-  int stages = (kSmemBudget - 1024 - q_bytes - static_cast<int>(sizeof(Bars))) / stage_bytes;
+  const int hist_bytes = (a.hist != nullptr && p.G == 1 && HI >= 16) ? kTopkBins * 4 : 0;
+  int stages = (kSmemBudget - 1024 - q_bytes - static_cast<int>(sizeof(Bars)) - hist_bytes) / stage_bytes;
   stages = stages > 8 ? 8 : stages;
   if (stages < 2) return cudaErrorNotSupported;
   p.stages = stages;
@@ -308,6 +332,7 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   p.items_per_group = (n_tiles_all + p.tiles_per_item - 1) / p.tiles_per_item;
   p.errw = a.errw;
   p.budget = a.budget;
+  p.hist = (a.hist != nullptr && p.G == 1 && HI >= 16) ? a.hist : nullptr;
   const long long items = groups * p.items_per_group;
   if (items == 0 || n_tiles_all == 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorNotSupported;
@@ -338,14 +363,16 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const size_t smem = 1024 + q_bytes + static_cast<size_t>(stages) * stage_bytes + sizeof(Bars);
+  const size_t smem = 1024 + q_bytes + static_cast<size_t>(stages) * stage_bytes + sizeof(Bars) + hist_bytes;
   cudaError_t e = ensure_dyn_smem<indexer_kernel<HI>>(static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  indexer_kernel<HI><<<static_cast<unsigned>(items), kThreads, smem, s>>>(tmk, tmq, p);
-  return cudaGetLastError();
+  return launch_k(indexer_kernel<HI>, dim3(static_cast<unsigned>(items)), dim3(kThreads), smem, s, 1, tmk, tmq,
+                  p);
 }
 
 }  // namespace
+
+bool indexer_fills_hist(int Tq, int H_I) { return Tq == 1 && H_I >= 16; }
 
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
   switch (a.H_I) {

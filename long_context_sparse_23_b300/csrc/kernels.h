@@ -29,11 +29,19 @@ struct IndexerArgs {
   int B, Tq, N, H_I, d_I, m;
   uint32_t* errw;
   long long budget;
+  uint32_t* hist;  // [B*Tq][kTopkBins] top-k bucket histogram to accumulate into, or nullptr
 };
 // returns cudaErrorNotSupported for shapes outside the instantiated set
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s);
+// whether launch_indexer fills IndexerArgs::hist for this shape (else it is ignored)
+bool indexer_fills_hist(int Tq, int H_I);
 
 // ---- (3) top-k --------------------------------------------------------------
+constexpr int kTopkBins = 4096;        // buckets of 12 key bits (two levels: bits 31..20, 19..8)
+constexpr int kTopkChunk = 4096;       // keys per candidate-select CTA (long rows)
+constexpr int kTopkShortMax = 16384;   // rows up to this length are selected in shared memory
+constexpr int kTopkMaxN = 1 << 24;
+
 struct TopkArgs {
   const float* scores;
   long long ld;
@@ -41,9 +49,25 @@ struct TopkArgs {
   int B, Tq, N, m, k;
   int32_t* idx_out;
   float* score_out;
+  // long-row scratch (topk_scratch_carve): the two bucket histograms, and per
+  // chunk a candidate count and a candidate list of (key, index) pairs
+  uint32_t* hist;
+  uint32_t* hist2;
+  uint32_t* ccount;
+  uint2* cand;
 };
-cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 bool topk_supported(int N);
+bool topk_long_rows(int N);
+// bytes of long-row scratch for nq queries (0 for short rows), and of its
+// leading part that must be zero before the histogram is accumulated
+size_t topk_scratch_bytes(long long nq, int N);
+size_t topk_scratch_zero_bytes(long long nq);
+void topk_scratch_carve(TopkArgs& a, void* base, long long nq);
+// hist_ready: the histogram was already accumulated (by the indexer) into a
+// zeroed scratch; otherwise the scratch is zeroed and the histogram built here.
+cudaError_t launch_topk(const TopkArgs& a, bool hist_ready, cudaStream_t s);
+// zero the leading (histogram) part of the long-row scratch carved into ``a``
+cudaError_t launch_topk_zero(const TopkArgs& a, long long nq, cudaStream_t s);
 
 // ---- (4) attention ----------------------------------------------------------
 struct AttendArgs {
@@ -66,6 +90,7 @@ struct AttendArgs {
 struct AttendPlan {
   int nsplit;
   int tiles_per_split;
+  int mode;  // 0: one split; 1: split partials in the workspace + combine kernel; 2: cluster merge
   size_t part_bytes;
 };
 AttendPlan plan_attend(int Tq, long long nq, int n_keys_max, int H, int d);

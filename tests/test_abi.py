@@ -46,19 +46,28 @@ def test_status_strings_and_version(L):
 def test_workspace_sizes(L):
     need = ctypes.c_size_t(0)
     assert L.csa_index_topk_workspace(4, 1, 262144, 64, 128, 1024, ctypes.byref(need)) == 0
-    assert need.value == 256 + 4 * 262144 * 4
+    # long rows: two bucket histograms, then per 4096-key chunk a count and a candidate list
+    topk_scratch = (4 * 2 * 4096 * 4 + 4 * 64 * 4 + 4 * 262144 * 8 + 255) // 256 * 256
+    assert need.value == 256 + 4 * 262144 * 4 + topk_scratch
+    assert L.csa_topk_workspace(4, 1, 262144, 1024, ctypes.byref(need)) == 0
+    assert need.value == 256 + topk_scratch
+    assert L.csa_topk_workspace(8192, 1, 2048, 1024, ctypes.byref(need)) == 0
+    assert need.value == 256                       # short rows: selected in shared memory
     assert L.csa_index_topk_workspace(1, 1, 5, 64, 128, 4, ctypes.byref(need)) == 0
     assert need.value == 256 + 256                # 8 floats rounded up to 256 bytes
     assert L.csa_attend_workspace(64, 1, 64, 128, 1024, 128, ctypes.byref(need)) == 0
-    splits = (1152 // 64 + 1) // 2                 # decode: 2 tiles of 64 keys per split
-    assert need.value == 256 + 64 * splits * 64 * 129 * 4
+    assert need.value == 256                       # decode: splits merge inside a thread-block cluster
     assert L.csa_attend_workspace(1, 8192, 16, 128, 1024, 128, ctypes.byref(need)) == 0
     assert need.value == 256                       # prefill: no split partials
-    # batch-invariant split plan: per-sequence bytes scale linearly with B
+    assert L.hca_attend_workspace(8, 1, 8192, 64, 128, 128, ctypes.byref(need)) == 0
+    assert need.value == 256                       # 130 tiles: 15 splits of 9 tiles, one cluster
+    # more than 16 * 128 tiles: split partials in the workspace (18 splits of 128 tiles here),
+    # batch-invariant: per-sequence bytes scale linearly with B
     a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
-    L.hca_attend_workspace(1, 1, 8192, 64, 128, 128, ctypes.byref(a))
-    L.hca_attend_workspace(8, 1, 8192, 64, 128, 128, ctypes.byref(b))
-    assert b.value - 256 == 8 * (a.value - 256)
+    L.hca_attend_workspace(1, 1, 140000, 64, 128, 128, ctypes.byref(a))
+    L.hca_attend_workspace(8, 1, 140000, 64, 128, 128, ctypes.byref(b))
+    assert a.value == 256 + (18 * 64 * 129 * 4 + 255) // 256 * 256
+    assert b.value - 256 == (8 * 18 * 64 * 129 * 4 + 255) // 256 * 256
     assert L.csa_attend_workspace(0, 1, 64, 128, 16, 8, ctypes.byref(need)) == _lib.CSA_ERR_INVALID
 
 
@@ -91,7 +100,7 @@ def test_validation_before_any_launch(L):
     targs = [A16, 64, A16, 1, 1, 64, 4, 16, A16, None, A16, 256, None]
     t = list(targs); t[7] = 5000
     assert L.csa_topk(*t) == _lib.CSA_ERR_UNSUPPORTED
-    t = list(targs); t[5] = 16 * 49152 + 1; t[1] = 16 * 49152 + 4
+    t = list(targs); t[5] = (1 << 24) + 1; t[1] = (1 << 24) + 4
     assert L.csa_topk(*t) == _lib.CSA_ERR_UNSUPPORTED
     t = list(targs); t[7] = 0
     assert L.csa_topk(*t) == _lib.CSA_ERR_INVALID

@@ -126,3 +126,10 @@ def test_attend_bad_indices_are_flagged_and_skipped():
     # a window that falls outside the raw buffer is flagged too
     csa.csa_attend(q, kc, vc, clean, kr, vr, torch.tensor([190], dtype=torch.int32, device="cuda"), qp, W + 10, ws=ws)
     assert ws.check_error() == 2
+
+
+def test_hca_long_list_partials_in_workspace():
+    """140000 entries at m = 1 (over 16 x 128 key tiles): the splits keep their
+    partials in the workspace and merge in the combine kernel."""
+    pos = np.array([[139999, 70000]])
+    _attn_case(12, 1, 2, 140000, 16, 128, 0, 128, 1, pos, 140000, 0, hca=True)
