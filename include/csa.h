@@ -179,17 +179,17 @@ csa_status csa_attend(const void* q, const void* k_cmp, const void* v_cmp, const
  *
  * Arguments, layouts, results and the argument errors are those of
  * csa_attend; inputs and outputs are still caller-owned device memory.  Key
- * lists of up to 16 * 128 tiles of 64 keys (k + W <= 131072) merge their
- * split partials inside a thread-block cluster and need no scratch at all;
- * longer lists keep their split partials in one fixed device array of
- * CSA_NOALLOC_SCRATCH_BYTES inside the library instead of a workspace.
- * Every GPU that loads the library holds that array until the process exits,
- * and no call allocates or frees anything.
+ * lists of up to 131072 keys (k + W) merge their split partials inside a
+ * thread-block cluster and need no scratch at all; longer lists keep their
+ * split partials in one fixed device array of CSA_NOALLOC_SCRATCH_BYTES
+ * inside the library instead of a workspace.  Every GPU that loads the
+ * library holds that array until the process exits, and no call allocates
+ * or frees anything.
  * - Returns CSA_ERR_WORKSPACE when the call's partials would exceed
- *   CSA_NOALLOC_SCRATCH_BYTES: with n_tiles = ceil((k + W) / 64) > 2048, a
- *   call splits every query's keys into n_split = ceil(n_tiles / 128)
- *   ranges and needs B * Tq * n_split * H * (d + 1) * 4 bytes (for example
- *   k + W = 139392, H = 64, d = 128: 594 KB per query, at most 56 queries).
+ *   CSA_NOALLOC_SCRATCH_BYTES: a list of k + W > 131072 keys is split into
+ *   n_split = ceil((k + W) / 8192) ranges and needs
+ *   B * Tq * n_split * H * (d + 1) * 4 bytes (for example k + W = 139392,
+ *   H = 64, d = 128: 594 KB per query, at most 56 queries).
  * - The first call on a device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
  * - Every call on a device shares the one array, which keeps the last call's

@@ -32,9 +32,7 @@ namespace csa {
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kTile = 64;  // keys per tile
-constexpr int kMaxTilesPerCta = 128;
+constexpr int kMaxKeysPerCta = 8192;  // slot codes staged in shared memory
 constexpr int kMaxCluster = 16;  // CTAs of one query merged through distributed shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -70,23 +68,118 @@ __device__ __forceinline__ int swz(int r, int ch) {
   return r * (D * 2) + ((ch ^ (r & 7)) << 4);
 }
 
+// One warp's share of one staged tile: keys [key0, key0 + KW) of the K/V
+// tile (rows addressed through swz), slot codes cs[0 .. KW) (-1 = no key),
+// for the warp's 16 query heads (fragments qf).  S = Q K^T on mma.sync, the
+// online softmax in the log2 domain (sl2 = scale * log2 e), then O += P V.
+// Updates the running (o, m, l) of the warp's rows g and g + 8.
+template <int D, int KW>
+__device__ __forceinline__ void tile_step(const uint32_t (&qf)[D / 16][4], const char* Kt, const char* Vt,
+                                          int key0, const int* cs, float sl2, float (&o)[D / 8][4], float& m0,
+                                          float& m1, float& l0, float& l1) {
+  constexpr int NT = KW / 8;  // S n-tiles
+  constexpr int DT = D / 8;   // O n-tiles
+  const int lane = threadIdx.x & 31, c = lane & 3;
+  bool any = false;
+#pragma unroll
+  for (int i = 0; i < KW; i += 32) any |= __any_sync(0xffffffffu, cs[min(i + lane, KW - 1)] != -1);
+  if (!any) return;
+  // ---- S = Q K^T over this warp's KW keys
+  float s[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+    for (int jp = 0; jp < NT / 2; ++jp) {
+      uint32_t r[4];
+      const int key = key0 + jp * 16 + ((lane >> 4) << 3) + (lane & 7);
+      const int ch = 2 * kk + ((lane >> 3) & 1);
+      ldsm_x4(r, Kt + swz<D>(key, ch));
+      mma_16816(s[2 * jp], qf[kk], r[0], r[1]);
+      mma_16816(s[2 * jp + 1], qf[kk], r[2], r[3]);
+    }
+  }
+  // ---- online softmax (log2 domain)
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const float b0 = cs[8 * j + 2 * c] != -1 ? 0.f : -INFINITY;
+    const float b1 = cs[8 * j + 2 * c + 1] != -1 ? 0.f : -INFINITY;
+    s[j][0] = fmaf(s[j][0], sl2, b0);
+    s[j][1] = fmaf(s[j][1], sl2, b1);
+    s[j][2] = fmaf(s[j][2], sl2, b0);
+    s[j][3] = fmaf(s[j][3], sl2, b1);
+    mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
+    mx1 = fmaxf(mx1, fmaxf(s[j][2], s[j][3]));
+  }
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+  const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+  const float r0 = n0 == -INFINITY ? 0.f : n0;
+  const float r1 = n1 == -INFINITY ? 0.f : n1;
+  const float al0 = ex2(m0 - r0), al1 = ex2(m1 - r1);
+  m0 = n0;
+  m1 = n1;
+  l0 *= al0;
+  l1 *= al1;
+#pragma unroll
+  for (int i = 0; i < DT; ++i) {
+    o[i][0] *= al0;
+    o[i][1] *= al0;
+    o[i][2] *= al1;
+    o[i][3] *= al1;
+  }
+  uint32_t pf[KW / 16][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const float p0 = ex2(s[j][0] - r0), p1 = ex2(s[j][1] - r0);
+    const float p2 = ex2(s[j][2] - r1), p3 = ex2(s[j][3] - r1);
+    l0 += p0 + p1;
+    l1 += p2 + p3;
+    pf[j >> 1][(j & 1) * 2 + 0] = pack_bf16x2(p0, p1);
+    pf[j >> 1][(j & 1) * 2 + 1] = pack_bf16x2(p2, p3);
+  }
+  // ---- O += P V
+#pragma unroll
+  for (int kk = 0; kk < KW / 16; ++kk) {
+    // A fragment order: (g, k-lo), (g+8, k-lo), (g, k-hi), (g+8, k-hi)
+    const uint32_t af[4] = {pf[kk][0], pf[kk][1], pf[kk][2], pf[kk][3]};
+#pragma unroll
+    for (int dp = 0; dp < DT / 2; ++dp) {
+      uint32_t r[4];
+      const int key = key0 + kk * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
+      const int ch = 2 * dp + (lane >> 4);
+      ldsm_x4_t(r, Vt + swz<D>(key, ch));
+      mma_16816(o[2 * dp], af, r[0], r[1]);
+      mma_16816(o[2 * dp + 1], af, r[2], r[3]);
+    }
+  }
+}
+
 // mode: 0 = one split (write the output), 1 = split partials to global
 // memory (merged by attend_combine_kernel), 2 = the splits of a query form a
 // thread-block cluster and merge through distributed shared memory.
-template <int D, int HG>
-__global__ void __launch_bounds__(kThreads) attend_kernel(AttendArgs a, int nsplit, int tps, int mode) {
+// NW warps per CTA (4: 64-key tiles, 8: 128-key tiles); warp = (head group
+// of 16, key sub-range), each warp owns 16 * HG keys of every tile.
+template <int D, int HG, int NW>
+__global__ void __launch_bounds__(32 * NW) attend_kernel(AttendArgs a, int nsplit, int tps, int mode) {
   pdl_wait_then_release();
-  constexpr int KS = 4 / HG;      // key sub-ranges per tile
-  constexpr int KW = kTile / KS;  // keys per warp per tile: 64, 32, 16
+  constexpr int kThreads = 32 * NW;
+  constexpr int kTile = 16 * NW;  // keys per tile
+  constexpr int KS = NW / HG;     // key sub-ranges per tile
+  constexpr int KW = kTile / KS;  // keys per warp per tile: 16 * HG
   constexpr int CH = D / 8;       // 16-byte chunks per row
-  constexpr int NT = KW / 8;      // S n-tiles per warp
   constexpr int DT = D / 8;       // O n-tiles
   constexpr int TILE_BYTES = kTile * D * 2;
 
   extern __shared__ __align__(128) char smem[];
-  char* Ks = smem;                    // [2][kTile][D]
-  char* Vs = smem + 2 * TILE_BYTES;   // [2][kTile][D]
-  int* codes = reinterpret_cast<int*>(smem + 4 * TILE_BYTES);  // [tps * kTile] slot row codes
+  const int nstage = tps > 1 ? 2 : 1;         // one tile per CTA needs no second buffer
+  char* Ks = smem;                            // [nstage][kTile][D]
+  char* Vs = smem + nstage * TILE_BYTES;      // [nstage][kTile][D]
+  int* codes = reinterpret_cast<int*>(smem + 2 * nstage * TILE_BYTES);  // [tps * kTile] slot row codes
 
   const int split = blockIdx.x;
   const long long qi = blockIdx.y;
@@ -176,87 +269,8 @@ __global__ void __launch_bounds__(kThreads) attend_kernel(AttendArgs a, int nspl
     }
     __syncthreads();
 
-    const int* cs = codes + (tile - tile0) * kTile + ks * KW;
-    bool any = false;
-#pragma unroll
-    for (int i = 0; i < KW; i += 32) any |= __any_sync(0xffffffffu, cs[min(i + lane, KW - 1)] != -1);
-    if (any) {
-      const char* Kt = Ks + stage * TILE_BYTES;
-      const char* Vt = Vs + stage * TILE_BYTES;
-      // ---- S = Q K^T over this warp's KW keys
-      float s[NT][4];
-#pragma unroll
-      for (int j = 0; j < NT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-        for (int jp = 0; jp < NT / 2; ++jp) {
-          uint32_t r[4];
-          const int key = ks * KW + jp * 16 + ((lane >> 4) << 3) + (lane & 7);
-          const int ch = 2 * kk + ((lane >> 3) & 1);
-          ldsm_x4(r, Kt + swz<D>(key, ch));
-          mma_16816(s[2 * jp], qf[kk], r[0], r[1]);
-          mma_16816(s[2 * jp + 1], qf[kk], r[2], r[3]);
-        }
-      }
-      // ---- online softmax (log2 domain)
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        const float b0 = cs[8 * j + 2 * c] != -1 ? 0.f : -INFINITY;
-        const float b1 = cs[8 * j + 2 * c + 1] != -1 ? 0.f : -INFINITY;
-        s[j][0] = fmaf(s[j][0], sl2, b0);
-        s[j][1] = fmaf(s[j][1], sl2, b1);
-        s[j][2] = fmaf(s[j][2], sl2, b0);
-        s[j][3] = fmaf(s[j][3], sl2, b1);
-        mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
-        mx1 = fmaxf(mx1, fmaxf(s[j][2], s[j][3]));
-      }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-      const float r0 = n0 == -INFINITY ? 0.f : n0;
-      const float r1 = n1 == -INFINITY ? 0.f : n1;
-      const float al0 = ex2(m0 - r0), al1 = ex2(m1 - r1);
-      m0 = n0;
-      m1 = n1;
-      l0 *= al0;
-      l1 *= al1;
-#pragma unroll
-      for (int i = 0; i < DT; ++i) {
-        o[i][0] *= al0;
-        o[i][1] *= al0;
-        o[i][2] *= al1;
-        o[i][3] *= al1;
-      }
-      uint32_t pf[KW / 16][4];
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        const float p0 = ex2(s[j][0] - r0), p1 = ex2(s[j][1] - r0);
-        const float p2 = ex2(s[j][2] - r1), p3 = ex2(s[j][3] - r1);
-        l0 += p0 + p1;
-        l1 += p2 + p3;
-        pf[j >> 1][(j & 1) * 2 + 0] = pack_bf16x2(p0, p1);
-        pf[j >> 1][(j & 1) * 2 + 1] = pack_bf16x2(p2, p3);
-      }
-      // ---- O += P V
-#pragma unroll
-      for (int kk = 0; kk < KW / 16; ++kk) {
-        // A fragment order: (g, k-lo), (g+8, k-lo), (g, k-hi), (g+8, k-hi)
-        const uint32_t af[4] = {pf[kk][0], pf[kk][1], pf[kk][2], pf[kk][3]};
-#pragma unroll
-        for (int dp = 0; dp < DT / 2; ++dp) {
-          uint32_t r[4];
-          const int key = ks * KW + kk * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
-          const int ch = 2 * dp + (lane >> 4);
-          ldsm_x4_t(r, Vt + swz<D>(key, ch));
-          mma_16816(o[2 * dp], af, r[0], r[1]);
-          mma_16816(o[2 * dp + 1], af, r[2], r[3]);
-        }
-      }
-    }
+    tile_step<D, KW>(qf, Ks + stage * TILE_BYTES, Vs + stage * TILE_BYTES, ks * KW,
+                     codes + (tile - tile0) * kTile + ks * KW, sl2, o, m0, m1, l0, l1);
     __syncthreads();
   }
 
@@ -266,11 +280,115 @@ __global__ void __launch_bounds__(kThreads) attend_kernel(AttendArgs a, int nspl
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
+  const int h0 = hg * 16 + g, h1 = h0 + 8;
+  if (mode == 2) {
+    // ---- cluster merge.  Every warp's (o, m, l) over its key sub-range is
+    // one partial: partial p = rank * KS + ks of the query.  Each CTA owns a
+    // slice of the heads and folds all C * KS partials of them, in partial
+    // order, through distributed shared memory.
+    constexpr int LDO = D + 4;  // padded row: the warps' row stores do not collide on banks
+    float* po = reinterpret_cast<float*>(smem);  // [KS][H][LDO] unnormalised o
+    float* pm = po + KS * a.H * LDO;              // [KS][H] running max (log2 domain)
+    float* pl = pm + KS * a.H;                    // [KS][H] sum of exponentials
+    __syncthreads();                              // the last tile's buffers are free
+    {
+      float* mo = po + (ks * a.H) * LDO;
+#pragma unroll
+      for (int i = 0; i < DT; ++i) {
+        const int col = 8 * i + 2 * c;
+        if (h0 < a.H) *reinterpret_cast<float2*>(mo + h0 * LDO + col) = make_float2(o[i][0], o[i][1]);
+        if (h1 < a.H) *reinterpret_cast<float2*>(mo + h1 * LDO + col) = make_float2(o[i][2], o[i][3]);
+      }
+      if (c == 0) {
+        if (h0 < a.H) {
+          pm[ks * a.H + h0] = m0;
+          pl[ks * a.H + h0] = l0;
+        }
+        if (h1 < a.H) {
+          pm[ks * a.H + h1] = m1;
+          pl[ks * a.H + h1] = l1;
+        }
+      }
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    const int C = static_cast<int>(cluster.num_blocks());
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int NP = C * KS;                     // partials of the query
+    const int hpc = (a.H + C - 1) / C;         // heads per CTA
+    const int h_lo = rank * hpc;
+    const int nh = max(0, min(a.H, h_lo + hpc) - h_lo);
+    float* wm = pl + KS * a.H;                 // [nh][NP] max, then weight
+    float* wl = wm + hpc * NP;                 // [nh][NP] sum
+    for (int i = tid; i < nh * NP; i += kThreads) {
+      const int hl = i / NP, pp = i % NP;
+      const int r = pp / KS, s2 = pp % KS;
+      wm[i] = *cluster.map_shared_rank(pm + s2 * a.H + h_lo + hl, r);
+      wl[i] = *cluster.map_shared_rank(pl + s2 * a.H + h_lo + hl, r);
+    }
+    __syncthreads();
+    if (tid < nh) {
+      float* m_ = wm + tid * NP;
+      const float* l_ = wl + tid * NP;
+      float M = -INFINITY;
+      for (int pp = 0; pp < NP; ++pp) M = fmaxf(M, m_[pp]);
+      float den = 0.f;
+      for (int pp = 0; pp < NP; ++pp) {
+        const float f = M == -INFINITY ? 0.f : ex2(m_[pp] - M);
+        m_[pp] = f;
+        den = fmaf(f, l_[pp], den);
+      }
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      for (int pp = 0; pp < NP; ++pp) m_[pp] *= inv;
+      if (a.lse) a.lse[qi * a.H + h_lo + tid] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
+    }
+    __syncthreads();
+    // the slice's outputs, four columns per item; eight partials in flight
+    for (int it = tid; it < nh * (D / 4); it += kThreads) {
+      const int hl = it / (D / 4), col = 4 * (it % (D / 4));
+      const int h = h_lo + hl;
+      const float* w_ = wm + hl * NP;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int p0 = 0; p0 < NP; p0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int pp = p0 + u;
+          if (pp < NP)
+            v[u] = *reinterpret_cast<const float4*>(
+                cluster.map_shared_rank(po + ((pp % KS) * a.H + h) * LDO + col, pp / KS));
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int pp = p0 + u;
+          if (pp < NP) {
+            const float f = w_[pp];
+            acc.x = fmaf(f, v[u].x, acc.x);
+            acc.y = fmaf(f, v[u].y, acc.y);
+            acc.z = fmaf(f, v[u].z, acc.z);
+            acc.w = fmaf(f, v[u].w, acc.w);
+          }
+        }
+      }
+      const long long o0 = (qi * a.H + h) * static_cast<long long>(D) + col;
+      if (a.out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + o0) = acc;
+      } else {
+        uint2 pk;
+        pk.x = pack_bf16x2(acc.x, acc.y);
+        pk.y = pack_bf16x2(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + o0) = pk;
+      }
+    }
+    cluster.sync();  // peers may still read this CTA's partials until here
+    return;
+  }
+
   // ---- merge the KS key sub-ranges of each head group (shared memory)
   if constexpr (KS > 1) {
-    float* xo = reinterpret_cast<float*>(smem);                 // [4 warps][16][D]
-    float* xm = reinterpret_cast<float*>(smem + 4 * 16 * D * 4);  // [4 warps][16]
-    float* xl = xm + 4 * 16;
+    float* xo = reinterpret_cast<float*>(smem);                   // [NW warps][16][D]
+    float* xm = reinterpret_cast<float*>(smem + NW * 16 * D * 4);  // [NW warps][16]
+    float* xl = xm + NW * 16;
     float* mo = xo + warp * 16 * D;
 #pragma unroll
     for (int i = 0; i < DT; ++i) {
@@ -316,94 +434,6 @@ __global__ void __launch_bounds__(kThreads) attend_kernel(AttendArgs a, int nspl
       l0 = L0;
       l1 = L1;
     }
-  }
-  const int h0 = hg * 16 + g, h1 = h0 + 8;
-  if (mode == 2) {
-    // ---- cluster merge: every CTA publishes (o, m, l) in its shared memory,
-    // then owns a slice of the (head, column) outputs and folds the cluster's
-    // partials into it in split order
-    float* po = reinterpret_cast<float*>(smem);   // [H][D] unnormalised
-    float* pm = po + a.H * D;                      // [H] running max (log2 domain)
-    float* pl = pm + a.H;                          // [H] sum of exponentials
-    __syncthreads();                               // the merge above is done with smem
-    if (ks == 0) {
-#pragma unroll
-      for (int i = 0; i < DT; ++i) {
-        const int col = 8 * i + 2 * c;
-        if (h0 < a.H) *reinterpret_cast<float2*>(po + h0 * D + col) = make_float2(o[i][0], o[i][1]);
-        if (h1 < a.H) *reinterpret_cast<float2*>(po + h1 * D + col) = make_float2(o[i][2], o[i][3]);
-      }
-      if (c == 0) {
-        if (h0 < a.H) {
-          pm[h0] = m0;
-          pl[h0] = l0;
-        }
-        if (h1 < a.H) {
-          pm[h1] = m1;
-          pl[h1] = l1;
-        }
-      }
-    }
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();
-    const int C = static_cast<int>(cluster.num_blocks());
-    const int rank = static_cast<int>(cluster.block_rank());
-    // every split's (max, sum) of every head, fetched once into local shared
-    // memory (after the partial o, which nothing overwrites)
-    float* wgt = pl + a.H;  // [kMaxCluster][H] weights 2^(m_r - M) / L
-    for (int i = tid; i < C * a.H; i += kThreads) {
-      const int r = i / a.H, h = i % a.H;
-      wgt[i] = *cluster.map_shared_rank(pm + h, r);
-      wgt[kMaxCluster * a.H + i] = *cluster.map_shared_rank(pl + h, r);
-    }
-    __syncthreads();
-    if (tid < a.H) {
-      const int h = tid;
-      float M = -INFINITY;
-      for (int r = 0; r < C; ++r) M = fmaxf(M, wgt[r * a.H + h]);
-      float den = 0.f;
-      for (int r = 0; r < C; ++r) {
-        const float f = M == -INFINITY ? 0.f : ex2(wgt[r * a.H + h] - M);
-        wgt[r * a.H + h] = f;
-        den = fmaf(f, wgt[kMaxCluster * a.H + r * a.H + h], den);
-      }
-      const float inv = den > 0.f ? 1.f / den : 0.f;
-      for (int r = 0; r < C; ++r) wgt[r * a.H + h] *= inv;
-      if (a.lse && rank == 0) a.lse[qi * a.H + h] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
-    }
-    __syncthreads();
-    // this CTA's slice of the output, four columns per thread, all splits'
-    // partials requested before any is used
-    const int n4 = a.H * D / 4;
-    for (int e4 = rank * kThreads + tid; e4 < n4; e4 += C * kThreads) {
-      const int h = (4 * e4) / D;
-      float4 v[kMaxCluster];
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r)
-        if (r < C) v[r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(po + 4 * e4, r));
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) {
-        if (r < C) {
-          const float f = wgt[r * a.H + h];
-          acc.x = fmaf(f, v[r].x, acc.x);
-          acc.y = fmaf(f, v[r].y, acc.y);
-          acc.z = fmaf(f, v[r].z, acc.z);
-          acc.w = fmaf(f, v[r].w, acc.w);
-        }
-      }
-      const long long o0 = qi * static_cast<long long>(a.H) * D + 4 * e4;
-      if (a.out_f32) {
-        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + o0) = acc;
-      } else {
-        uint2 pk;
-        pk.x = pack_bf16x2(acc.x, acc.y);
-        pk.y = pack_bf16x2(acc.z, acc.w);
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + o0) = pk;
-      }
-    }
-    cluster.sync();  // peers may still read this CTA's partials until here
-    return;
   }
   if (ks != 0) return;
 
@@ -458,6 +488,240 @@ __global__ void __launch_bounds__(kThreads) attend_kernel(AttendArgs a, int nspl
   }
 }
 
+// Decode-shaped calls (few queries per sequence): CTA = (key range, group of
+// 16 heads, query).  The 8 warps own 16 keys each of every 128-key tile, so
+// a CTA's tiles (at most a few) are gathered up front through a cp.async
+// ring of up to three stages.  The warps' partials merge in shared memory
+// (padded rows, no bank conflicts) into one (O, max, sum) per head, and the
+// key ranges of one (query, head group) -- a thread-block cluster along x --
+// fold their partials into the output through distributed shared memory:
+// range r owns heads [r * hpc, (r + 1) * hpc) of the group and reads every
+// range's partial of them, in range order.
+template <int D>
+__global__ void __launch_bounds__(256) attend_decode_kernel(AttendArgs a, int tpr) {
+  pdl_wait_then_release();
+  constexpr int kThreads = 256, kTile = 128, KW = 16, NWD = 8;
+  constexpr int CH = D / 8, DT = D / 8;
+  constexpr int TILE_BYTES = kTile * D * 2;
+  constexpr int LDO = D + 4;  // padded partial rows
+  extern __shared__ __align__(128) char smem[];
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int gh = blockIdx.y;
+  const long long qi = blockIdx.z;
+  const int b = static_cast<int>(qi / a.Tq);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int nstage = tpr < 3 ? tpr : 3;
+  char* Ks = smem;                                                     // [nstage][kTile][D]
+  char* Vs = smem + nstage * TILE_BYTES;                               // [nstage][kTile][D]
+  int* codes = reinterpret_cast<int*>(smem + 2 * nstage * TILE_BYTES);  // [tpr * kTile]
+
+  const int t = a.q_pos[qi];
+  int n_c;
+  if (a.idx) {
+    n_c = a.k;
+  } else {
+    n_c = t >= 0 ? (t + 1) / a.m : 0;
+    n_c = n_c < a.N ? n_c : a.N;
+  }
+  const int n_tiles = (n_c + a.W + kTile - 1) / kTile;
+  const int tile0 = rank * tpr;
+  const int tile1 = min(n_tiles, tile0 + tpr);
+  const int ntile = max(0, tile1 - tile0);
+
+  // Q fragments of the group's heads (rows gh*16 + g and + 8; zero past H)
+  uint32_t qf[D / 16][4];
+  const int h0 = gh * 16 + g, h1 = h0 + 8;
+  {
+    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
+        static_cast<const char*>(a.q) + (static_cast<size_t>(qi) * a.H + h0) * D * 2);
+    const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
+        static_cast<const char*>(a.q) + (static_cast<size_t>(qi) * a.H + h1) * D * 2);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qf[kk][0] = h0 < a.H ? q0[kk * 8 + c] : 0u;
+      qf[kk][1] = h1 < a.H ? q1[kk * 8 + c] : 0u;
+      qf[kk][2] = h0 < a.H ? q0[kk * 8 + 4 + c] : 0u;
+      qf[kk][3] = h1 < a.H ? q1[kk * 8 + 4 + c] : 0u;
+    }
+  }
+  // slot codes of the range
+  {
+    const int raw_base = a.W > 0 ? a.raw_base[b] : 0;
+    bool bad = false;
+    for (int i = tid; i < ntile * kTile; i += kThreads)
+      codes[i] = slot_code(a, qi, b, t, n_c, raw_base, tile0 * kTile + i, &bad);
+    if (bad) raise_flag(a.errw, kFlagIndex);
+  }
+  __syncthreads();
+  const char* kc_base = static_cast<const char*>(a.k_cmp) + static_cast<size_t>(b) * a.N * D * 2;
+  const char* vc_base = static_cast<const char*>(a.v_cmp) + static_cast<size_t>(b) * a.N * D * 2;
+  const char* kr_base = static_cast<const char*>(a.k_raw) + static_cast<size_t>(b) * a.T_raw * D * 2;
+  const char* vr_base = static_cast<const char*>(a.v_raw) + static_cast<size_t>(b) * a.T_raw * D * 2;
+  auto load_tile = [&](int stage, int j) {
+    const int* cs = codes + j * kTile;
+#pragma unroll
+    for (int rr = 0; rr < kTile * CH / kThreads; ++rr) {
+      const int i = tid + rr * kThreads;
+      const int r = i / CH, ch = i % CH;
+      const int code = cs[r];
+      const char* kp = code >= 0 ? kc_base + static_cast<size_t>(code) * D * 2
+                                 : kr_base + static_cast<size_t>(code <= -2 ? -code - 2 : 0) * D * 2;
+      const char* vp = code >= 0 ? vc_base + static_cast<size_t>(code) * D * 2
+                                 : vr_base + static_cast<size_t>(code <= -2 ? -code - 2 : 0) * D * 2;
+      const bool valid = code != -1;
+      cp_async16(Ks + stage * TILE_BYTES + swz<D>(r, ch), valid ? kp + ch * 16 : kc_base, valid);
+      cp_async16(Vs + stage * TILE_BYTES + swz<D>(r, ch), valid ? vp + ch * 16 : vc_base, valid);
+    }
+    cp_async_commit();
+  };
+  const int S = ntile < nstage ? ntile : nstage;
+  for (int j = 0; j < S; ++j) load_tile(j, j);
+
+  float o[DT][4];
+#pragma unroll
+  for (int i = 0; i < DT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const float sl2 = a.scale * kLog2e;
+  for (int j = 0; j < ntile; ++j) {
+    // tiles committed so far: min(ntile, S + j); tile j may leave the later ones pending
+    const int pending = min(ntile, S + j) - 1 - j;
+    if (pending >= 2)
+      cp_async_wait<2>();
+    else if (pending == 1)
+      cp_async_wait<1>();
+    else
+      cp_async_wait<0>();
+    __syncthreads();
+    const int stage = j % nstage;
+    tile_step<D, KW>(qf, Ks + stage * TILE_BYTES, Vs + stage * TILE_BYTES, warp * KW, codes + j * kTile + warp * KW,
+                     sl2, o, m0, m1, l0, l1);
+    if (j + S < ntile) {
+      __syncthreads();  // every warp is done with this stage
+      load_tile(stage, j + S);
+    }
+  }
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+  // ---- the warps' partials -> one (O, max, sum) per head of the CTA
+  float* xo = reinterpret_cast<float*>(smem);  // [NWD][16][LDO]
+  float* xm = xo + NWD * 16 * LDO;              // [NWD][16]
+  float* xl = xm + NWD * 16;                    // [NWD][16]
+  float* po = xl + NWD * 16;                    // [16][LDO]  the CTA's partial, read by the cluster
+  float* pm = po + 16 * LDO;                    // [16]
+  float* pl = pm + 16;                          // [16]
+  __syncthreads();                              // the tile buffers are free
+  {
+    float* mo = xo + warp * 16 * LDO;
+#pragma unroll
+    for (int i = 0; i < DT; ++i) {
+      const int col = 8 * i + 2 * c;
+      *reinterpret_cast<float2*>(mo + g * LDO + col) = make_float2(o[i][0], o[i][1]);
+      *reinterpret_cast<float2*>(mo + (g + 8) * LDO + col) = make_float2(o[i][2], o[i][3]);
+    }
+    if (c == 0) {
+      xm[warp * 16 + g] = m0;
+      xm[warp * 16 + g + 8] = m1;
+      xl[warp * 16 + g] = l0;
+      xl[warp * 16 + g + 8] = l1;
+    }
+  }
+  __syncthreads();
+  {
+    // thread -> (row hr, 8 columns)
+    const int hr = tid >> 4, c0 = (tid & 15) * (D / 16);
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NWD; ++w) M = fmaxf(M, xm[w * 16 + hr]);
+    const float R = M == -INFINITY ? 0.f : M;
+    float f[NWD];
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < NWD; ++w) {
+      f[w] = ex2(xm[w * 16 + hr] - R);
+      L = fmaf(f[w], xl[w * 16 + hr], L);
+    }
+#pragma unroll
+    for (int cc = 0; cc < D / 16; cc += 4) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < NWD; ++w) {
+        const float4 v = *reinterpret_cast<const float4*>(xo + (w * 16 + hr) * LDO + c0 + cc);
+        acc.x = fmaf(f[w], v.x, acc.x);
+        acc.y = fmaf(f[w], v.y, acc.y);
+        acc.z = fmaf(f[w], v.z, acc.z);
+        acc.w = fmaf(f[w], v.w, acc.w);
+      }
+      *reinterpret_cast<float4*>(po + hr * LDO + c0 + cc) = acc;
+    }
+    if ((tid & 15) == 0) {
+      pm[hr] = M;
+      pl[hr] = L;
+    }
+  }
+  cluster.sync();
+  // ---- this range's heads of the group, from every range's partial
+  const int hpc = (16 + C - 1) / C;
+  const int r_lo = rank * hpc;
+  const int nr = max(0, min(16, r_lo + hpc) - r_lo);
+  for (int it = tid; it < nr * (D / 4); it += kThreads) {
+    const int hr = r_lo + it / (D / 4), col = 4 * (it % (D / 4));
+    const int h = gh * 16 + hr;
+    float mr[kMaxCluster], lr[kMaxCluster];
+    float4 v[kMaxCluster];
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) {
+      if (r < C) {
+        mr[r] = *cluster.map_shared_rank(pm + hr, r);
+        lr[r] = *cluster.map_shared_rank(pl + hr, r);
+        v[r] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(po + hr * LDO + col, r));
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r)
+      if (r < C) M = fmaxf(M, mr[r]);
+    float den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) {
+        if (r < C) {
+          const float f = ex2(mr[r] - M);
+          den = fmaf(f, lr[r], den);
+          acc.x = fmaf(f, v[r].x, acc.x);
+          acc.y = fmaf(f, v[r].y, acc.y);
+          acc.z = fmaf(f, v[r].z, acc.z);
+          acc.w = fmaf(f, v[r].w, acc.w);
+        }
+      }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    acc.x *= inv;
+    acc.y *= inv;
+    acc.z *= inv;
+    acc.w *= inv;
+    if (h < a.H) {
+      const long long o0 = (qi * a.H + h) * static_cast<long long>(D) + col;
+      if (a.out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + o0) = acc;
+      } else {
+        uint2 pk;
+        pk.x = pack_bf16x2(acc.x, acc.y);
+        pk.y = pack_bf16x2(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + o0) = pk;
+      }
+      if (a.lse && col == 0) a.lse[qi * a.H + h] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
+    }
+  }
+  cluster.sync();  // peers may still read this CTA's partial until here
+}
+
 // Merge split partials of one (query, head) in split order.
 template <int D>
 __global__ void __launch_bounds__(D) attend_combine_kernel(AttendArgs a, int nsplit) {
@@ -486,21 +750,26 @@ __global__ void __launch_bounds__(D) attend_combine_kernel(AttendArgs a, int nsp
   if (a.lse && threadIdx.x == 0) a.lse[qh] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
 }
 
-template <int D, int HG>
+template <int D, int HG, int NW>
 cudaError_t launch_impl(const AttendArgs& a, const AttendPlan& p, cudaStream_t s) {
+  constexpr int kTile = 16 * NW;
   constexpr int TILE_BYTES = kTile * D * 2;
-  constexpr int KS = 4 / HG;
-  size_t smem = 4 * TILE_BYTES + static_cast<size_t>(p.tiles_per_split) * kTile * sizeof(int);
+  constexpr int KS = NW / HG;
+  const int nstage = p.tiles_per_split > 1 ? 2 : 1;
+  size_t smem = 2 * nstage * TILE_BYTES + static_cast<size_t>(p.tiles_per_split) * kTile * sizeof(int);
   if (KS > 1) {
-    const size_t need = 4 * 16 * D * 4 + 2 * 4 * 16 * 4;
+    const size_t need = NW * 16 * D * 4 + 2 * NW * 16 * 4;
     smem = smem > need ? smem : need;
   }
   if (p.mode == 2) {
-    // the CTA's partial (o, m, l), then every split's (m, l) of every head
-    const size_t need = static_cast<size_t>(a.H) * (D + 2 + 2 * kMaxCluster) * 4;
+    // every warp's partial (o on padded rows, m, l), then the (max, sum) of
+    // this CTA's heads over all the query's partials
+    const int np = p.nsplit * KS, hpc = (a.H + p.nsplit - 1) / p.nsplit;
+    const size_t need = static_cast<size_t>(KS) * a.H * (D + 4 + 2) * 4 + 2 * static_cast<size_t>(hpc) * np * 4;
     smem = smem > need ? smem : need;
   }
-  cudaError_t e = ensure_dyn_smem<attend_kernel<D, HG>>(static_cast<int>(smem));
+  auto kern = attend_kernel<D, HG, NW>;
+  cudaError_t e = ensure_dyn_smem<attend_kernel<D, HG, NW>>(static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long nq = static_cast<long long>(a.B) * a.Tq;
   const dim3 grid(p.nsplit, static_cast<unsigned>(nq));
@@ -509,24 +778,50 @@ cudaError_t launch_impl(const AttendArgs& a, const AttendPlan& p, cudaStream_t s
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!nonportable_set[dev]) {
-      e = cudaFuncSetAttribute(attend_kernel<D, HG>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
       nonportable_set[dev] = true;
     }
   }
-  e = launch_k(attend_kernel<D, HG>, grid, dim3(kThreads), smem, s, p.mode == 2 ? p.nsplit : 1, a, p.nsplit,
-               p.tiles_per_split, p.mode);
+  e = launch_k(kern, grid, dim3(32 * NW), smem, s, p.mode == 2 ? p.nsplit : 1, a, p.nsplit, p.tiles_per_split,
+               p.mode);
   if (e != cudaSuccess || p.mode != 1) return e;
   return launch_k(attend_combine_kernel<D>, dim3(static_cast<unsigned>(nq * a.H)), dim3(D), 0, s, 1, a,
                   p.nsplit);
 }
 
 template <int D>
+cudaError_t launch_decode(const AttendArgs& a, const AttendPlan& p, cudaStream_t s) {
+  constexpr int TILE_BYTES = 128 * D * 2;
+  const int nstage = p.tiles_per_split < 3 ? p.tiles_per_split : 3;
+  size_t smem = 2 * nstage * TILE_BYTES + static_cast<size_t>(p.tiles_per_split) * 128 * sizeof(int);
+  const size_t merge = (8 * 16 * (D + 4) + 2 * 8 * 16 + 16 * (D + 4) + 2 * 16) * 4;
+  smem = smem > merge ? smem : merge;
+  auto kern = attend_decode_kernel<D>;
+  cudaError_t e = ensure_dyn_smem<attend_decode_kernel<D>>(static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  if (p.nsplit > 8) {
+    static bool nonportable_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!nonportable_set[dev]) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      nonportable_set[dev] = true;
+    }
+  }
+  const long long nq = static_cast<long long>(a.B) * a.Tq;
+  const dim3 grid(p.nsplit, (a.H + 15) / 16, static_cast<unsigned>(nq));
+  return launch_k(kern, grid, dim3(256), smem, s, p.nsplit, a, p.tiles_per_split);
+}
+
+template <int D, int NW>
 cudaError_t launch_d(const AttendArgs& a, const AttendPlan& p, cudaStream_t s) {
+  if (p.mode == 3) return launch_decode<D>(a, p, s);
   const int hg = (a.H + 15) / 16;
-  if (hg <= 1) return launch_impl<D, 1>(a, p, s);
-  if (hg <= 2) return launch_impl<D, 2>(a, p, s);
-  return launch_impl<D, 4>(a, p, s);
+  if (hg <= 1) return launch_impl<D, 1, NW>(a, p, s);
+  if (hg <= 2) return launch_impl<D, 2, NW>(a, p, s);
+  return launch_impl<D, 4, NW>(a, p, s);
 }
 
 }  // namespace
@@ -535,19 +830,39 @@ AttendPlan plan_attend(int Tq, long long nq, int n_keys_max, int H, int d) {
   // The split depends only on the queries per sequence and the key count, never
   // on the batch size or the GPU, so a sequence gives bit-identical results
   // alone or inside any batch.  Prefill-like calls (many queries per sequence)
-  // fill the GPU without splitting (up to 128 tiles per CTA); decode-like calls
-  // split every query's keys over up to kMaxCluster CTAs.  Up to kMaxCluster
-  // splits of a query run as one thread-block cluster and merge through
-  // distributed shared memory; more splits (over kMaxCluster * 128 tiles) keep
-  // their partials in the workspace and merge in a second kernel.
+  // fill the GPU with 4-warp CTAs over 64-key tiles, without splitting (up to
+  // 8192 keys per CTA); decode-like calls use 8-warp CTAs over 128-key tiles
+  // and split every query's keys over up to kMaxCluster CTAs.  Up to
+  // kMaxCluster splits of a query run as one thread-block cluster and merge
+  // through distributed shared memory; more splits (over kMaxCluster * 8192
+  // keys) keep their partials in the workspace and merge in a second kernel.
   AttendPlan p;
-  const int n_tiles = (n_keys_max + kTile - 1) / kTile;
+  p.nw = Tq >= 16 ? 4 : 8;
+  const int tile = 16 * p.nw;
+  if (Tq < 16) {
+    // decode kernel: ranges of about three 128-key tiles, up to kMaxCluster
+    // ranges (64 tiles each at most) per (query, head group)
+    const int n_tiles = (n_keys_max + tile - 1) / tile;
+    int nr = (n_tiles + 2) / 3;
+    nr = nr < 1 ? 1 : (nr > kMaxCluster ? kMaxCluster : nr);
+    int tpr = (n_tiles + nr - 1) / nr;
+    tpr = tpr < 1 ? 1 : tpr;
+    if (tpr <= kMaxKeysPerCta / tile && nq <= 65535) {
+      p.tiles_per_split = tpr;
+      p.nsplit = n_tiles > 0 ? (n_tiles + tpr - 1) / tpr : 1;
+      p.mode = 3;
+      p.part_bytes = 0;
+      return p;
+    }
+  }
+  const int max_tps = kMaxKeysPerCta / tile;
+  const int n_tiles = (n_keys_max + tile - 1) / tile;
   int tps;
   if (Tq >= 16) {
-    tps = n_tiles < kMaxTilesPerCta ? n_tiles : kMaxTilesPerCta;
+    tps = n_tiles < max_tps ? n_tiles : max_tps;
   } else {
     tps = (n_tiles + kMaxCluster - 1) / kMaxCluster;
-    tps = tps > kMaxTilesPerCta ? kMaxTilesPerCta : tps;
+    tps = tps > max_tps ? max_tps : tps;
   }
   if (tps > n_tiles) tps = n_tiles;
   if (tps < 1) tps = 1;
@@ -560,8 +875,8 @@ AttendPlan plan_attend(int Tq, long long nq, int n_keys_max, int H, int d) {
 
 cudaError_t launch_attend(const AttendArgs& a, const AttendPlan& p, cudaStream_t s) {
   if (static_cast<long long>(a.B) * a.Tq == 0) return cudaSuccess;
-  if (a.d == 128) return launch_d<128>(a, p, s);
-  if (a.d == 64) return launch_d<64>(a, p, s);
+  if (a.d == 128) return p.nw == 8 ? launch_d<128, 8>(a, p, s) : launch_d<128, 4>(a, p, s);
+  if (a.d == 64) return p.nw == 8 ? launch_d<64, 8>(a, p, s) : launch_d<64, 4>(a, p, s);
   return cudaErrorNotSupported;
 }
 

@@ -90,7 +90,10 @@ struct AttendArgs {
 struct AttendPlan {
   int nsplit;
   int tiles_per_split;
-  int mode;  // 0: one split; 1: split partials in the workspace + combine kernel; 2: cluster merge
+  // 0: one split; 1: split partials in the workspace + combine kernel; 2: cluster merge;
+  // 3: decode kernel (key ranges x 16-head groups, cluster merge)
+  int mode;
+  int nw;    // warps per CTA: 4 (64-key tiles) or 8 (128-key tiles)
   size_t part_bytes;
 };
 AttendPlan plan_attend(int Tq, long long nq, int n_keys_max, int H, int d);

@@ -102,6 +102,46 @@ __device__ __forceinline__ V block_incl_scan(V v, V* tmp) {
   return v + add;
 }
 
+// Inclusive scan of three counters per thread at once (one set of barriers).
+struct Tri {
+  uint32_t x, y, z;
+};
+template <int T>
+__device__ __forceinline__ Tri block_incl_scan3(Tri v, Tri* tmp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t nx = __shfl_up_sync(0xffffffffu, v.x, o);
+    const uint32_t ny = __shfl_up_sync(0xffffffffu, v.y, o);
+    const uint32_t nz = __shfl_up_sync(0xffffffffu, v.z, o);
+    if (lane >= o) {
+      v.x += nx;
+      v.y += ny;
+      v.z += nz;
+    }
+  }
+  if (lane == 31) tmp[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    Tri w = lane < T / 32 ? tmp[lane] : Tri{0u, 0u, 0u};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t nx = __shfl_up_sync(0xffffffffu, w.x, o);
+      const uint32_t ny = __shfl_up_sync(0xffffffffu, w.y, o);
+      const uint32_t nz = __shfl_up_sync(0xffffffffu, w.z, o);
+      if (lane >= o) {
+        w.x += nx;
+        w.y += ny;
+        w.z += nz;
+      }
+    }
+    if (lane < T / 32) tmp[lane] = w;
+  }
+  __syncthreads();
+  const Tri add = warp > 0 ? tmp[warp - 1] : Tri{0u, 0u, 0u};
+  return Tri{v.x + add.x, v.y + add.y, v.z + add.z};
+}
+
 // The bucket holding the k-th largest key, from a 4096-bin histogram in
 // global memory.  Thread t owns bins [4096 - (t+1)*P, 4096 - t*P), so a scan
 // in thread order runs from the top bucket down.  All T threads call it.
@@ -423,34 +463,6 @@ __device__ __forceinline__ void load_bins(const uint32_t* __restrict__ hist, uin
   }
 }
 
-// find_bucket on bins already loaded by load_bins
-template <int T>
-__device__ Bucket scan_bins(const uint32_t (&c)[kTopkBins / T], uint32_t k, uint32_t* tmp, Bucket* sb) {
-  constexpr int P = kTopkBins / T;
-  const int lo = kTopkBins - (static_cast<int>(threadIdx.x) + 1) * P;
-  uint32_t s = 0;
-#pragma unroll
-  for (int i = 0; i < P; ++i) s += c[i];
-  if (threadIdx.x == 0) *sb = Bucket{-1, 0u, 0u};
-  const uint32_t incl = block_incl_scan<T>(s, tmp);
-  const uint32_t excl = incl - s;
-  if (excl < k && k <= incl) {
-    uint32_t run = excl;
-#pragma unroll
-    for (int i = P - 1; i >= 0; --i) {
-      if (run + c[i] >= k) {
-        *sb = Bucket{lo + i, run, c[i]};
-        break;
-      }
-      run += c[i];
-    }
-  }
-  __syncthreads();
-  const Bucket b = *sb;
-  __syncthreads();
-  return b;
-}
-
 __global__ void __launch_bounds__(kFinThreads) topk_finish_kernel(TopkArgs a, int cap) {
   pdl_wait_then_release();
   // dynamic: per chunk count and start offset, then (cap) staged keys and indices
@@ -458,9 +470,9 @@ __global__ void __launch_bounds__(kFinThreads) topk_finish_kernel(TopkArgs a, in
   __shared__ uint32_t hist[256];
   __shared__ uint32_t tmp[32];
   __shared__ uint32_t wgt[32], weq[32];
-  __shared__ unsigned long long tmp64[32];
   __shared__ Rule rule;
-  __shared__ Bucket sb;
+  __shared__ Bucket sb, sb2;
+  __shared__ Tri tri_tmp[32];
   constexpr int NW = kFinThreads / 32;
   const long long q = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -485,31 +497,72 @@ __global__ void __launch_bounds__(kFinThreads) topk_finish_kernel(TopkArgs a, in
   uint32_t c1[kTopkBins / kFinThreads], c2[kTopkBins / kFinThreads];
   load_bins<kFinThreads>(a.hist + q * kTopkBins, c1);
   load_bins<kFinThreads>(a.hist2 + q * kTopkBins, c2);
-  for (int c = tid; c < nch; c += kFinThreads) cnt_s[c] = ccount[c];
-  const Bucket b1 = scan_bins<kFinThreads>(c1, k, tmp, &sb);
-  Bucket b2{-1, 0u, 0u};
-  if (b1.beta >= 0) b2 = scan_bins<kFinThreads>(c2, k - b1.above, tmp, &sb);
+  const int per = (nch + kFinThreads - 1) / kFinThreads;  // chunks owned by a thread
+  const int c_lo = min(nch, tid * per), c_hi = min(nch, c_lo + per);
+  Tri v{0u, 0u, 0u};
+  for (int c = c_lo; c < c_hi; ++c) {
+    const uint32_t n = ccount[c];
+    cnt_s[c] = n;
+    v.z += n;
+  }
+#pragma unroll
+  for (int i = 0; i < kTopkBins / kFinThreads; ++i) {
+    v.x += c1[i];
+    v.y += c2[i];
+  }
+  // one scan serves both bucket searches (thread order = descending buckets)
+  // and the chunk offsets
+  const Tri incl = block_incl_scan3<kFinThreads>(v, tri_tmp);
+  if (tid == 0) {
+    sb = Bucket{-1, 0u, 0u};
+    sb2 = Bucket{-1, 0u, 0u};
+  }
+  {
+    uint32_t run = incl.z - v.z;
+    for (int c = c_lo; c < c_hi; ++c) {
+      off_s[c] = run;
+      run += cnt_s[c];
+    }
+    if (tid == kFinThreads - 1) off_s[nch] = incl.z;
+  }
+  __syncthreads();
+  constexpr int P = kTopkBins / kFinThreads;
+  const int bin_lo = kTopkBins - (tid + 1) * P;
+  if (incl.x - v.x < k && k <= incl.x) {
+    uint32_t run = incl.x - v.x;
+#pragma unroll
+    for (int i = P - 1; i >= 0; --i) {
+      if (run + c1[i] >= k) {
+        sb = Bucket{bin_lo + i, run, c1[i]};
+        break;
+      }
+      run += c1[i];
+    }
+  }
+  __syncthreads();
+  const Bucket b1 = sb;
+  if (b1.beta >= 0) {
+    const uint32_t k2 = k - b1.above;
+    if (incl.y - v.y < k2 && k2 <= incl.y) {
+      uint32_t run = incl.y - v.y;
+#pragma unroll
+      for (int i = P - 1; i >= 0; --i) {
+        if (run + c2[i] >= k2) {
+          sb2 = Bucket{bin_lo + i, run, c2[i]};
+          break;
+        }
+        run += c2[i];
+      }
+    }
+  }
+  __syncthreads();
+  const Bucket b2 = sb2;
   if (b1.beta < 0 || b2.beta < 0) {
     // the histograms do not describe this row: select from the row itself
     const Rule r = digit_select<kFinThreads>(GlobalKeys{row}, n_vis, Rule{0u, 0u, k, 0u}, 24, hist, tmp, &rule);
     compact_row<kFinThreads>(GlobalKeys{row}, n_vis, r, out, sout, wgt, weq);
     return;
   }
-  // chunk start offsets in the concatenated list
-  {
-    const int per = (nch + kFinThreads - 1) / kFinThreads;
-    const int c_lo = min(nch, tid * per), c_hi = min(nch, c_lo + per);
-    uint32_t v = 0;
-    for (int c = c_lo; c < c_hi; ++c) v += cnt_s[c];
-    const uint32_t incl = block_incl_scan<kFinThreads>(v, tmp);
-    uint32_t run = incl - v;
-    for (int c = c_lo; c < c_hi; ++c) {
-      off_s[c] = run;
-      run += cnt_s[c];
-    }
-    if (tid == kFinThreads - 1) off_s[nch] = incl;
-  }
-  __syncthreads();
   const int n_all = static_cast<int>(off_s[nch]);
   const bool staged = n_all <= cap;
   if (staged) {

@@ -60,8 +60,8 @@ def test_workspace_sizes(L):
     assert L.csa_attend_workspace(1, 8192, 16, 128, 1024, 128, ctypes.byref(need)) == 0
     assert need.value == 256                       # prefill: no split partials
     assert L.hca_attend_workspace(8, 1, 8192, 64, 128, 128, ctypes.byref(need)) == 0
-    assert need.value == 256                       # 130 tiles: 15 splits of 9 tiles, one cluster
-    # more than 16 * 128 tiles: split partials in the workspace (18 splits of 128 tiles here),
+    assert need.value == 256                       # 8320 keys: 13 splits of 5 128-key tiles, one cluster
+    # more than 131072 keys: 8192-key splits with partials in the workspace (18 here),
     # batch-invariant: per-sequence bytes scale linearly with B
     a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
     L.hca_attend_workspace(1, 1, 140000, 64, 128, 128, ctypes.byref(a))

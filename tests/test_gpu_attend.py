@@ -129,7 +129,7 @@ def test_attend_bad_indices_are_flagged_and_skipped():
 
 
 def test_hca_long_list_partials_in_workspace():
-    """140000 entries at m = 1 (over 16 x 128 key tiles): the splits keep their
+    """140000 entries at m = 1 (over 131072 keys): the splits keep their
     partials in the workspace and merge in the combine kernel."""
     pos = np.array([[139999, 70000]])
     _attn_case(12, 1, 2, 140000, 16, 128, 0, 128, 1, pos, 140000, 0, hca=True)

@@ -4,8 +4,8 @@ Some callers cannot hand the library a workspace: operators hosted by a
 framework whose memory planner owns the device (they receive only their inputs
 and outputs), and latency-bound code that must never reach cudaMalloc or
 cudaFree.  csa_attend_noalloc serves them: short key lists merge their split
-partials inside a thread-block cluster, and long ones (over 2048 tiles of 64
-keys per query) keep them in one fixed device array inside the library.  These tests call it through the C
+partials inside a thread-block cluster, and long ones (over 131072 keys per
+query) keep them in one fixed device array inside the library.  These tests call it through the C
 ABI and check it against csa_attend, which takes a workspace, with the
 attention tolerance |err| <= 1e-2 + 1e-2 |ref| used by every attention test.
 
@@ -42,7 +42,7 @@ def test_noalloc_rejects_calls_beyond_its_scratch(L):
     """Partials larger than the fixed array are refused before any device work."""
     limit = _scratch_limit()
     H, d, k, W = 64, 128, 139264, 128
-    splits = -(-((k + W) // 64) // 128)               # over 2048 tiles: splits of 128 tiles, partials in scratch
+    splits = -(-(k + W) // 8192)                      # over 131072 keys: 8192-key splits, partials in scratch
     per_query = splits * H * (d + 1) * 4
     B_ok, B_bad = limit // per_query, limit // per_query + 1
     args = lambda B: (A16, A16, A16, A16, A16, A16, A16, A16, B, 1, 262144, 256, H, d, k, W, 0.0,
@@ -108,7 +108,7 @@ def test_noalloc_matches_workspace_attention_twice(L):
         return out.cpu().numpy(), lse.cpu().numpy()
 
     # two calls in a row whose split partials go through the shared array (over
-    # 2048 key tiles per query), then a 1M-decode-shaped call that merges inside
+    # 131072 keys per query), then a 1M-decode-shaped call that merges inside
     # a thread-block cluster and does not touch it
     cases = [case(21, 2, 150000, 139264, 128, 64, 128, 4 * 150000 - 1),
              case(22, 3, 140000, 135000, 64, 32, 64, 4 * 140000 - 1),
