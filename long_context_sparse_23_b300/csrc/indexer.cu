@@ -9,13 +9,16 @@
 // 128-key tile = the 128 TMEM lanes) and (query, head) pairs on N (a group of
 // G queries x H_I heads, N <= 256 columns), K = d_I.  So every epilogue thread
 // owns one key row and reduces sum_h w_h * max(acc, 0) over its own TMEM
-// columns -- no cross-thread reduction.  Warp roles per CTA (192 threads):
+// columns -- no cross-thread reduction.  Warp roles per CTA (320 threads):
 //   warp 0     TMA producer: the query group once, then key tiles into an
 //              S-stage shared-memory ring (128-byte swizzle, OOB rows zero);
 //   warp 1     allocates TMEM; one lane issues tcgen05.mma (kind::f16, bf16
 //              operands, fp32 accumulators) into two TMEM accumulator buffers;
-//   warps 2-5  epilogue: tcgen05.ld the tile's accumulators, apply ReLU and the
-//              head weights, store fp32 scores (one coalesced row per warp).
+//   warps 2-9  epilogue, two groups of four alternating tiles (group e owns
+//              TMEM accumulator buffer e): tcgen05.ld the tile's accumulators,
+//              apply ReLU and the head weights, store fp32 scores (one
+//              coalesced row per warp) and count them into the top-k bucket
+//              histogram.
 // mbarriers connect the stages (full/empty per smem stage, full/empty per
 // TMEM buffer); every wait is bounded and reports CSA_FLAG_TIMEOUT instead of
 // hanging.  Tiles past the group's last visible block are never loaded.
@@ -26,7 +29,8 @@ namespace csa {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kEpiGroups = 2;                       // epilogue warp groups, alternating tiles
+constexpr int kThreads = 64 + 128 * kEpiGroups;    // producer, MMA, epilogue warps
 constexpr int kTileKeys = 128;
 constexpr int kHalfBytes = kTileKeys * 128;  // one 64-wide K half of a key tile
 constexpr int kSmemBudget = 220 * 1024;
@@ -201,11 +205,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---- epilogue warps 2..5: TMEM lane quarter = warp % 4
+    // ---- epilogue warps 2..: TMEM lane quarter = warp % 4; group e handles
+    // the tiles i = e (mod kEpiGroups), i.e. TMEM accumulator buffer e
     const int quarter = warp & 3;
+    const int egroup = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
-    for (int i = 0; i < ntile; ++i) {
+    for (int i = egroup; i < ntile; i += kEpiGroups) {
       const int acc = i & 1;
       const uint32_t aph = (i >> 1) & 1;
       if (!mbar_wait(&bars->tfull[acc], aph, p.budget, abort_v)) {
