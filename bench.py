@@ -3,11 +3,12 @@ dominant kernel's fraction of its roofline and the CPU oracle beside it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--all]
 
-One step = one pass of the decode hot path over one batch: Lightning-Indexer
-scores -> top-k -> window-merged sparse attention (+ split combine), for the
+One step = one pass of the decode hot path over one batch: one csa_layer call
+(Lightning-Indexer scores -> top-k -> window-merged sparse attention) for the
 B=4 sequences of the 1M-token workload (262144 compressed entries each, one
-query at position 1048575).  Steps are replayed from a CUDA graph; the device
-time is taken with CUDA events on the launching stream.  Under torchrun every
+query at position 1048575), caches resident in HBM.  K steps are captured in
+one CUDA graph and replayed once as the timed region; the device time is taken
+with CUDA events on the launching stream.  Under torchrun every
 rank runs its own replica (independent sequences: weak scaling, no data-path
 collective); the reported time is the max over ranks.
 """
@@ -104,58 +105,38 @@ class ClockSampler:
 # ---------------------------------------------------------------- workload
 
 class DecodeStep:
-    """Device buffers and the two library calls of one decode step:
-    csa_index_topk (indexer scores + top-k) and csa_attend (selected entries
-    + window)."""
+    """Device buffers and the library call of one decode step: csa_layer with
+    the compressed caches given (indexer scores -> top-k -> window-merged
+    sparse attention, enqueued by one call)."""
 
     def __init__(self, name: str, device):
         import long_context_sparse_23_b300 as csa
         from long_context_sparse_23_b300 import _lib
         self.csa, self.L = csa, _lib.lib()
         self.wl = wl = S.WORKLOADS[name]
-        self.inp = S.make_inputs(wl, device)
-        B, Tq = self.inp["q_pos"].shape
+        self.inp = i = S.make_inputs(wl, device)
+        B, Tq = i["q_pos"].shape
         self.B, self.Tq = B, Tq
-        self.idx = torch.empty(B, Tq, wl.k, dtype=torch.int32, device=device)
         self.out = torch.empty(B, Tq, wl.H, wl.d, dtype=torch.bfloat16, device=device)
-        n1, n2 = ctypes.c_size_t(0), ctypes.c_size_t(0)
-        self.L.csa_index_topk_workspace(B, Tq, wl.N, wl.H_I, wl.d_I, wl.k, ctypes.byref(n1))
-        self.L.csa_attend_workspace(B, Tq, wl.H, wl.d, wl.k, wl.W, ctypes.byref(n2))
-        self.ws = csa.Workspace(max(n1.value, n2.value), device)
-
-    def index_topk(self, st):
-        i, wl = self.inp, self.wl
-        r = self.L.csa_index_topk(i["q_idx"].data_ptr(), i["i_cmp"].data_ptr(), i["w"].data_ptr(),
-                                  i["q_pos"].data_ptr(), self.B, self.Tq, wl.N, wl.H_I, wl.d_I, wl.m, wl.k,
-                                  self.idx.data_ptr(), None, self.ws.ptr, self.ws.nbytes, st)
-        assert r == 0, r
-
-    def attend(self, st):
-        i, wl = self.inp, self.wl
-        r = self.L.csa_attend(i["q"].data_ptr(), i["k_cmp"].data_ptr(), i["v_cmp"].data_ptr(),
-                              self.idx.data_ptr(), i["k_raw"].data_ptr(), i["v_raw"].data_ptr(),
-                              i["raw_base"].data_ptr(), i["q_pos"].data_ptr(), self.B, self.Tq, wl.N,
-                              wl.raw_len, wl.H, wl.d, wl.k, wl.W, 0.0, self.out.data_ptr(), 0, None,
-                              self.ws.ptr, self.ws.nbytes, st)
-        assert r == 0, r
+        self.args = csa.layer_args(B=B, Tq=Tq, N=wl.N, m=wl.m, H=wl.H, d=wl.d, H_I=wl.H_I, d_I=wl.d_I, k=wl.k,
+                                   W=wl.W, T_raw=wl.raw_len, k_cmp=i["k_cmp"], v_cmp=i["v_cmp"],
+                                   i_cmp=i["i_cmp"], k_win=i["k_raw"], v_win=i["v_raw"],
+                                   raw_base=i["raw_base"], q=i["q"], q_idx=i["q_idx"], w=i["w"],
+                                   q_pos=i["q_pos"], out=self.out)
+        need = ctypes.c_size_t(0)
+        assert self.L.csa_layer_workspace(ctypes.byref(self.args), ctypes.byref(need)) == 0
+        self.ws = csa.Workspace(need.value, device)
 
     def step(self, st):
-        self.index_topk(st)
-        self.attend(st)
+        r = self.L.csa_layer(ctypes.byref(self.args), self.ws.ptr, self.ws.nbytes, st)
+        assert r == 0, r
 
     def kernels_per_step(self):
-        """Our kernel launches in one step: the indexer, top-k (select + finish
-        for long rows, + the histogram pass when the indexer does not build
-        it; one kernel for short rows), attention (+ the split combine)."""
+        """Our kernel launches in one step: histogram zeroing, the indexer (which
+        also accumulates the top-k histogram when Tq == 1, else a histogram
+        kernel follows) and the fused top-k + attention kernel."""
         wl = self.wl
-        if wl.N > 16384:
-            topk = 2 + (0 if self.Tq == 1 and wl.H_I >= 16 else 1)
-        else:
-            topk = 1
-        need = ctypes.c_size_t(0)
-        self.L.csa_attend_workspace(1, self.Tq, wl.H, wl.d, wl.k, wl.W, ctypes.byref(need))
-        combine = 1 if need.value > 256 else 0
-        return 1 + topk + 1 + combine
+        return 3 if (self.Tq == 1 and wl.H_I >= 16) else 4
 
     # algorithmic work of the indexer launch (per visible entry: its d_I-wide bf16
     # key read once + one fp32 score written; per query: its H_I x d_I bf16 queries)
@@ -216,36 +197,29 @@ def time_steps(gk, steps, stream):
     return e0.elapsed_time(e1) / steps
 
 
-def stage_breakdown(ds: DecodeStep, steps: int, warmup: int, stream):
-    """Average device time of each library call: plain launches with CUDA
-    events between the calls on the launching stream.  Each batch of steps is
-    queued behind a GPU-side sleep, so the host has enqueued the whole batch
-    before the first kernel starts and the events time kernels back to back
-    (not host launch latency)."""
-    names = ("index_topk", "attend")
-    fns = (ds.index_topk, ds.attend)
+def layer_time(ds: DecodeStep, steps: int, warmup: int, stream):
+    """Average device time of one csa_layer call between CUDA events recorded
+    on the launching stream, from plain (non-graph) launches: each batch of
+    calls is queued behind a GPU-side sleep, so the events time back-to-back
+    kernels, not host launch latency."""
     st = stream.cuda_stream
     batch = 50
-    tot = {n: 0.0 for n in names}
-    done = 0
+    tot, done = 0.0, 0
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             ds.step(st)
         while done < steps:
             nb = min(batch, steps - done)
-            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nb)]
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(nb + 1)]
             torch.cuda._sleep(20_000_000)       # ~10 ms of GPU time to queue behind
+            ev[0].record(stream)
             for i in range(nb):
-                ev[i][0].record(stream)
-                for j, f in enumerate(fns):
-                    f(st)
-                    ev[i][j + 1].record(stream)
+                ds.step(st)
+                ev[i + 1].record(stream)
             stream.synchronize()
-            for i in range(nb):
-                for j, n in enumerate(names):
-                    tot[n] += ev[i][j].elapsed_time(ev[i][j + 1])
+            tot += sum(ev[i].elapsed_time(ev[i + 1]) for i in range(nb))
             done += nb
-    return {n: tot[n] / steps for n in names}
+    return tot / steps
 
 
 def e2e_decode(ds: DecodeStep, steps: int, warmup: int):
@@ -260,7 +234,7 @@ def e2e_decode(ds: DecodeStep, steps: int, warmup: int):
     a = csa.layer_args(B=ds.B, Tq=ds.Tq, N=wl.N, m=wl.m, H=wl.H, d=wl.d, H_I=wl.H_I, d_I=wl.d_I, k=wl.k,
                        W=wl.W, T_raw=wl.raw_len, k_cmp=i["k_cmp"], v_cmp=i["v_cmp"], i_cmp=i["i_cmp"],
                        k_win=i["k_raw"], v_win=i["v_raw"], raw_base=i["raw_base"], q=dq, q_idx=dqi,
-                       w=i["w"], q_pos=i["q_pos"], idx_out=ds.idx, out=ds.out)
+                       w=i["w"], q_pos=i["q_pos"], out=ds.out)
     need = ctypes.c_size_t(0)
     ds.L.csa_layer_workspace(ctypes.byref(a), ctypes.byref(need))
     ws = csa.Workspace(need.value)
@@ -412,13 +386,14 @@ def main():
     # the indexer's own launches inside the timed region
     ms_idx = sum(b.elapsed_time(e) for b, e in zip(ev_b, ev_e)) / K
     if args.quick:
-        stages = stage_breakdown(ds, 50, 5, stream)
+        stages = {"csa_layer_plain_launches": layer_time(ds, 50, 5, stream)}
         if rank == 0:
             print(json.dumps({"workload": args.workload, "ms_per_step": ms, "steps": K, "indexer_ms": ms_idx,
                               "stages_ms": stages, "queries_per_s": ds.B * ds.Tq * world / (ms * 1e-3),
                               "clocks": clocks}))
         return
-    stages = stage_breakdown(ds, max(20, min(args.steps, 400)), 5, stream)
+    stages = {"csa_layer_plain_launches": layer_time(ds, max(20, min(args.steps, 400)), 5, stream),
+              "indexer_in_graph": ms_idx}
     torch.cuda.synchronize()
     if world > 1:
         t = torch.tensor([ms], device=dev)
@@ -462,7 +437,7 @@ def main():
             "config": {"workload": args.workload, "B": wl.B, "context": wl.T, "entries": wl.N, "m": wl.m,
                        "H": wl.H, "d": wl.d, "H_I": wl.H_I, "d_I": wl.d_I, "k": wl.k, "W": wl.W,
                        "l2": f"inputs exceed L2: {ibytes / 1e6:.0f} MB of indexer keys streamed per step",
-                       "launch": "one CUDA graph of K unrolled steps (csa_index_topk + csa_attend)"},
+                       "launch": "one CUDA graph of K unrolled csa_layer calls (caches resident, decode)"},
             "clocks": clocks, "gpu_launches": launches, "roofline": roof,
             "e2e": {"value": e2e_qps, "unit": "queries/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "stages_ms": {k: round(v, 5) for k, v in stages.items()}, "also": extra}

@@ -233,7 +233,7 @@ csa_status csa_topk(const float* scores, int64_t ld_scores, const int32_t* q_pos
   if (!scores || !al16(scores) || ld_scores < N || ld_scores % 4 != 0) return CSA_ERR_INVALID;
   st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES + topk_bytes(B, Tq, N));
   if (st != CSA_OK) return st;
-  csa::TopkArgs a{scores, ld_scores, q_pos, B, Tq, N, m, k, idx_out, score_out, nullptr, nullptr, nullptr, nullptr};
+  csa::TopkArgs a{scores, ld_scores, q_pos, B, Tq, N, m, k, idx_out, score_out, nullptr, nullptr, nullptr, nullptr, nullptr};
   if (csa::topk_long_rows(N))
     csa::topk_scratch_carve(a, static_cast<char*>(ws) + CSA_WS_HEADER_BYTES, static_cast<long long>(B) * Tq);
   return cuda_status(csa::launch_topk(a, false, static_cast<cudaStream_t>(stream)));
@@ -271,7 +271,7 @@ csa_status csa_index_topk(const void* q_idx, const void* k_idx, const float* w,
   float* S = reinterpret_cast<float*>(static_cast<char*>(ws) + CSA_WS_HEADER_BYTES);
   const long long ld = scores_ld(N);
   csa::IndexerArgs ia{q_idx, k_idx, w, q_pos, S, ld, B, Tq, N, H_I, d_I, m, err_word(ws), g_wait_budget, nullptr};
-  csa::TopkArgs ta{S, ld, q_pos, B, Tq, N, m, k, idx_out, score_out, nullptr, nullptr, nullptr, nullptr};
+  csa::TopkArgs ta{S, ld, q_pos, B, Tq, N, m, k, idx_out, score_out, nullptr, nullptr, nullptr, nullptr, nullptr};
   return index_then_topk(ia, ta, reinterpret_cast<char*>(S) + scores_bytes(B, Tq, N), s);
 }
 
@@ -427,7 +427,65 @@ csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* s
   const long long ld = scores_ld(a->N);
   csa::IndexerArgs ia{a->q_idx, a->i_cmp, a->w, a->q_pos, S, ld, a->B, a->Tq, a->N, a->H_I, a->d_I,
                       a->m, err_word(ws), g_wait_budget, nullptr};
-  csa::TopkArgs ta{S, ld, a->q_pos, a->B, a->Tq, a->N, a->m, a->k, idx, nullptr, nullptr, nullptr, nullptr, nullptr};
+  csa::TopkArgs ta{S, ld, a->q_pos, a->B, a->Tq, a->N, a->m, a->k, idx, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  if (!do_compress && csa::tail_supported(a->Tq, a->N, a->k, a->W, a->H, a->d)) {
+    // decode: indexer (+ bucket histogram), then one fused top-k + attention kernel
+    const long long nq = static_cast<long long>(a->B) * a->Tq;
+    csa::topk_scratch_carve(ta, tk, nq);
+    const bool fused = csa::indexer_fills_hist(a->Tq, a->H_I);
+    if (fused) {
+      st = cuda_status(csa::launch_topk_zero(ta, nq, s));
+      if (st != CSA_OK) return st;
+      ia.hist = ta.hist;
+    }
+    st = cuda_status(launch_indexer_marked(ia, s));
+    if (st != CSA_OK) return st;
+    if (!fused) {
+      st = cuda_status(csa::launch_topk_hist(ta, s));
+      if (st != CSA_OK) return st;
+    }
+    csa::TailArgs tl;
+    tl.scores = S;
+    tl.ld = ld;
+    tl.q_pos = a->q_pos;
+    tl.B = a->B;
+    tl.Tq = a->Tq;
+    tl.N = a->N;
+    tl.m = a->m;
+    tl.k = a->k;
+    tl.hist = ta.hist;
+    tl.hist2 = ta.hist2;
+    tl.hist3 = ta.hist3;
+    tl.cand = ta.cand;
+    tl.idx_out = a->idx_out;
+    tl.score_out = nullptr;
+    tl.budget = g_wait_budget;
+    csa::AttendArgs& at = tl.at;
+    at.q = a->q;
+    at.k_cmp = a->k_cmp;
+    at.v_cmp = a->v_cmp;
+    at.idx = nullptr;
+    at.k_raw = a->k_win;
+    at.v_raw = a->v_win;
+    at.raw_base = a->raw_base;
+    at.q_pos = a->q_pos;
+    at.B = a->B;
+    at.Tq = a->Tq;
+    at.N = a->N;
+    at.T_raw = a->T_raw;
+    at.H = a->H;
+    at.d = a->d;
+    at.k = a->k;
+    at.W = a->W;
+    at.m = a->m;
+    at.scale = a->scale > 0.f ? a->scale : 1.0f / std::sqrt(static_cast<float>(a->d));
+    at.out = a->out;
+    at.out_f32 = a->out_dtype == CSA_F32;
+    at.lse = a->lse;
+    at.part = nullptr;
+    at.errw = err_word(ws);
+    return cuda_status(csa::launch_decode_tail(tl, s));
+  }
   st = index_then_topk(ia, ta, tk, s);
   if (st != CSA_OK) return st;
   const int n_keys_max = a->k + a->W;

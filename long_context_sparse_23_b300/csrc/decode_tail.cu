@@ -1,0 +1,518 @@
+// Fused decode tail of the CSA layer: top-k selection and window-merged
+// sparse attention for decode-shaped calls, one thread-block cluster of 16
+// CTAs per query.  "DeepSeek V4 technical review", section 2.1: the indexer's
+// top-k blocks (k = 1024) are attended together with the sliding window of
+// raw tokens (octagono "Hybrid Attention: CSA and HCA"); the selection and the
+// attention compute exactly what topk_*_kernel and attend_*_kernel compute.
+//
+// Input: the indexer's fp32 scores of the query's n_vis visible blocks and a
+// 4096-bin histogram of their order-preserving keys' top 12 bits.  Steps,
+// with a cluster barrier between them:
+//  1. CTA r scans its chunk [r*E, (r+1)*E) of the scores and keeps, in index
+//     order, every key whose bucket is >= beta, the bucket holding the k-th
+//     largest key (candidates: in global memory, staged in shared memory when
+//     they fit);
+//  2. every CTA reads the candidates of bucket beta and fixes the same exact
+//     rule (prefix, mask, k_rem) with a histogram of key bits 19..8 and at
+//     most one 8-bit pass: keys above the prefix are kept, and of the keys
+//     equal to it the k_rem with the lowest indices;
+//  3. each CTA counts its kept candidates, learns the counts of the CTAs
+//     before it, and so the rank of each kept block in ascending order; it
+//     writes idx_out and sends (rank -> block) to the CTA that attends that
+//     rank;
+//  4. CTA r attends the virtual key slots [r*S_r, (r+1)*S_r) of the query
+//     (selected blocks by rank, then the window) for every head (8 warps:
+//     4 groups of 16 heads x 2 key halves, mma.sync), merges the halves, and
+//     sends each head's (O, max, sum) to the CTA owning that head;
+//  5. each CTA folds the partials of its heads in rank order and writes the
+//     output.
+// Everything merges in a fixed order: results do not depend on scheduling.
+#include <cooperative_groups.h>
+
+#include "attend_tile.cuh"
+#include "common.cuh"
+#include "kernels.h"
+#include "select.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace csa {
+
+namespace {
+
+constexpr int kT = 256;         // threads per CTA
+constexpr int kC = kTailCluster;  // CTAs per query (one cluster)
+constexpr int kCandR = 512;     // candidates of one rank staged in shared memory
+constexpr int kRun = 64;        // consecutive scores per thread in the candidate scan
+constexpr int kBulk = 16384;    // bytes per bulk copy
+
+// Shared-memory layout (bytes), the same on host and device.
+struct TailLayout {
+  int stage;      // steps 1-2: a batch of scores, then the ranks' candidate lists
+  int kv, codes;  // step 3: the K/V tile and slot codes (overlap the above)
+  int merge;      // step 3: the two key halves' partials (overlap the K/V tile)
+  int map, recv;  // persistent: rank -> block of this CTA's slots, partials of its heads
+  int total;
+  int hpc;        // heads owned per CTA
+};
+
+__host__ __device__ inline TailLayout tail_layout(int S_r, int H, int D, int E) {
+  TailLayout L;
+  const int ldo = D + 4;
+  L.stage = 0;
+  const int scores = (E < kT * kRun ? E : kT * kRun) * 4;
+  const int lists = kC * kCandR * 8;
+  const int sel_end = scores > lists ? scores : lists;
+  L.kv = 0;
+  L.codes = L.kv + 2 * S_r * D * 2;
+  const int kv_end = L.codes + S_r * 4;
+  L.merge = 0;  // [2][H][ldo] o, then [2][H] m, [2][H] l
+  const int merge_end = L.merge + (2 * H * ldo + 4 * H) * 4;
+  int a_end = sel_end > kv_end ? sel_end : kv_end;
+  a_end = a_end > merge_end ? a_end : merge_end;
+  L.map = (a_end + 15) / 16 * 16;
+  L.recv = L.map + (S_r * 4 + 15) / 16 * 16;
+  L.hpc = (H + kC - 1) / kC;
+  L.total = L.recv + (L.hpc * kC * ldo + 2 * L.hpc * kC) * 4;
+  return L;
+}
+
+// One-dimensional bulk copy (TMA) global -> this CTA's shared memory,
+// completing on ``bar``; 16-byte aligned addresses, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, int S_r) {
+  pdl_wait_then_release();
+  constexpr int LDO = D + 4;
+  constexpr int CH = D / 8, DT = D / 8;
+  extern __shared__ __align__(128) char smem[];
+  __shared__ uint32_t tmp[32];
+  __shared__ Bucket sb;
+  __shared__ Rule rule;
+  __shared__ uint32_t tot32;
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int r = static_cast<int>(cluster.block_rank());
+  const long long q = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const AttendArgs& at = a.at;
+  const int H = at.H;
+  const TailLayout L = tail_layout(S_r, H, D, E);
+  int* map = reinterpret_cast<int*>(smem + L.map);
+  float* recv = reinterpret_cast<float*>(smem + L.recv);  // [hpc][kC][LDO]
+  float* recv_m = recv + L.hpc * kC * LDO;                // [hpc][kC]
+  float* recv_l = recv_m + L.hpc * kC;                    // [hpc][kC]
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t n_own_s;                            // this rank's candidates, read by the cluster
+  __shared__ uint32_t rcnt[kC], wg[kT / 32], we[kT / 32];
+  uint32_t bar_phase = 0;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  // wait for the bulk copies on ``bar`` (bounded; a timeout is reported)
+  auto bulk_wait = [&]() {
+    if (!mbar_wait(&bar, bar_phase, a.budget, nullptr)) raise_flag(at.errw, kFlagTimeout);
+    bar_phase ^= 1u;
+  };
+
+  const int b = static_cast<int>(q / at.Tq);
+  const int t = a.q_pos[q];
+  int n_vis = t >= 0 ? (t + 1) / a.m : 0;
+  n_vis = n_vis < a.N ? n_vis : a.N;
+  const int k = a.k;
+  const int K_total = k + at.W;
+  const int A = (K_total + S_r - 1) / S_r;  // CTAs with key slots
+  const bool all = n_vis <= k;              // every visible block is kept (uniform over the cluster)
+  const float* row = a.scores + q * a.ld;
+  uint2* gl_all = a.cand + q * static_cast<long long>(kC) * E;  // [kC][E]
+  const int lo = r * E, hi = min(n_vis, lo + E);
+
+  Bucket b1{0, 0u, 0u};
+  if (!all) {
+    b1 = find_bucket<kT>(a.hist + q * kTopkBins, static_cast<uint32_t>(k), tmp, &sb);
+    if (b1.beta < 0) {
+      // the histogram does not describe the row (uniform): report and write nothing
+      if (r == 0 && tid == 0) raise_flag(at.errw, kFlagIndex);
+      return;
+    }
+  }
+
+  // ---- 1. candidates of this CTA's chunk, in index order; the keys of
+  // bucket beta also count into the second-level histogram (bits 19..8)
+  uint32_t n_own = 0;
+  if (!all) {
+    const uint32_t beta = static_cast<uint32_t>(b1.beta);
+    uint2* gl = gl_all + static_cast<long long>(r) * E;
+    uint32_t* hist2 = a.hist2 + q * kTopkBins;
+    float* stage = reinterpret_cast<float*>(smem + L.stage);  // [kT * kRun] scores of the batch
+    for (int sub = lo; sub < hi; sub += kT * kRun) {
+      // the batch's scores to shared memory by bulk copy (rounded up to 4
+      // scores: the row holds ld >= N, a multiple of 4)
+      const uint32_t bytes = static_cast<uint32_t>(min(kT * kRun, ((hi - sub) + 3) & ~3)) * 4;
+      if (tid == 0) {
+        fence_proxy_async();  // the stage was read by the threads of the last batch
+        mbar_expect_tx(&bar, bytes);
+        for (uint32_t off = 0; off < bytes; off += kBulk)
+          bulk_g2s(reinterpret_cast<char*>(stage) + off, reinterpret_cast<const char*>(row + sub) + off,
+                   min(static_cast<uint32_t>(kBulk), bytes - off), &bar);
+      }
+      bulk_wait();
+      // thread tid owns the run [sub + kRun*tid, sub + kRun*(tid+1)); its 16
+      // float4 reads start at a rotated position (fewer bank conflicts)
+      const int i0 = sub + kRun * tid;
+      unsigned long long take = 0ull;
+#pragma unroll
+      for (int jr = 0; jr < kRun / 4; ++jr) {
+        const int j = (jr + tid) & (kRun / 4 - 1);
+        const float4 fv = *reinterpret_cast<const float4*>(stage + kRun * tid + 4 * j);
+        const float v4[4] = {fv.x, fv.y, fv.z, fv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t key = score_key(v4[e]);
+          const bool in = i0 + 4 * j + e < hi;
+          if (in && (key >> 20) >= beta) take |= 1ull << (4 * j + e);
+          // bucket beta holds about k of the keys: one reduction per key of it
+          if (in && (key >> 20) == beta) atomicAdd(hist2 + ((key >> 8) & (kTopkBins - 1)), 1u);
+        }
+      }
+      const uint32_t mine = static_cast<uint32_t>(__popcll(take));
+      const uint32_t incl = block_incl_scan<kT>(mine, tmp);
+      if (tid == kT - 1) tot32 = incl;
+      __syncthreads();
+      uint32_t pos = n_own + incl - mine;
+      while (take) {
+        const int p = __ffsll(static_cast<long long>(take)) - 1;
+        take &= take - 1;
+        gl[pos++] = make_uint2(score_key(stage[kRun * tid + p]), static_cast<uint32_t>(i0 + p));
+      }
+      n_own += tot32;
+      __syncthreads();  // the stage and tot32 are rewritten by the next batch
+    }
+  }
+  if (tid == 0) n_own_s = n_own;
+  cluster.sync();  // #1: every rank's candidates and bucket counts are written
+
+  // ---- 2. the rule, and this CTA's ranks of the selection (every CTA reads
+  // all candidates, so no further exchange is needed before the attention)
+  if (all) {
+    for (int j = tid; j < S_r; j += kT) {
+      const int pos = r * S_r + j;
+      map[j] = pos < n_vis ? pos : -1;
+    }
+    if (a.idx_out) {
+      for (int p = r * kT + tid; p < k; p += kC * kT) {
+        a.idx_out[q * k + p] = p < n_vis ? p : -1;
+        if (a.score_out) a.score_out[q * k + p] = p < n_vis ? key_score(score_key(row[p])) : 0.f;
+      }
+    }
+  } else {
+    if (tid < kC) rcnt[tid] = *cluster.map_shared_rank(&n_own_s, tid);
+    __syncthreads();
+    bool staged = true;
+    for (int i = 0; i < kC; ++i) staged = staged && rcnt[i] <= static_cast<uint32_t>(kCandR);
+    uint2* lists = reinterpret_cast<uint2*>(smem + L.stage);  // [kC][kCandR]
+    if (staged && tid == 0) {
+      uint32_t total = 0;
+      for (int i = 0; i < kC; ++i) total += (rcnt[i] + 1) / 2 * 16;
+      fence_proxy_async();  // the stage held the scores, read by the threads
+      mbar_expect_tx(&bar, total);
+      for (int i = 0; i < kC; ++i)
+        if (rcnt[i]) bulk_g2s(lists + i * kCandR, gl_all + static_cast<long long>(i) * E, (rcnt[i] + 1) / 2 * 16, &bar);
+    }
+    // the rule's top 24 bits while the lists arrive
+    const uint32_t beta = static_cast<uint32_t>(b1.beta);
+    const uint32_t k2 = static_cast<uint32_t>(k) - b1.above;
+    const Bucket b2 = find_bucket<kT>(a.hist2 + q * kTopkBins, k2, tmp, &sb);
+    Rule rl{(beta << 20) | (static_cast<uint32_t>(b2.beta) << 8), 0xFFFFFF00u, k2 - b2.above, 0u};
+    rl.done = (b2.beta >= 0 && b2.hb == rl.k_rem) ? 1u : 0u;
+    if (staged) bulk_wait();
+    // candidate c of rank i
+    auto cand_at = [&](int i, int c) -> uint2 {
+      return staged ? lists[i * kCandR + c] : gl_all[static_cast<long long>(i) * E + c];
+    };
+    if (!rl.done) {
+      // the last 8 bits among the keys with this 24-bit prefix (few keys)
+      __shared__ uint32_t hbin[256];
+      if (tid < 256) hbin[tid] = 0u;
+      if (tid == 0) rule = rl;
+      __syncthreads();
+      for (int i = 0; i < kC; ++i) {
+        const int n = static_cast<int>(rcnt[i]);
+        for (int c = tid; c < n; c += kT) {
+          const uint32_t key = cand_at(i, c).x;
+          if ((key & rl.mask) == rl.prefix) atomicAdd(&hbin[key & 255u], 1u);
+        }
+      }
+      __syncthreads();
+      pick_digit<kT>(hbin, rl, 0, tmp, &rule);
+      rl = rule;
+      __syncthreads();
+    }
+    // ordered compaction: warp w walks ranks [w*RPW, (w+1)*RPW) (index order)
+    constexpr int NW = kT / 32, RPW = kC / NW;
+    uint32_t ngt = 0, neq = 0;
+    for (int i = warp * RPW; i < (warp + 1) * RPW; ++i) {
+      const int n = static_cast<int>(rcnt[i]);
+      for (int base = 0; base < n; base += 32) {
+        const int c = base + lane;
+        const uint32_t key = c < n ? cand_at(i, c).x & rl.mask : 0u;
+        ngt += __popc(__ballot_sync(0xffffffffu, c < n && key > rl.prefix));
+        neq += __popc(__ballot_sync(0xffffffffu, c < n && key == rl.prefix));
+      }
+    }
+    if (lane == 0) {
+      wg[warp] = ngt;
+      we[warp] = neq;
+    }
+    __syncthreads();
+    uint32_t run_gt = 0, run_eq = 0;
+    for (int w = 0; w < warp; ++w) {
+      run_gt += wg[w];
+      run_eq += we[w];
+    }
+    const unsigned ltm = lanemask_lt();
+    const int p_lo = r * S_r, p_hi = p_lo + S_r;
+    for (int i = warp * RPW; i < (warp + 1) * RPW; ++i) {
+      const int n = static_cast<int>(rcnt[i]);
+      for (int base = 0; base < n; base += 32) {
+        const int c = base + lane;
+        const uint2 cv = c < n ? cand_at(i, c) : make_uint2(0u, 0u);
+        const uint32_t key = cv.x & rl.mask;
+        const bool gt = c < n && key > rl.prefix;
+        const bool eq = c < n && key == rl.prefix;
+        const unsigned bgt = __ballot_sync(0xffffffffu, gt);
+        const unsigned beq = __ballot_sync(0xffffffffu, eq);
+        const uint32_t gt_b = run_gt + __popc(bgt & ltm);
+        const uint32_t eq_b = run_eq + __popc(beq & ltm);
+        if (gt || (eq && eq_b < rl.k_rem)) {
+          const int pos = static_cast<int>(gt_b + min(eq_b, rl.k_rem));
+          if (pos >= p_lo && pos < p_hi) {  // this CTA attends that rank and reports it
+            map[pos - p_lo] = static_cast<int>(cv.y);
+            if (a.idx_out) a.idx_out[q * k + pos] = static_cast<int32_t>(cv.y);
+            if (a.score_out) a.score_out[q * k + pos] = key_score(cv.x);
+          }
+        }
+        run_gt += __popc(bgt);
+        run_eq += __popc(beq);
+      }
+    }
+  }
+  __syncthreads();  // this CTA's map is complete
+
+  // ---- 4. attention over this CTA's key slots
+  if (r < A) {
+    char* Ks = smem + L.kv;
+    char* Vs = Ks + S_r * D * 2;
+    int* codes = reinterpret_cast<int*>(smem + L.codes);
+    const int s0 = r * S_r;
+    const int raw_base = at.W > 0 ? at.raw_base[b] : 0;
+    bool bad = false;
+    for (int j = tid; j < S_r; j += kT) {
+      const int s = s0 + j;
+      int code = -1;
+      if (s < k) {
+        code = map[j];
+      } else if (s < K_total) {
+        const int u = t - at.W + 1 + (s - k);
+        if (u >= 0) {
+          const int rr = u - raw_base;
+          if (rr < 0 || rr >= at.T_raw)
+            bad = true;
+          else
+            code = -rr - 2;
+        }
+      }
+      codes[j] = code;
+    }
+    if (bad) raise_flag(at.errw, kFlagIndex);
+    __syncthreads();
+    const char* kc_base = static_cast<const char*>(at.k_cmp) + static_cast<size_t>(b) * at.N * D * 2;
+    const char* vc_base = static_cast<const char*>(at.v_cmp) + static_cast<size_t>(b) * at.N * D * 2;
+    const char* kr_base = static_cast<const char*>(at.k_raw) + static_cast<size_t>(b) * at.T_raw * D * 2;
+    const char* vr_base = static_cast<const char*>(at.v_raw) + static_cast<size_t>(b) * at.T_raw * D * 2;
+    for (int i = tid; i < S_r * CH; i += kT) {
+      const int rw = i / CH, ch = i % CH;
+      const int code = codes[rw];
+      const char* kp = code >= 0 ? kc_base + static_cast<size_t>(code) * D * 2
+                                 : kr_base + static_cast<size_t>(code <= -2 ? -code - 2 : 0) * D * 2;
+      const char* vp = code >= 0 ? vc_base + static_cast<size_t>(code) * D * 2
+                                 : vr_base + static_cast<size_t>(code <= -2 ? -code - 2 : 0) * D * 2;
+      const bool valid = code != -1;
+      cp_async16(Ks + swz<D>(rw, ch), valid ? kp + ch * 16 : kc_base, valid);
+      cp_async16(Vs + swz<D>(rw, ch), valid ? vp + ch * 16 : vc_base, valid);
+    }
+    cp_async_commit();
+    // Q fragments of head group hg (rows hg*16 + g and + 8)
+    const int hg = warp & 3, kh = warp >> 2;
+    const int g = lane >> 2, c = lane & 3;
+    const int h0 = hg * 16 + g, h1 = h0 + 8;
+    uint32_t qf[D / 16][4];
+    {
+      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
+          static_cast<const char*>(at.q) + (static_cast<size_t>(q) * H + h0) * D * 2);
+      const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
+          static_cast<const char*>(at.q) + (static_cast<size_t>(q) * H + h1) * D * 2);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        qf[kk][0] = h0 < H ? q0[kk * 8 + c] : 0u;
+        qf[kk][1] = h1 < H ? q1[kk * 8 + c] : 0u;
+        qf[kk][2] = h0 < H ? q0[kk * 8 + 4 + c] : 0u;
+        qf[kk][3] = h1 < H ? q1[kk * 8 + 4 + c] : 0u;
+      }
+    }
+    float o[DT][4];
+#pragma unroll
+    for (int i = 0; i < DT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const float sl2 = at.scale * kLog2e;
+    cp_async_wait<0>();
+    __syncthreads();
+    if (hg * 16 < H) {
+      const int half = S_r / 2;
+      for (int kb = 0; kb < half; kb += 16)
+        tile_step<D, 16>(qf, Ks, Vs, kh * half + kb, codes + kh * half + kb, sl2, o, m0, m1, l0, l1);
+    }
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    __syncthreads();  // the K/V tile is consumed; the merge area overlaps it
+    float* xo = reinterpret_cast<float*>(smem + L.merge);  // [2][H][LDO]
+    float* xm = xo + 2 * H * LDO;                          // [2][H]
+    float* xl = xm + 2 * H;                                // [2][H]
+    if (hg * 16 < H) {
+#pragma unroll
+      for (int i = 0; i < DT; ++i) {
+        const int col = 8 * i + 2 * c;
+        if (h0 < H) *reinterpret_cast<float2*>(xo + (kh * H + h0) * LDO + col) = make_float2(o[i][0], o[i][1]);
+        if (h1 < H) *reinterpret_cast<float2*>(xo + (kh * H + h1) * LDO + col) = make_float2(o[i][2], o[i][3]);
+      }
+      if (c == 0) {
+        if (h0 < H) {
+          xm[kh * H + h0] = m0;
+          xl[kh * H + h0] = l0;
+        }
+        if (h1 < H) {
+          xm[kh * H + h1] = m1;
+          xl[kh * H + h1] = l1;
+        }
+      }
+    }
+    __syncthreads();
+    // merge the two key halves and send each head's partial to its owner
+    for (int it = tid; it < H * (D / 4); it += kT) {
+      const int h = it / (D / 4), col = 4 * (it % (D / 4));
+      const float ma = xm[h], mb = xm[H + h];
+      const float M = fmaxf(ma, mb);
+      const float R = M == -INFINITY ? 0.f : M;
+      const float fa = ex2(ma - R), fb = ex2(mb - R);
+      const float4 va = *reinterpret_cast<const float4*>(xo + h * LDO + col);
+      const float4 vb = *reinterpret_cast<const float4*>(xo + (H + h) * LDO + col);
+      float4 v;
+      v.x = fa * va.x + fb * vb.x;
+      v.y = fa * va.y + fb * vb.y;
+      v.z = fa * va.z + fb * vb.z;
+      v.w = fa * va.w + fb * vb.w;
+      const int owner = h / L.hpc, hl = h - owner * L.hpc;
+      *reinterpret_cast<float4*>(cluster.map_shared_rank(recv + (hl * kC + r) * LDO + col, owner)) = v;
+      if (col == 0) {
+        *cluster.map_shared_rank(recv_m + hl * kC + r, owner) = M;
+        *cluster.map_shared_rank(recv_l + hl * kC + r, owner) = fa * xl[h] + fb * xl[H + h];
+      }
+    }
+  }
+  cluster.sync();  // #4: every partial has arrived
+
+  // ---- 5. this CTA's heads, from the A partials in rank order
+  const int h_lo = r * L.hpc;
+  const int nh = max(0, min(H, h_lo + L.hpc) - h_lo);
+  for (int it = tid; it < nh * (D / 4); it += kT) {
+    const int hl = it / (D / 4), col = 4 * (it % (D / 4));
+    const int h = h_lo + hl;
+    float M = -INFINITY;
+    for (int p = 0; p < A; ++p) M = fmaxf(M, recv_m[hl * kC + p]);
+    float den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+      for (int p = 0; p < A; ++p) {
+        const float f = ex2(recv_m[hl * kC + p] - M);
+        den = fmaf(f, recv_l[hl * kC + p], den);
+        const float4 v = *reinterpret_cast<const float4*>(recv + (hl * kC + p) * LDO + col);
+        acc.x = fmaf(f, v.x, acc.x);
+        acc.y = fmaf(f, v.y, acc.y);
+        acc.z = fmaf(f, v.z, acc.z);
+        acc.w = fmaf(f, v.w, acc.w);
+      }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    acc.x *= inv;
+    acc.y *= inv;
+    acc.z *= inv;
+    acc.w *= inv;
+    const long long o0 = (q * H + h) * static_cast<long long>(D) + col;
+    if (at.out_f32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(at.out) + o0) = acc;
+    } else {
+      uint2 pk;
+      pk.x = pack_bf16x2(acc.x, acc.y);
+      pk.y = pack_bf16x2(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(at.out) + o0) = pk;
+    }
+    if (at.lse && col == 0) at.lse[q * H + h] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
+  }
+}
+
+}  // namespace
+
+int tail_chunk(int N) { return ((N + kC - 1) / kC + 1023) / 1024 * 1024; }
+
+int tail_slots(int k, int W) {
+  const int per = (k + W + kC - 1) / kC;
+  return (per + 31) / 32 * 32;
+}
+
+bool tail_supported(int Tq, int N, int k, int W, int H, int d) {
+  // Only the call's per-sequence shape decides (never B), so a sequence gives
+  // the same bits alone or inside any batch.  Up to kTailMinEntries entries
+  // the separate kernels (select, finish, decode attention) spread a batch
+  // over more of the GPU.
+  return Tq < 16 && N > kTailMinEntries && topk_long_rows(N) && H >= 1 && H <= 64 &&
+         (d == 64 || d == 128) && tail_slots(k, W) <= kTailMaxSlots && k + W > 0;
+}
+
+cudaError_t launch_decode_tail(const TailArgs& a, cudaStream_t s) {
+  const long long nq = static_cast<long long>(a.B) * a.Tq;
+  if (nq == 0) return cudaSuccess;
+  if (nq > 65535) return cudaErrorNotSupported;
+  const int E = tail_chunk(a.N);
+  const int S_r = tail_slots(a.k, a.at.W);
+  const TailLayout L = tail_layout(S_r, a.at.H, a.at.d, E);
+  static bool attr_set[2][64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const int which = a.at.d == 128 ? 0 : 1;
+  auto kern = a.at.d == 128 ? decode_tail_kernel<128> : decode_tail_kernel<64>;
+  if (!attr_set[which][dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    const TailLayout Lmax = tail_layout(kTailMaxSlots, 64, a.at.d, kT * kRun);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lmax.total);
+    if (e != cudaSuccess) return e;
+    attr_set[which][dev] = true;
+  }
+  return launch_k(kern, dim3(kC, static_cast<unsigned>(nq)), dim3(kT), static_cast<size_t>(L.total), s, kC, a,
+                  E, S_r);
+}
+
+size_t tail_cand_bytes_per_query(int N) { return static_cast<size_t>(kC) * tail_chunk(N) * 8; }
+
+}  // namespace csa

@@ -140,6 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmq);
       const int qrow = (b * p.Tq + j0) * HI;
+      // the keys are read once: evict-first, so the scores this kernel writes
+      // stay in L2 for the top-k that reads them next
+      const uint64_t key_policy = l2_policy_evict_first();
       mbar_expect_tx(&bars->qfull, p.kh * p.NC * 128);
       for (int h = 0; h < p.kh; ++h) tma_load_2d(qs + h * p.NC * 128, &tmq, &bars->qfull, h * 64, qrow);
       int issued = 0;
@@ -154,7 +157,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(&bars->full[s], p.kh * kHalfBytes);
         char* dst = ks + s * p.kh * kHalfBytes;
         for (int h = 0; h < p.kh; ++h)
-          tma_load_3d(dst + h * kHalfBytes, &tmk, &bars->full[s], h * 64, (tile_lo + i) * kTileKeys, b);
+          tma_load_3d_hint(dst + h * kHalfBytes, &tmk, &bars->full[s], h * 64, (tile_lo + i) * kTileKeys, b,
+                           key_policy);
         issued = i + 1;
       }
       // drain: every issued copy has landed before the CTA may exit

@@ -49,10 +49,12 @@ struct TopkArgs {
   int B, Tq, N, m, k;
   int32_t* idx_out;
   float* score_out;
-  // long-row scratch (topk_scratch_carve): the two bucket histograms, and per
-  // chunk a candidate count and a candidate list of (key, index) pairs
+  // long-row scratch (topk_scratch_carve): the bucket histograms (key bits
+  // 31..20, 19..8 and 7..0), and per chunk a candidate count and a candidate
+  // list of (key, index) pairs
   uint32_t* hist;
   uint32_t* hist2;
+  uint32_t* hist3;
   uint32_t* ccount;
   uint2* cand;
 };
@@ -98,5 +100,32 @@ struct AttendPlan {
 };
 AttendPlan plan_attend(int Tq, long long nq, int n_keys_max, int H, int d);
 cudaError_t launch_attend(const AttendArgs& a, const AttendPlan& plan, cudaStream_t s);
+
+// ---- fused decode tail: long-row top-k + attention, one cluster per query -------
+constexpr int kTailCluster = 16;    // CTAs per query
+constexpr int kTailMaxSlots = 256;  // key slots attended by one CTA
+constexpr int kTailMinEntries = 65536;  // decode calls with more entries per sequence use the fused tail
+struct TailArgs {
+  const float* scores;  // [B*Tq][ld] indexer scores
+  long long ld;
+  const int32_t* q_pos;
+  int B, Tq, N, m, k;
+  const uint32_t* hist;  // [B*Tq][kTopkBins] bucket histogram of the visible scores
+  uint32_t* hist2;       // [B*Tq][kTopkBins] zeroed: second level (key bits 19..8)
+  uint32_t* hist3;       // [B*Tq][256] zeroed: third level (key bits 7..0)
+  uint2* cand;           // [B*Tq][kTailCluster][tail_chunk(N)] candidate lists
+  int32_t* idx_out;      // [B*Tq][k] or nullptr
+  float* score_out;      // [B*Tq][k] or nullptr
+  AttendArgs at;         // queries, caches, window, output (at.idx unused)
+  long long budget;      // clock64 budget of each bounded wait
+};
+int tail_chunk(int N);
+int tail_slots(int k, int W);
+bool tail_supported(int Tq, int N, int k, int W, int H, int d);
+size_t tail_cand_bytes_per_query(int N);
+cudaError_t launch_decode_tail(const TailArgs& a, cudaStream_t s);
+// the zeroing and histogram pass of the long-row top-k alone (for callers
+// whose indexer did not accumulate the histogram)
+cudaError_t launch_topk_hist(const TopkArgs& a, cudaStream_t s);
 
 }  // namespace csa

@@ -46,8 +46,9 @@ def test_status_strings_and_version(L):
 def test_workspace_sizes(L):
     need = ctypes.c_size_t(0)
     assert L.csa_index_topk_workspace(4, 1, 262144, 64, 128, 1024, ctypes.byref(need)) == 0
-    # long rows: two bucket histograms, then per 4096-key chunk a count and a candidate list
-    topk_scratch = (4 * 2 * 4096 * 4 + 4 * 64 * 4 + 4 * 262144 * 8 + 255) // 256 * 256
+    # long rows: three bucket histograms (4096, 4096, 256 bins), then per 4096-key chunk a count,
+    # and candidate lists of (key, index) pairs for every visible entry
+    topk_scratch = (4 * (2 * 4096 + 256) * 4 + 4 * 64 * 4 + 4 * 262144 * 8 + 255) // 256 * 256
     assert need.value == 256 + 4 * 262144 * 4 + topk_scratch
     assert L.csa_topk_workspace(4, 1, 262144, 1024, ctypes.byref(need)) == 0
     assert need.value == 256 + topk_scratch

@@ -88,7 +88,7 @@ def _decode_check(wl, inp_cpu, idx, out, rows):
         sel = gidx[b, j][gidx[b, j] >= 0]
         kc = O.bf16_to_f64(bits(S.rows_bf16(wl.seed, S.TID["k_cmp"], wl.N, wl.d, b, torch.from_numpy(sel.astype(np.int64)))))
         vc = O.bf16_to_f64(bits(S.rows_bf16(wl.seed, S.TID["v_cmp"], wl.N, wl.d, b, torch.from_numpy(sel.astype(np.int64)))))
-        win = O.window_rows(t, wl.W, wl.raw_base, wl.raw_len)
+        win = O.window_rows(t, wl.W, int(c["raw_base"][b]), wl.raw_len)
         ref, _ = O.attend_one(O.bf16_to_f64(c["q"][b, j]), kc, vc, np.arange(len(sel)),
                               O.bf16_to_f64(c["k_raw"][b]), O.bf16_to_f64(c["v_raw"][b]), win, scale)
         assert_attention_close(gout[b, j], ref, f"b={b} j={j}")
@@ -125,3 +125,42 @@ def test_layer_decode_1m_and_causal_tail_agree():
     assert np.all(it[:, :3] < 262143) and np.all(it[:, :3] >= -1)
     cpu = S.make_inputs(wt, "cpu", only={"q", "q_idx", "w", "q_pos", "k_raw", "v_raw", "i_cmp"})
     _decode_check(wt, cpu, idx_t, out_t, [(b, j) for b in range(4) for j in range(4)])
+
+
+def test_layer_decode_fused_tail_matches_separate_calls():
+    """Decode csa_layer at 1M context runs the fused top-k + attention kernel;
+    csa_index_topk followed by csa_attend runs the separate kernels.  Same
+    indices, bit for bit; outputs within the attention tolerance of each other."""
+    import long_context_sparse_23_b300 as csa
+    wl = S.WORKLOADS["decode_1m"]
+    g = S.make_inputs(wl, "cuda", batches=[0, 1])
+    idx_l, out_l = _decode_layer(g, wl, out_dtype=torch.float32)
+    idx_s = csa.csa_index_topk(g["q_idx"], g["i_cmp"], g["w"], g["q_pos"], wl.m, wl.k)
+    out_s = csa.csa_attend(g["q"], g["k_cmp"], g["v_cmp"], idx_s, g["k_raw"], g["v_raw"], g["raw_base"],
+                           g["q_pos"], wl.W, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(idx_l, idx_s)
+    assert_attention_close(out_l.cpu().numpy(), out_s.double().cpu().numpy(), "fused vs separate")
+
+
+def test_layer_decode_tail_ties_and_short_visibility():
+    """The fused decode tail on degenerate inputs: every score equal (the
+    lowest indices win; the tie bucket is too large to stage), scores tied in
+    groups of eight (ties at the threshold), and a query that sees fewer
+    blocks than k (everything visible kept, -1 padding)."""
+    B, N, m, H, d, H_I, d_I, k, W = 3, 70000, 4, 64, 128, 64, 128, 1024, 128
+    wl = S.WORKLOADS["decode_128k"].replace(B=B, T=N * m, positions=(N * m - 1,), raw_len=256)
+    g = S.make_inputs(wl, "cuda")
+    g["q_idx"][0].zero_()                                      # sequence 0: all scores 0
+    g["i_cmp"][1] = g["i_cmp"][1][::8].repeat_interleave(8, 0)[:N]   # sequence 1: ties in groups of 8
+    g["q_pos"][2, 0] = 2001                                    # sequence 2: n_vis = 500 < k
+    g["raw_base"][2] = 2002 - 256
+    for name in ("k_raw", "v_raw"):                            # its window rows: tokens 1746..2001
+        g[name][2] = S.rows_bf16(wl.seed, S.TID[name], wl.T, d, 2,
+                                 torch.arange(2002 - 256, 2002, device="cuda"))
+    idx, out = _decode_layer(g, wl)
+    gi = idx.cpu().numpy()
+    np.testing.assert_array_equal(gi[0, 0], np.arange(k))
+    np.testing.assert_array_equal(gi[2, 0], np.concatenate([np.arange(500), -np.ones(k - 500, np.int32)]))
+    cpu = {key: v.cpu() for key, v in g.items()}
+    _decode_check(wl, cpu, idx, out, [(0, 0), (1, 0), (2, 0)])
