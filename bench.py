@@ -1,7 +1,7 @@
 """Benchmark: CSA decode queries/s at 1M-token context (and 128K), with the
 dominant kernel's fraction of its roofline and the CPU oracle beside it.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--all]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload W] [--quick]
 
 One step = one pass of the decode hot path over one batch: one csa_layer call
 (Lightning-Indexer scores -> top-k -> window-merged sparse attention) for the
@@ -35,10 +35,10 @@ import csa_synth as S  # noqa: E402
 HEADLINE = "decode_1m"
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
-# DRAM bytes per launch of the indexer on the 1M decode workload, from an ncu
-# capture (profiles/indexer_decode_1m.md); valid only for the source it was
-# measured on.
-TRAFFIC = {"indexer": {"src_sha": None, "bytes": None}}
+# DRAM bytes (read + write) per launch of the indexer on the 1M decode
+# workload, from an ncu capture of this launch configuration
+# (profiles/decode_1m_step.md); valid only for the source it was measured on.
+TRAFFIC = {"indexer": {"src_sha": "fda269be6187b2c2", "bytes": 273524992}}
 
 
 def _src_sha(*names):
@@ -319,6 +319,90 @@ def oracle_rate(name: str, budget_s: float, steps: int = 0, warmup: int = 0):
                                                  f"recent {n} of {n_vis} visible entries, scaled by n/n_vis")
 
 
+# ---------------------------------------------------------------- other workloads
+
+def time_calls(fn, stream, steps, warmup=3):
+    """ms per call of ``fn(stream_handle)``: ``steps`` calls captured in one
+    CUDA graph, replayed once between CUDA events (after warm-up replays)."""
+    with torch.cuda.stream(stream):
+        fn(stream.cuda_stream)
+        stream.synchronize()
+        g1 = graph_of(fn, stream)
+        gk = graph_of(fn, stream, n=steps)
+    warm(g1, warmup, stream, min_warm_s=0.1)
+    return time_steps(gk, steps, stream)
+
+
+def prefill_8k(dev, stream, steps):
+    """The whole layer over an 8192-token prefill (compress -> indexer ->
+    top-k -> attention): tokens/s, and the indexer's bf16 tensor-core rate
+    (timed inside the graph with csa_set_indexer_events)."""
+    import long_context_sparse_23_b300 as csa
+    from long_context_sparse_23_b300 import _lib
+    L = _lib.lib()
+    wl = S.WORKLOADS["prefill_8k"]
+    i = S.make_inputs(wl, dev)
+    B, T = wl.B, wl.T
+    N = T // wl.m
+    kc = torch.empty(B, N, wl.d, dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    ic = torch.empty(B, N, wl.d_I, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(B, T, wl.H, wl.d, dtype=torch.bfloat16, device=dev)
+    a = csa.layer_args(B=B, Tq=T, N=N, m=wl.m, H=wl.H, d=wl.d, H_I=wl.H_I, d_I=wl.d_I, k=wl.k, W=wl.W, T=T,
+                       T_raw=T, x_k=i["k_raw"], x_v=i["v_raw"], x_i=i["i_raw"], g_k=i["g_k"], g_v=i["g_v"],
+                       g_i=i["g_i"], k_cmp=kc, v_cmp=vc, i_cmp=ic, k_win=i["k_raw"], v_win=i["v_raw"],
+                       raw_base=i["raw_base"], q=i["q"], q_idx=i["q_idx"], w=i["w"], q_pos=i["q_pos"], out=out)
+    need = ctypes.c_size_t(0)
+    L.csa_layer_workspace(ctypes.byref(a), ctypes.byref(need))
+    ws = csa.Workspace(need.value, dev)
+
+    def step(st):
+        assert L.csa_layer(ctypes.byref(a), ws.ptr, ws.nbytes, st) == 0
+
+    ms = time_calls(step, stream, steps)
+    ev_b, ev_e = timing_events(steps, stream), timing_events(steps, stream)
+    with torch.cuda.stream(stream):
+        gk = graph_of(step, stream, n=steps, marks=(ev_b, ev_e), L=L)
+        gk.replay()
+        stream.synchronize()
+    ms_idx = sum(b.elapsed_time(e) for b, e in zip(ev_b, ev_e)) / steps
+    flops = sum(min(N, (t + 1) // wl.m) for t in range(T)) * wl.H_I * wl.d_I * 2
+    peaks, _ = _peaks()
+    tf = flops / (ms_idx * 1e-3) / 1e12
+    return {"tokens_per_s": B * T / (ms * 1e-3), "ms_per_layer": ms, "indexer_ms": ms_idx,
+            "indexer_tflops": tf, "indexer_flops": flops,
+            "indexer_frac_of_bf16_peak": tf / peaks["bf16_tflops"], "bf16_peak_tflops": peaks["bf16_tflops"]}
+
+
+def hca_decode_1m(dev, stream, steps):
+    """HCA at 1M context, B = 8: compression of the raw K/V streams at m' = 128
+    (GB/s) and the dense attention over the 8192 entries + window (queries/s)."""
+    import long_context_sparse_23_b300 as csa
+    wl = S.WORKLOADS["hca_decode_1m"]
+    i = S.make_inputs(wl, dev)
+    B, T, m = wl.B, wl.T, wl.m
+    outs = [torch.empty(B, T // m, wl.d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    out = torch.empty(B, 1, wl.H, wl.d, dtype=torch.bfloat16, device=dev)
+    ws = csa.Workspace(1 << 16, dev)
+
+    def comp(st):
+        csa.csa_compress([i["k_raw"], i["v_raw"]], [i["g_k"], i["g_v"]], m, outs=outs)
+
+    def att(st):
+        csa.hca_attend(i["q"], outs[0], outs[1], i["k_raw"], i["v_raw"], i["raw_base"], i["q_pos"], m, wl.W,
+                       ws=ws)
+
+    with torch.cuda.stream(stream):
+        ms_c = time_calls(comp, stream, max(3, steps // 20))
+        ms_a = time_calls(att, stream, steps)
+    rd = 4 * B * T * wl.d * 2
+    wr = 2 * B * (T // m) * wl.d * 2
+    peaks, _ = _peaks()
+    gbs = (rd + wr) / (ms_c * 1e-3) / 1e9
+    return {"compress_ms": ms_c, "compress_gbs": gbs, "compress_frac_of_hbm": gbs / peaks["hbm_gbs"],
+            "raw_tokens_per_s": B * T / (ms_c * 1e-3), "attend_ms": ms_a, "queries_per_s": B / (ms_a * 1e-3)}
+
+
 # ---------------------------------------------------------------- main
 
 def main():
@@ -327,7 +411,6 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--all", action="store_true", help="also time the 8K prefill and the 1M HCA decode")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--workload", default=HEADLINE, choices=["decode_1m", "decode_128k", "decode_1m_tail"],
                     help="decode workload to time (the headline is decode_1m)")
@@ -429,6 +512,10 @@ def main():
     ms2 = time_steps(gk, K2, stream)
     extra["decode_128k"] = {"queries_per_s": ds2.B * ds2.Tq / (ms2 * 1e-3), "ms_per_step": ms2}
     del ds2, g1, gk
+    torch.cuda.empty_cache()
+    extra["prefill_8k"] = prefill_8k(dev, stream, max(5, args.steps // 100))
+    torch.cuda.empty_cache()
+    extra["hca_decode_1m"] = hca_decode_1m(dev, stream, max(10, args.steps // 10))
     torch.cuda.empty_cache()
 
     line = {"metric": metric, "value": qps, "unit": "queries/s", "n_gpus": world, "steps": args.steps,

@@ -87,7 +87,9 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
-template <int D>
+// KH: keys per warp per tile step (the half of S_r a warp attends is walked
+// in steps of KH keys; KH = S_r / 2 makes it one step).
+template <int D, int KH>
 __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, int S_r) {
   pdl_wait_then_release();
   constexpr int LDO = D + 4;
@@ -169,7 +171,7 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
       // thread tid owns the run [sub + kRun*tid, sub + kRun*(tid+1)); its 16
       // float4 reads start at a rotated position (fewer bank conflicts)
       const int i0 = sub + kRun * tid;
-      unsigned long long take = 0ull;
+      unsigned long long take = 0ull, inb = 0ull;
 #pragma unroll
       for (int jr = 0; jr < kRun / 4; ++jr) {
         const int j = (jr + tid) & (kRun / 4 - 1);
@@ -177,12 +179,17 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
         const float v4[4] = {fv.x, fv.y, fv.z, fv.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const uint32_t key = score_key(v4[e]);
+          const uint32_t bin = score_key(v4[e]) >> 20;
           const bool in = i0 + 4 * j + e < hi;
-          if (in && (key >> 20) >= beta) take |= 1ull << (4 * j + e);
-          // bucket beta holds about k of the keys: one reduction per key of it
-          if (in && (key >> 20) == beta) atomicAdd(hist2 + ((key >> 8) & (kTopkBins - 1)), 1u);
+          const unsigned long long bit = 1ull << (4 * j + e);
+          take |= (in && bin >= beta) ? bit : 0ull;
+          inb |= (in && bin == beta) ? bit : 0ull;
         }
+      }
+      // bucket beta holds about k of the keys: one reduction per key of it
+      for (unsigned long long m2 = inb; m2; m2 &= m2 - 1) {
+        const int p = __ffsll(static_cast<long long>(m2)) - 1;
+        atomicAdd(hist2 + ((score_key(stage[kRun * tid + p]) >> 8) & (kTopkBins - 1)), 1u);
       }
       const uint32_t mine = static_cast<uint32_t>(__popcll(take));
       const uint32_t incl = block_incl_scan<kT>(mine, tmp);
@@ -378,8 +385,8 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     __syncthreads();
     if (hg * 16 < H) {
       const int half = S_r / 2;
-      for (int kb = 0; kb < half; kb += 16)
-        tile_step<D, 16>(qf, Ks, Vs, kh * half + kb, codes + kh * half + kb, sl2, o, m0, m1, l0, l1);
+      for (int kb = 0; kb < half; kb += KH)
+        tile_step<D, KH>(qf, Ks, Vs, kh * half + kb, codes + kh * half + kb, sl2, o, m0, m1, l0, l1);
     }
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
@@ -496,11 +503,14 @@ cudaError_t launch_decode_tail(const TailArgs& a, cudaStream_t s) {
   const int E = tail_chunk(a.N);
   const int S_r = tail_slots(a.k, a.at.W);
   const TailLayout L = tail_layout(S_r, a.at.H, a.at.d, E);
-  static bool attr_set[2][64] = {};
+  static bool attr_set[4][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  const int which = a.at.d == 128 ? 0 : 1;
-  auto kern = a.at.d == 128 ? decode_tail_kernel<128> : decode_tail_kernel<64>;
+  // one tile step of S_r / 2 keys per warp for the common slot count, else steps of 16
+  const bool kh48 = S_r == 96;
+  const int which = (a.at.d == 128 ? 0 : 2) + (kh48 ? 1 : 0);
+  auto kern = a.at.d == 128 ? (kh48 ? decode_tail_kernel<128, 48> : decode_tail_kernel<128, 16>)
+                            : (kh48 ? decode_tail_kernel<64, 48> : decode_tail_kernel<64, 16>);
   if (!attr_set[which][dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
