@@ -123,6 +123,7 @@ csa_status index_then_topk(const csa::IndexerArgs& ia_in, const csa::TopkArgs& t
       cudaError_t e = csa::launch_topk_zero(ta, nq, s);
       if (e != cudaSuccess) return CSA_ERR_CUDA;
       ia.hist = ta.hist;
+      ia.after_zero = 1;
     }
   }
   csa_status st = cuda_status(launch_indexer_marked(ia, s));
@@ -220,7 +221,7 @@ csa_status csa_index_scores(const void* q_idx, const void* k_idx, const float* w
   st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES);
   if (st != CSA_OK) return st;
   csa::IndexerArgs a{q_idx, k_idx, w, q_pos, scores, ld_scores, B, Tq, N, H_I, d_I, m,
-                     err_word(ws), g_wait_budget, nullptr};
+                     err_word(ws), g_wait_budget, nullptr, 0};
   return cuda_status(launch_indexer_marked(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -270,7 +271,7 @@ csa_status csa_index_topk(const void* q_idx, const void* k_idx, const float* w,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* S = reinterpret_cast<float*>(static_cast<char*>(ws) + CSA_WS_HEADER_BYTES);
   const long long ld = scores_ld(N);
-  csa::IndexerArgs ia{q_idx, k_idx, w, q_pos, S, ld, B, Tq, N, H_I, d_I, m, err_word(ws), g_wait_budget, nullptr};
+  csa::IndexerArgs ia{q_idx, k_idx, w, q_pos, S, ld, B, Tq, N, H_I, d_I, m, err_word(ws), g_wait_budget, nullptr, 0};
   csa::TopkArgs ta{S, ld, q_pos, B, Tq, N, m, k, idx_out, score_out, nullptr, nullptr, nullptr, nullptr, nullptr};
   return index_then_topk(ia, ta, reinterpret_cast<char*>(S) + scores_bytes(B, Tq, N), s);
 }
@@ -426,7 +427,7 @@ csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* s
   }
   const long long ld = scores_ld(a->N);
   csa::IndexerArgs ia{a->q_idx, a->i_cmp, a->w, a->q_pos, S, ld, a->B, a->Tq, a->N, a->H_I, a->d_I,
-                      a->m, err_word(ws), g_wait_budget, nullptr};
+                      a->m, err_word(ws), g_wait_budget, nullptr, 0};
   csa::TopkArgs ta{S, ld, a->q_pos, a->B, a->Tq, a->N, a->m, a->k, idx, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   if (!do_compress && csa::tail_supported(a->Tq, a->N, a->k, a->W, a->H, a->d)) {
     // decode: indexer (+ bucket histogram), then one fused top-k + attention kernel
@@ -437,6 +438,7 @@ csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* s
       st = cuda_status(csa::launch_topk_zero(ta, nq, s));
       if (st != CSA_OK) return st;
       ia.hist = ta.hist;
+      ia.after_zero = 1;
     }
     st = cuda_status(launch_indexer_marked(ia, s));
     if (st != CSA_OK) return st;

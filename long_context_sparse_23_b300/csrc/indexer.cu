@@ -53,6 +53,7 @@ struct KParams {
   uint32_t* errw;
   long long budget;
   uint32_t* hist;  // [B*Tq][kTopkBins] (G == 1 only), or nullptr
+  int after_zero;  // see IndexerArgs::after_zero
 };
 
 struct __align__(8) Bars {
@@ -67,7 +68,11 @@ template <int HI>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
                    KParams p) {
-  pdl_wait_then_release();
+  if (p.after_zero) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  } else {
+    pdl_wait_then_release();
+  }
   extern __shared__ __align__(1024) char smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle atoms
   char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -282,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tbase, p.tmem_cols);
   }
+  if (p.after_zero) asm volatile("griddepcontrol.wait;" ::: "memory");  // the histogram is zeroed
   if (p.hist) {
     uint32_t* g = p.hist + (static_cast<long long>(b) * p.Tq + j0) * kTopkBins;
     for (int i = tid; i < kTopkBins; i += kThreads)
@@ -343,6 +349,7 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   p.errw = a.errw;
   p.budget = a.budget;
   p.hist = (a.hist != nullptr && p.G == 1 && HI >= 16) ? a.hist : nullptr;
+  p.after_zero = p.hist != nullptr && a.after_zero;
   const long long items = groups * p.items_per_group;
   if (items == 0 || n_tiles_all == 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorNotSupported;

@@ -30,6 +30,10 @@ struct IndexerArgs {
   uint32_t* errw;
   long long budget;
   uint32_t* hist;  // [B*Tq][kTopkBins] top-k bucket histogram to accumulate into, or nullptr
+  // 1 when the launch directly follows the library's histogram-zeroing
+  // kernel, which itself waited for every earlier kernel: the indexer then
+  // streams at once and waits for the zeroing only before its histogram flush
+  int after_zero;
 };
 // returns cudaErrorNotSupported for shapes outside the instantiated set
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s);
