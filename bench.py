@@ -38,7 +38,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch of the indexer on the 1M decode
 # workload, from an ncu capture of this launch configuration
 # (profiles/decode_1m_step.md); valid only for the source it was measured on.
-TRAFFIC = {"indexer": {"src_sha": "fda269be6187b2c2", "bytes": 273524992}}
+TRAFFIC = {"indexer": {"src_sha": "56c3e826b66aea96", "bytes": 272958464}}
 
 
 def _src_sha(*names):
@@ -132,11 +132,17 @@ class DecodeStep:
         assert r == 0, r
 
     def kernels_per_step(self):
-        """Our kernel launches in one step: histogram zeroing, the indexer (which
-        also accumulates the top-k histogram when Tq == 1, else a histogram
-        kernel follows) and the fused top-k + attention kernel."""
+        """Our kernel launches in one csa_layer decode step.  Over 16384 entries
+        (long rows): histogram zeroing, the indexer (which also accumulates the
+        top-k histogram when Tq == 1, else a histogram kernel follows), then
+        over 65536 entries the fused top-k + attention kernel, else the select
+        and finish passes of the top-k and the decode attention."""
         wl = self.wl
-        return 3 if (self.Tq == 1 and wl.H_I >= 16) else 4
+        fused_hist = self.Tq == 1 and wl.H_I >= 16
+        if wl.N <= 16384:
+            return 3
+        n = 2 + (0 if fused_hist else 1)      # zeroing, indexer (+ histogram pass)
+        return n + (1 if wl.N > 65536 else 3)  # fused tail, or select + finish + attention
 
     # algorithmic work of the indexer launch (per visible entry: its d_I-wide bf16
     # key read once + one fp32 score written; per query: its H_I x d_I bf16 queries)

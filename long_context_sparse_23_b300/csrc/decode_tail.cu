@@ -38,6 +38,7 @@ namespace cg = cooperative_groups;
 
 namespace csa {
 
+
 namespace {
 
 constexpr int kT = 256;         // threads per CTA
@@ -49,9 +50,10 @@ constexpr int kBulk = 16384;    // bytes per bulk copy
 // Shared-memory layout (bytes), the same on host and device.
 struct TailLayout {
   int stage;      // steps 1-2: a batch of scores, then the ranks' candidate lists
-  int kv, codes;  // step 3: the K/V tile and slot codes (overlap the above)
-  int merge;      // step 3: the two key halves' partials (overlap the K/V tile)
+  int kv, codes;  // step 3: the K/V tile and slot codes (after the lists: filled during step 2)
+  int merge;      // step 3: the two key halves' partials (overlap the above once consumed)
   int map, recv;  // persistent: rank -> block of this CTA's slots, partials of its heads
+  int qs;         // persistent: the query's rows [H][D] bf16
   int total;
   int hpc;        // heads owned per CTA
 };
@@ -63,17 +65,17 @@ __host__ __device__ inline TailLayout tail_layout(int S_r, int H, int D, int E) 
   const int scores = (E < kT * kRun ? E : kT * kRun) * 4;
   const int lists = kC * kCandR * 8;
   const int sel_end = scores > lists ? scores : lists;
-  L.kv = 0;
+  L.kv = (sel_end + 127) / 128 * 128;
   L.codes = L.kv + 2 * S_r * D * 2;
   const int kv_end = L.codes + S_r * 4;
-  L.merge = 0;  // [2][H][ldo] o, then [2][H] m, [2][H] l
-  const int merge_end = L.merge + (2 * H * ldo + 4 * H) * 4;
-  int a_end = sel_end > kv_end ? sel_end : kv_end;
-  a_end = a_end > merge_end ? a_end : merge_end;
+  L.merge = 0;  // [2][H][ldo] o, then [2][H] m, [2][H] l, then [H][4] push weights
+  const int merge_end = L.merge + (2 * H * ldo + 4 * H + 4 * H) * 4;
+  const int a_end = kv_end > merge_end ? kv_end : merge_end;
   L.map = (a_end + 15) / 16 * 16;
   L.recv = L.map + (S_r * 4 + 15) / 16 * 16;
   L.hpc = (H + kC - 1) / kC;
-  L.total = L.recv + (L.hpc * kC * ldo + 2 * L.hpc * kC) * 4;
+  L.qs = L.recv + ((L.hpc * kC * ldo + 2 * L.hpc * kC) * 4 + 127) / 128 * 128;
+  L.total = L.qs + H * D * 2;
   return L;
 }
 
@@ -111,12 +113,13 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
   float* recv = reinterpret_cast<float*>(smem + L.recv);  // [hpc][kC][LDO]
   float* recv_m = recv + L.hpc * kC * LDO;                // [hpc][kC]
   float* recv_l = recv_m + L.hpc * kC;                    // [hpc][kC]
-  __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t bar, bar_q;
   __shared__ uint32_t n_own_s;                            // this rank's candidates, read by the cluster
   __shared__ uint32_t rcnt[kC], wg[kT / 32], we[kT / 32];
   uint32_t bar_phase = 0;
   if (tid == 0) {
     mbar_init(&bar, 1);
+    mbar_init(&bar_q, 1);
     mbar_fence_init();
   }
   __syncthreads();
@@ -137,13 +140,50 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
   const float* row = a.scores + q * a.ld;
   uint2* gl_all = a.cand + q * static_cast<long long>(kC) * E;  // [kC][E]
   const int lo = r * E, hi = min(n_vis, lo + E);
+  char* qs = smem + L.qs;  // the query's rows, used by step 3
+  if (r < A && tid == 0) {
+    mbar_expect_tx(&bar_q, static_cast<uint32_t>(H * D * 2));
+    bulk_g2s(qs, static_cast<const char*>(at.q) + static_cast<size_t>(q) * H * D * 2,
+             static_cast<uint32_t>(H * D * 2), &bar_q);
+  }
+  // K/V tile of this CTA's key slots; kept compressed rows are requested as
+  // soon as their rank is known (step 2), the rest in step 3
+  char* Ks = smem + L.kv;
+  char* Vs = Ks + S_r * D * 2;
+  const char* kc_base = static_cast<const char*>(at.k_cmp) + static_cast<size_t>(b) * at.N * D * 2;
+  const char* vc_base = static_cast<const char*>(at.v_cmp) + static_cast<size_t>(b) * at.N * D * 2;
+  auto gather_row = [&](int j, int row_c) {  // one lane copies compressed row row_c into slot j
+#pragma unroll
+    for (int ch = 0; ch < CH; ++ch) {
+      cp_async16(Ks + swz<D>(j, ch), kc_base + static_cast<size_t>(row_c) * D * 2 + ch * 16, true);
+      cp_async16(Vs + swz<D>(j, ch), vc_base + static_cast<size_t>(row_c) * D * 2 + ch * 16, true);
+    }
+  };
 
+  // the scores of this CTA's first batch to shared memory by bulk copy
+  // (rounded up to 4 scores: the row holds ld >= N, a multiple of 4), issued
+  // before the bucket search, which does not need them
+  float* stage = reinterpret_cast<float*>(smem + L.stage);  // [kT * kRun] scores of a batch
+  auto issue_batch = [&](int sub) {
+    const uint32_t bytes = static_cast<uint32_t>(min(kT * kRun, ((hi - sub) + 3) & ~3)) * 4;
+    if (tid == 0) {
+      fence_proxy_async();  // the stage was read by the threads of the last batch
+      mbar_expect_tx(&bar, bytes);
+      for (uint32_t off = 0; off < bytes; off += kBulk)
+        bulk_g2s(reinterpret_cast<char*>(stage) + off, reinterpret_cast<const char*>(row + sub) + off,
+                 min(static_cast<uint32_t>(kBulk), bytes - off), &bar);
+    }
+  };
+  if (!all && lo < hi) issue_batch(lo);
   Bucket b1{0, 0u, 0u};
   if (!all) {
     b1 = find_bucket<kT>(a.hist + q * kTopkBins, static_cast<uint32_t>(k), tmp, &sb);
     if (b1.beta < 0) {
-      // the histogram does not describe the row (uniform): report and write nothing
+      // the histogram does not describe the row (uniform): report and write
+      // nothing, once this CTA's copy of the query has landed
       if (r == 0 && tid == 0) raise_flag(at.errw, kFlagIndex);
+      if (r < A) mbar_wait(&bar_q, 0, a.budget, nullptr);
+      if (lo < hi) mbar_wait(&bar, 0, a.budget, nullptr);
       return;
     }
   }
@@ -155,18 +195,8 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     const uint32_t beta = static_cast<uint32_t>(b1.beta);
     uint2* gl = gl_all + static_cast<long long>(r) * E;
     uint32_t* hist2 = a.hist2 + q * kTopkBins;
-    float* stage = reinterpret_cast<float*>(smem + L.stage);  // [kT * kRun] scores of the batch
     for (int sub = lo; sub < hi; sub += kT * kRun) {
-      // the batch's scores to shared memory by bulk copy (rounded up to 4
-      // scores: the row holds ld >= N, a multiple of 4)
-      const uint32_t bytes = static_cast<uint32_t>(min(kT * kRun, ((hi - sub) + 3) & ~3)) * 4;
-      if (tid == 0) {
-        fence_proxy_async();  // the stage was read by the threads of the last batch
-        mbar_expect_tx(&bar, bytes);
-        for (uint32_t off = 0; off < bytes; off += kBulk)
-          bulk_g2s(reinterpret_cast<char*>(stage) + off, reinterpret_cast<const char*>(row + sub) + off,
-                   min(static_cast<uint32_t>(kBulk), bytes - off), &bar);
-      }
+      if (sub != lo) issue_batch(sub);  // the first batch was requested before the bucket search
       bulk_wait();
       // thread tid owns the run [sub + kRun*tid, sub + kRun*(tid+1)); its 16
       // float4 reads start at a rotated position (fewer bank conflicts)
@@ -302,8 +332,9 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
         const uint32_t eq_b = run_eq + __popc(beq & ltm);
         if (gt || (eq && eq_b < rl.k_rem)) {
           const int pos = static_cast<int>(gt_b + min(eq_b, rl.k_rem));
-          if (pos >= p_lo && pos < p_hi) {  // this CTA attends that rank and reports it
+          if (pos >= p_lo && pos < p_hi && pos < k) {  // this CTA attends that rank and reports it
             map[pos - p_lo] = static_cast<int>(cv.y);
+            gather_row(pos - p_lo, static_cast<int>(cv.y));
             if (a.idx_out) a.idx_out[q * k + pos] = static_cast<int32_t>(cv.y);
             if (a.score_out) a.score_out[q * k + pos] = key_score(cv.x);
           }
@@ -315,19 +346,19 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
   }
   __syncthreads();  // this CTA's map is complete
 
-  // ---- 4. attention over this CTA's key slots
+  // ---- 3. attention over this CTA's key slots
   if (r < A) {
-    char* Ks = smem + L.kv;
-    char* Vs = Ks + S_r * D * 2;
     int* codes = reinterpret_cast<int*>(smem + L.codes);
     const int s0 = r * S_r;
     const int raw_base = at.W > 0 ? at.raw_base[b] : 0;
     bool bad = false;
+    // slot codes: kept blocks (already requested in step 2 unless every visible
+    // block is kept), then window rows, then nothing
     for (int j = tid; j < S_r; j += kT) {
       const int s = s0 + j;
       int code = -1;
       if (s < k) {
-        code = map[j];
+        code = all ? (s < n_vis ? s : -1) : map[j];
       } else if (s < K_total) {
         const int u = t - at.W + 1 + (s - k);
         if (u >= 0) {
@@ -342,12 +373,11 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     }
     if (bad) raise_flag(at.errw, kFlagIndex);
     __syncthreads();
-    const char* kc_base = static_cast<const char*>(at.k_cmp) + static_cast<size_t>(b) * at.N * D * 2;
-    const char* vc_base = static_cast<const char*>(at.v_cmp) + static_cast<size_t>(b) * at.N * D * 2;
     const char* kr_base = static_cast<const char*>(at.k_raw) + static_cast<size_t>(b) * at.T_raw * D * 2;
     const char* vr_base = static_cast<const char*>(at.v_raw) + static_cast<size_t>(b) * at.T_raw * D * 2;
     for (int i = tid; i < S_r * CH; i += kT) {
       const int rw = i / CH, ch = i % CH;
+      if (!all && s0 + rw < k) continue;  // requested in step 2
       const int code = codes[rw];
       const char* kp = code >= 0 ? kc_base + static_cast<size_t>(code) * D * 2
                                  : kr_base + static_cast<size_t>(code <= -2 ? -code - 2 : 0) * D * 2;
@@ -358,16 +388,15 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
       cp_async16(Vs + swz<D>(rw, ch), valid ? vp + ch * 16 : vc_base, valid);
     }
     cp_async_commit();
-    // Q fragments of head group hg (rows hg*16 + g and + 8)
+    // Q fragments of head group hg (rows hg*16 + g and + 8) from shared memory
     const int hg = warp & 3, kh = warp >> 2;
     const int g = lane >> 2, c = lane & 3;
     const int h0 = hg * 16 + g, h1 = h0 + 8;
+    if (!mbar_wait(&bar_q, 0, a.budget, nullptr)) raise_flag(at.errw, kFlagTimeout);
     uint32_t qf[D / 16][4];
     {
-      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
-          static_cast<const char*>(at.q) + (static_cast<size_t>(q) * H + h0) * D * 2);
-      const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
-          static_cast<const char*>(at.q) + (static_cast<size_t>(q) * H + h1) * D * 2);
+      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qs + static_cast<size_t>(h0) * D * 2);
+      const uint32_t* q1 = reinterpret_cast<const uint32_t*>(qs + static_cast<size_t>(h1) * D * 2);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         qf[kk][0] = h0 < H ? q0[kk * 8 + c] : 0u;
@@ -415,13 +444,23 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
       }
     }
     __syncthreads();
-    // merge the two key halves and send each head's partial to its owner
-    for (int it = tid; it < H * (D / 4); it += kT) {
-      const int h = it / (D / 4), col = 4 * (it % (D / 4));
-      const float ma = xm[h], mb = xm[H + h];
+    // per head: the merged max and the two halves' weights
+    float* xw = xl + 2 * H;  // [H][4]: M, weight of half 0, weight of half 1, sum
+    if (tid < H) {
+      const float ma = xm[tid], mb = xm[H + tid];
       const float M = fmaxf(ma, mb);
       const float R = M == -INFINITY ? 0.f : M;
       const float fa = ex2(ma - R), fb = ex2(mb - R);
+      xw[4 * tid] = M;
+      xw[4 * tid + 1] = fa;
+      xw[4 * tid + 2] = fb;
+      xw[4 * tid + 3] = fa * xl[tid] + fb * xl[H + tid];
+    }
+    __syncthreads();
+    // merge the two key halves and send each head's partial to its owner
+    for (int it = tid; it < H * (D / 4); it += kT) {
+      const int h = it / (D / 4), col = 4 * (it % (D / 4));
+      const float fa = xw[4 * h + 1], fb = xw[4 * h + 2];
       const float4 va = *reinterpret_cast<const float4*>(xo + h * LDO + col);
       const float4 vb = *reinterpret_cast<const float4*>(xo + (H + h) * LDO + col);
       float4 v;
@@ -432,14 +471,14 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
       const int owner = h / L.hpc, hl = h - owner * L.hpc;
       *reinterpret_cast<float4*>(cluster.map_shared_rank(recv + (hl * kC + r) * LDO + col, owner)) = v;
       if (col == 0) {
-        *cluster.map_shared_rank(recv_m + hl * kC + r, owner) = M;
-        *cluster.map_shared_rank(recv_l + hl * kC + r, owner) = fa * xl[h] + fb * xl[H + h];
+        *cluster.map_shared_rank(recv_m + hl * kC + r, owner) = xw[4 * h];
+        *cluster.map_shared_rank(recv_l + hl * kC + r, owner) = xw[4 * h + 3];
       }
     }
   }
   cluster.sync();  // #4: every partial has arrived
 
-  // ---- 5. this CTA's heads, from the A partials in rank order
+  // ---- 4. this CTA's heads, from the A partials in rank order
   const int h_lo = r * L.hpc;
   const int nh = max(0, min(H, h_lo + L.hpc) - h_lo);
   for (int it = tid; it < nh * (D / 4); it += kT) {
@@ -493,7 +532,8 @@ bool tail_supported(int Tq, int N, int k, int W, int H, int d) {
   // the separate kernels (select, finish, decode attention) spread a batch
   // over more of the GPU.
   return Tq < 16 && N > kTailMinEntries && topk_long_rows(N) && H >= 1 && H <= 64 &&
-         (d == 64 || d == 128) && tail_slots(k, W) <= kTailMaxSlots && k + W > 0;
+         (d == 64 || d == 128) && tail_slots(k, W) <= kTailMaxSlots && k + W > 0 &&
+         tail_layout(kTailMaxSlots, 64, d, kT * kRun).total <= 220 * 1024;
 }
 
 cudaError_t launch_decode_tail(const TailArgs& a, cudaStream_t s) {
@@ -526,3 +566,4 @@ cudaError_t launch_decode_tail(const TailArgs& a, cudaStream_t s) {
 size_t tail_cand_bytes_per_query(int N) { return static_cast<size_t>(kC) * tail_chunk(N) * 8; }
 
 }  // namespace csa
+

@@ -107,7 +107,7 @@ cudaError_t launch_attend(const AttendArgs& a, const AttendPlan& plan, cudaStrea
 
 // ---- fused decode tail: long-row top-k + attention, one cluster per query -------
 constexpr int kTailCluster = 16;    // CTAs per query
-constexpr int kTailMaxSlots = 256;  // key slots attended by one CTA
+constexpr int kTailMaxSlots = 128;  // key slots attended by one CTA
 constexpr int kTailMinEntries = 65536;  // decode calls with more entries per sequence use the fused tail
 struct TailArgs {
   const float* scores;  // [B*Tq][ld] indexer scores
