@@ -598,32 +598,85 @@ __global__ void __launch_bounds__(256) attend_decode_kernel(AttendArgs a, int tp
   cluster.sync();  // peers may still read this CTA's partial until here
 }
 
-// Merge split partials of one (query, head) in split order.
+// Merge split partials of one (query, head) in split order.  The splits'
+// log2-sum-exps are read in parallel (one split per thread), their weights
+// are staged in shared memory a chunk of D splits at a time, and every thread
+// folds its column over the chunk with independent loads.
 template <int D>
 __global__ void __launch_bounds__(D) attend_combine_kernel(AttendArgs a, int nsplit) {
   pdl_wait_then_release();
+  __shared__ float wf[D];
+  __shared__ float red[D / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long qh = blockIdx.x;  // qi * H + h
   const long long qi = qh / a.H;
   const int h = static_cast<int>(qh % a.H);
   const size_t stride = D + 1;
   const float* pb = a.part + static_cast<size_t>(qi) * nsplit * a.H * stride + h * stride;
   const size_t sstride = static_cast<size_t>(a.H) * stride;
+  if (nsplit <= 32) {
+    // every split's log2-sum-exp and value in flight at once, then the merge
+    // in split order
+    float ls[32], vs[32];
+#pragma unroll
+    for (int s = 0; s < 32; ++s) {
+      ls[s] = s < nsplit ? pb[s * sstride + D] : -INFINITY;
+      vs[s] = s < nsplit ? pb[s * sstride + tid] : 0.f;
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < 32; ++s) M = fmaxf(M, ls[s]);
+    float acc = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int s = 0; s < 32; ++s) {
+        if (s < nsplit) {
+          const float f = ex2(ls[s] - M);
+          den += f;
+          acc = fmaf(f, vs[s], acc);
+        }
+      }
+    }
+    const float val = den > 0.f ? acc / den : 0.f;
+    if (a.out_f32)
+      static_cast<float*>(a.out)[qh * D + tid] = val;
+    else
+      static_cast<__nv_bfloat16*>(a.out)[qh * D + tid] = __float2bfloat16_rn(val);
+    if (a.lse && tid == 0) a.lse[qh] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
+    return;
+  }
   float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, pb[s * sstride + D]);
+  for (int s = tid; s < nsplit; s += D) M = fmaxf(M, pb[s * sstride + D]);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = red[0];
+#pragma unroll
+  for (int w = 1; w < D / 32; ++w) M = fmaxf(M, red[w]);
   float acc = 0.f, den = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < nsplit; ++s) {
-      const float f = ex2(pb[s * sstride + D] - M);
-      den += f;
-      acc = fmaf(f, pb[s * sstride + threadIdx.x], acc);
+  if (M != -INFINITY) {  // uniform over the block
+    for (int c0 = 0; c0 < nsplit; c0 += D) {
+      const int s = c0 + tid;
+      wf[tid] = s < nsplit ? ex2(pb[s * sstride + D] - M) : 0.f;
+      __syncthreads();
+      const int n = nsplit - c0 < D ? nsplit - c0 : D;
+      const float* col = pb + c0 * sstride + tid;
+#pragma unroll 8
+      for (int i = 0; i < n; ++i) {
+        const float f = wf[i];
+        den += f;
+        acc = fmaf(f, col[i * sstride], acc);
+      }
+      __syncthreads();  // wf is rewritten by the next chunk
     }
   }
   const float val = den > 0.f ? acc / den : 0.f;
   if (a.out_f32)
-    static_cast<float*>(a.out)[qh * D + threadIdx.x] = val;
+    static_cast<float*>(a.out)[qh * D + tid] = val;
   else
-    static_cast<__nv_bfloat16*>(a.out)[qh * D + threadIdx.x] = __float2bfloat16_rn(val);
-  if (a.lse && threadIdx.x == 0) a.lse[qh] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
+    static_cast<__nv_bfloat16*>(a.out)[qh * D + tid] = __float2bfloat16_rn(val);
+  if (a.lse && tid == 0) a.lse[qh] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
 }
 
 template <int D, int HG, int NW>
@@ -747,6 +800,18 @@ AttendPlan plan_attend(int Tq, long long nq, int n_keys_max, int H, int d) {
   p.mode = p.nsplit == 1 ? 0 : (p.nsplit <= kMaxCluster ? 2 : 1);
   p.part_bytes = p.mode == 1 ? static_cast<size_t>(nq) * p.nsplit * H * (d + 1) * sizeof(float) : 0;
   return p;
+}
+
+cudaError_t launch_attend_combine(const AttendArgs& a, int nsplit, cudaStream_t s) {
+  const long long nq = static_cast<long long>(a.B) * a.Tq;
+  if (nq * a.H == 0) return cudaSuccess;
+  if (a.d == 128)
+    return launch_k(attend_combine_kernel<128>, dim3(static_cast<unsigned>(nq * a.H)), dim3(128), 0, s, 1, a,
+                    nsplit);
+  if (a.d == 64)
+    return launch_k(attend_combine_kernel<64>, dim3(static_cast<unsigned>(nq * a.H)), dim3(64), 0, s, 1, a,
+                    nsplit);
+  return cudaErrorNotSupported;
 }
 
 cudaError_t launch_attend(const AttendArgs& a, const AttendPlan& p, cudaStream_t s) {

@@ -131,6 +131,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
   }
 }
 
+// The same, but a waiting thread is suspended in hardware for up to
+// ``sleep_ns`` per attempt (mbarrier.try_wait's suspend-time hint) instead of
+// polling: warps that wait long leave the issue slots and the shared-memory
+// pipe to the warps that work.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, long long budget,
+                                                volatile int* abort, uint32_t sleep_ns = 1000u) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(sleep_ns)
+        : "memory");
+    if (ok) return true;
+    if (abort != nullptr && *abort) return false;
+    if (clock64() - t0 > budget) return false;
+  }
+}
+
 // ----------------------------------------------------------------------------
 // TMA: tiled bulk tensor loads into shared memory, completion on an mbarrier
 // ----------------------------------------------------------------------------

@@ -136,6 +136,18 @@ size_t attend_part_bytes(int B, int Tq, int n_keys_max, int H, int d) {
   return align_up(p.part_bytes, kAlignWs);
 }
 
+// HCA: the tcgen05 decode kernel's range partials or the general kernel's
+// split partials, whichever is larger (the raw-buffer length that also
+// decides between them is not an argument of the size query)
+size_t hca_part_bytes(int B, int Tq, int N, int H, int d, int W) {
+  const size_t gen = attend_part_bytes(B, Tq, N + W, H, d);
+  const long long nq = static_cast<long long>(B) * Tq;
+  const size_t dec = csa::hca_decode_supported(Tq, nq, N, 1, H, d, W)
+                         ? align_up(csa::hca_decode_part_bytes(nq, N, W, H, d), kAlignWs)
+                         : 0;
+  return gen > dec ? gen : dec;
+}
+
 }  // namespace
 
 extern "C" {
@@ -339,7 +351,7 @@ csa_status csa_attend(const void* q, const void* k_cmp, const void* v_cmp, const
 
 csa_status hca_attend_workspace(int B, int Tq, int N, int H, int d, int W, size_t* bytes) {
   if (!bytes || B <= 0 || Tq <= 0 || N < 0 || H <= 0 || d <= 0 || W < 0) return CSA_ERR_INVALID;
-  *bytes = CSA_WS_HEADER_BYTES + attend_part_bytes(B, Tq, N + W, H, d);
+  *bytes = CSA_WS_HEADER_BYTES + hca_part_bytes(B, Tq, N, H, d, W);
   return CSA_OK;
 }
 
@@ -351,8 +363,36 @@ csa_status hca_attend(const void* q, const void* k_cmp, const void* v_cmp, const
                                     H, d, W, out, out_dtype, lse);
   if (st != CSA_OK) return st;
   if (m <= 0) return CSA_ERR_INVALID;
-  return attend_common(q, k_cmp, v_cmp, nullptr, k_raw, v_raw, raw_base, q_pos, B, Tq, N, T_raw, H,
-                       d, 0, m, W, scale, out, out_dtype, lse, ws, ws_bytes, stream);
+  const long long nq = static_cast<long long>(B) * Tq;
+  if (!csa::hca_decode_supported(Tq, nq, N, T_raw, H, d, W))
+    return attend_common(q, k_cmp, v_cmp, nullptr, k_raw, v_raw, raw_base, q_pos, B, Tq, N, T_raw, H,
+                         d, 0, m, W, scale, out, out_dtype, lse, ws, ws_bytes, stream);
+  st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES + hca_part_bytes(B, Tq, N, H, d, W));
+  if (st != CSA_OK) return st;
+  csa::AttendArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.k_cmp = k_cmp;
+  a.v_cmp = v_cmp;
+  a.k_raw = k_raw;
+  a.v_raw = v_raw;
+  a.raw_base = raw_base;
+  a.q_pos = q_pos;
+  a.B = B;
+  a.Tq = Tq;
+  a.N = N;
+  a.T_raw = T_raw;
+  a.H = H;
+  a.d = d;
+  a.W = W;
+  a.m = m;
+  a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(d));
+  a.out = out;
+  a.out_f32 = out_dtype == CSA_F32;
+  a.lse = lse;
+  a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + CSA_WS_HEADER_BYTES);
+  a.errw = err_word(ws);
+  return cuda_status(csa::launch_hca_decode(a, g_wait_budget, static_cast<cudaStream_t>(stream)));
 }
 
 // ---------------------------------------------------------------- layer

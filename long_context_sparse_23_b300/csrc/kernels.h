@@ -1,10 +1,19 @@
 // Internal launch interface between the C ABI (csa_api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 namespace csa {
+
+// cuTensorMapEncodeTiled, resolved from the driver at run time (nullptr when
+// the driver does not provide it)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn();
 
 // ---- (1) compression -------------------------------------------------------
 struct CompressArgs {
@@ -104,6 +113,17 @@ struct AttendPlan {
 };
 AttendPlan plan_attend(int Tq, long long nq, int n_keys_max, int H, int d);
 cudaError_t launch_attend(const AttendArgs& a, const AttendPlan& plan, cudaStream_t s);
+// merge nsplit partials per (query, head) from a.part, in split order, into a.out / a.lse
+cudaError_t launch_attend_combine(const AttendArgs& a, int nsplit, cudaStream_t s);
+
+// ---- dense HCA attention for decode-shaped calls on tcgen05 ------------------
+// One CTA per (query, range of up to kHcaTiles 128-key tiles); the ranges of a
+// query merge through workspace partials when there are several.
+constexpr int kHcaTiles = 4;
+bool hca_decode_supported(int Tq, long long nq, int N, int T_raw, int H, int d, int W);
+int hca_decode_nsplit(int N, int W);
+size_t hca_decode_part_bytes(long long nq, int N, int W, int H, int d);
+cudaError_t launch_hca_decode(const AttendArgs& a, long long wait_budget, cudaStream_t s);
 
 // ---- fused decode tail: long-row top-k + attention, one cluster per query -------
 constexpr int kTailCluster = 16;    // CTAs per query

@@ -60,15 +60,26 @@ def test_workspace_sizes(L):
     assert need.value == 256                       # decode: splits merge inside a thread-block cluster
     assert L.csa_attend_workspace(1, 8192, 16, 128, 1024, 128, ctypes.byref(need)) == 0
     assert need.value == 256                       # prefill: no split partials
+    # HCA decode, H = 64, d = 128 (tensor-core kernel): ranges of 4 128-key tiles,
+    # partials (H x (d + 1) floats per range) in the workspace; 8192 + 128 keys
+    # -> 65 tiles -> 17 ranges
     assert L.hca_attend_workspace(8, 1, 8192, 64, 128, 128, ctypes.byref(need)) == 0
-    assert need.value == 256                       # 8320 keys: 13 splits of 5 128-key tiles, one cluster
-    # more than 131072 keys: 8192-key splits with partials in the workspace (18 here),
+    assert need.value == 256 + (8 * 17 * 64 * 129 * 4 + 255) // 256 * 256
+    # one range: no partials
+    assert L.hca_attend_workspace(8, 1, 300, 64, 128, 128, ctypes.byref(need)) == 0
+    assert need.value == 256
+    # other head counts keep the general kernel: one cluster per query up to
+    # 131072 keys, 8192-key splits with partials in the workspace beyond
+    assert L.hca_attend_workspace(8, 1, 8192, 32, 128, 128, ctypes.byref(need)) == 0
+    assert need.value == 256
     # batch-invariant: per-sequence bytes scale linearly with B
     a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
     L.hca_attend_workspace(1, 1, 140000, 64, 128, 128, ctypes.byref(a))
     L.hca_attend_workspace(8, 1, 140000, 64, 128, 128, ctypes.byref(b))
-    assert a.value == 256 + (18 * 64 * 129 * 4 + 255) // 256 * 256
-    assert b.value - 256 == (8 * 18 * 64 * 129 * 4 + 255) // 256 * 256
+    assert a.value == 256 + (274 * 64 * 129 * 4 + 255) // 256 * 256
+    assert b.value - 256 == (8 * 274 * 64 * 129 * 4 + 255) // 256 * 256
+    L.hca_attend_workspace(1, 1, 140000, 16, 128, 128, ctypes.byref(a))
+    assert a.value == 256 + (18 * 16 * 129 * 4 + 255) // 256 * 256
     assert L.csa_attend_workspace(0, 1, 64, 128, 16, 8, ctypes.byref(need)) == _lib.CSA_ERR_INVALID
 
 
