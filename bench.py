@@ -38,7 +38,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch of the indexer on the 1M decode
 # workload, from an ncu capture of this launch configuration
 # (profiles/decode_1m_step.md); valid only for the source it was measured on.
-TRAFFIC = {"indexer": {"src_sha": "56c3e826b66aea96", "bytes": 272958464}}
+TRAFFIC = {"indexer": {"src_sha": "7c855c7243f5815e", "bytes": 272947712}}
 
 
 def _src_sha(*names):
@@ -427,6 +427,34 @@ def hca_decode_1m(dev, stream, steps):
             "attend_l2": "6 rotating copies of the entries (201 MB > L2)"}
 
 
+def hca_attend_given(dev, stream, steps, warmup=3):
+    """Only the HCA attention at 1M context (B = 8, 8192 entries given as
+    synthetic caches, H = 64, d = 128, W = 128), six rotating copies of the
+    caches (201 MB > L2): the small case used for kernel profiles."""
+    import long_context_sparse_23_b300 as csa
+    wl = S.WORKLOADS["hca_decode_1m"]
+    B, N, m = wl.B, wl.T // wl.m, wl.m
+    q = S.normal_bf16(7, S.TID["q"], (B, 1, wl.H, wl.d), dev)
+    kr = S.normal_bf16(7, S.TID["k_raw"], (B, 2 * wl.W, wl.d), dev)
+    vr = S.normal_bf16(7, S.TID["v_raw"], (B, 2 * wl.W, wl.d), dev)
+    t = wl.q_positions[0]
+    q_pos = torch.full((B, 1), t, dtype=torch.int32, device=dev)
+    raw_base = torch.full((B,), t + 1 - 2 * wl.W, dtype=torch.int32, device=dev)
+    sets = [(S.normal_bf16(8 + r, S.TID["k_cmp"], (B, N, wl.d), dev), S.normal_bf16(8 + r, S.TID["v_cmp"], (B, N, wl.d), dev))
+            for r in range(6)]
+    ws = csa.Workspace(1 << 16, dev)
+    turn = [0]
+
+    def att(st):
+        kc, vc = sets[turn[0] % len(sets)]
+        turn[0] += 1
+        csa.hca_attend(q, kc, vc, kr, vr, raw_base, q_pos, m, wl.W, ws=ws)
+
+    ms = time_calls(att, stream, steps, warmup)
+    assert ws.check_error() == 0
+    return {"workload": "hca_attend_1m", "ms_per_call": ms, "queries_per_s": B / (ms * 1e-3), "steps": steps}
+
+
 def workload_config(name: str) -> dict:
     wl = S.WORKLOADS[name]
     n_vis = sum(min(wl.N, (t + 1) // wl.m) for t in wl.q_positions) * wl.B
@@ -445,8 +473,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--workload", default=HEADLINE, choices=["decode_1m", "decode_128k", "decode_1m_tail"],
-                    help="decode workload to time (the headline is decode_1m)")
+    ap.add_argument("--workload", default=HEADLINE,
+                    choices=["decode_1m", "decode_128k", "decode_1m_tail", "hca_attend_1m"],
+                    help="decode workload to time (the headline is decode_1m; hca_attend_1m times only the "
+                         "HCA attention over given caches, with --quick)")
     ap.add_argument("--quick", action="store_true",
                     help="time the device step only: no stage breakdown, e2e, 128K line or CPU baseline "
                          "(the form used for kernel profiles)")
@@ -455,6 +485,15 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.workload == "hca_attend_1m":
+        if not args.quick or args.impl != "ours" or world != 1:
+            raise SystemExit("hca_attend_1m is a profiling case: --quick, one GPU, --impl ours")
+        torch.cuda.set_device(local)
+        dev = torch.device("cuda", local)
+        import __graft_entry__
+        __graft_entry__.build()
+        print(json.dumps(hca_attend_given(dev, torch.cuda.Stream(device=dev), args.steps, args.warmup)))
+        return
     wl = S.WORKLOADS[args.workload]
     metric = (f"CSA decode queries/s @{'1M' if wl.T == 1 << 20 else '128K'} ctx (B={wl.B}, {wl.N} compressed "
               f"entries, top-{wl.k}, W={wl.W})")
