@@ -474,9 +474,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--workload", default=HEADLINE,
-                    choices=["decode_1m", "decode_128k", "decode_1m_tail", "hca_attend_1m"],
-                    help="decode workload to time (the headline is decode_1m; hca_attend_1m times only the "
-                         "HCA attention over given caches, with --quick)")
+                    choices=["decode_1m", "decode_128k", "decode_1m_tail", "hca_attend_1m", "prefill_8k"],
+                    help="decode workload to time (the headline is decode_1m); with --quick also "
+                         "hca_attend_1m (only the HCA attention over given caches) and prefill_8k (the whole "
+                         "layer over an 8192-token prefill)")
     ap.add_argument("--quick", action="store_true",
                     help="time the device step only: no stage breakdown, e2e, 128K line or CPU baseline "
                          "(the form used for kernel profiles)")
@@ -485,14 +486,18 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.workload == "hca_attend_1m":
+    if args.workload in ("hca_attend_1m", "prefill_8k"):
         if not args.quick or args.impl != "ours" or world != 1:
-            raise SystemExit("hca_attend_1m is a profiling case: --quick, one GPU, --impl ours")
+            raise SystemExit(f"{args.workload} is a profiling case: --quick, one GPU, --impl ours")
         torch.cuda.set_device(local)
         dev = torch.device("cuda", local)
         import __graft_entry__
         __graft_entry__.build()
-        print(json.dumps(hca_attend_given(dev, torch.cuda.Stream(device=dev), args.steps, args.warmup)))
+        st = torch.cuda.Stream(device=dev)
+        if args.workload == "hca_attend_1m":
+            print(json.dumps(hca_attend_given(dev, st, args.steps, args.warmup)))
+        else:
+            print(json.dumps(prefill_8k(dev, st, args.steps)))
         return
     wl = S.WORKLOADS[args.workload]
     metric = (f"CSA decode queries/s @{'1M' if wl.T == 1 << 20 else '128K'} ctx (B={wl.B}, {wl.N} compressed "

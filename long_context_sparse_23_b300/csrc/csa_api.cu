@@ -136,16 +136,27 @@ size_t attend_part_bytes(int B, int Tq, int n_keys_max, int H, int d) {
   return align_up(p.part_bytes, kAlignWs);
 }
 
-// HCA: the tcgen05 decode kernel's range partials or the general kernel's
-// split partials, whichever is larger (the raw-buffer length that also
-// decides between them is not an argument of the size query)
-size_t hca_part_bytes(int B, int Tq, int N, int H, int d, int W) {
-  const size_t gen = attend_part_bytes(B, Tq, N + W, H, d);
+// Attention partials: the tcgen05 decode kernel's range partials or the
+// general kernels' split partials, whichever is larger (the raw-buffer length
+// that can also decide between them is not an argument of the size queries)
+size_t attn_part_bytes(bool csa_mode, int B, int Tq, int N, int k, int W, int H, int d) {
+  const size_t gen = attend_part_bytes(B, Tq, (csa_mode ? k : N) + W, H, d);
   const long long nq = static_cast<long long>(B) * Tq;
-  const size_t dec = csa::hca_decode_supported(Tq, nq, N, 1, H, d, W)
-                         ? align_up(csa::hca_decode_part_bytes(nq, N, W, H, d), kAlignWs)
-                         : 0;
-  return gen > dec ? gen : dec;
+  if (!csa::attend_tc_supported(csa_mode, Tq, nq, N, 1, k, H, d, W)) return gen;
+  const csa::TcPlan p = csa::attend_tc_plan(csa::attend_tc_tiles(csa_mode, N, k, W));
+  const size_t tc = align_up(csa::attend_tc_part_bytes(nq, H, d, p), kAlignWs);
+  return gen > tc ? gen : tc;
+}
+
+// The attention kernel for a's shape: tcgen05 for decode-shaped calls with
+// H = 64 and d = 128, the mma.sync kernels otherwise.
+cudaError_t launch_attention(const csa::AttendArgs& a, cudaStream_t s) {
+  const bool csa_mode = a.idx != nullptr;
+  const long long nq = static_cast<long long>(a.B) * a.Tq;
+  if (csa::attend_tc_supported(csa_mode, a.Tq, nq, a.N, a.T_raw, a.k, a.H, a.d, a.W))
+    return csa::launch_attend_tc(a, g_wait_budget, s);
+  const csa::AttendPlan plan = csa::plan_attend(a.Tq, nq, (csa_mode ? a.k : a.N) + a.W, a.H, a.d);
+  return csa::launch_attend(a, plan, s);
 }
 
 }  // namespace
@@ -291,7 +302,7 @@ csa_status csa_index_topk(const void* q_idx, const void* k_idx, const float* w,
 // ---------------------------------------------------------------- (4)
 csa_status csa_attend_workspace(int B, int Tq, int H, int d, int k, int W, size_t* bytes) {
   if (!bytes || B <= 0 || Tq <= 0 || H <= 0 || d <= 0 || k < 0 || W < 0) return CSA_ERR_INVALID;
-  *bytes = CSA_WS_HEADER_BYTES + attend_part_bytes(B, Tq, k + W, H, d);
+  *bytes = CSA_WS_HEADER_BYTES + attn_part_bytes(true, B, Tq, 1, k, W, H, d);
   return CSA_OK;
 }
 
@@ -300,12 +311,11 @@ static csa_status attend_common(const void* q, const void* k_cmp, const void* v_
                                 const int32_t* raw_base, const int32_t* q_pos, int B, int Tq, int N,
                                 int T_raw, int H, int d, int k, int m, int W, float scale, void* out,
                                 int out_dtype, float* lse, void* ws, size_t ws_bytes, void* stream) {
-  const int n_keys_max = (idx ? k : N) + W;
-  const size_t need = CSA_WS_HEADER_BYTES + attend_part_bytes(B, Tq, n_keys_max, H, d);
+  const size_t need = CSA_WS_HEADER_BYTES + attn_part_bytes(idx != nullptr, B, Tq, N, k, W, H, d);
   csa_status st = check_ws(ws, ws_bytes, need);
   if (st != CSA_OK) return st;
-  const csa::AttendPlan plan = csa::plan_attend(Tq, static_cast<long long>(B) * Tq, n_keys_max, H, d);
   csa::AttendArgs a;
+  std::memset(&a, 0, sizeof(a));
   a.q = q;
   a.k_cmp = k_cmp;
   a.v_cmp = v_cmp;
@@ -329,7 +339,7 @@ static csa_status attend_common(const void* q, const void* k_cmp, const void* v_
   a.lse = lse;
   a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + CSA_WS_HEADER_BYTES);
   a.errw = err_word(ws);
-  return cuda_status(csa::launch_attend(a, plan, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_attention(a, static_cast<cudaStream_t>(stream)));
 }
 
 csa_status csa_attend(const void* q, const void* k_cmp, const void* v_cmp, const int32_t* idx,
@@ -351,7 +361,7 @@ csa_status csa_attend(const void* q, const void* k_cmp, const void* v_cmp, const
 
 csa_status hca_attend_workspace(int B, int Tq, int N, int H, int d, int W, size_t* bytes) {
   if (!bytes || B <= 0 || Tq <= 0 || N < 0 || H <= 0 || d <= 0 || W < 0) return CSA_ERR_INVALID;
-  *bytes = CSA_WS_HEADER_BYTES + hca_part_bytes(B, Tq, N, H, d, W);
+  *bytes = CSA_WS_HEADER_BYTES + attn_part_bytes(false, B, Tq, N, 0, W, H, d);
   return CSA_OK;
 }
 
@@ -363,36 +373,8 @@ csa_status hca_attend(const void* q, const void* k_cmp, const void* v_cmp, const
                                     H, d, W, out, out_dtype, lse);
   if (st != CSA_OK) return st;
   if (m <= 0) return CSA_ERR_INVALID;
-  const long long nq = static_cast<long long>(B) * Tq;
-  if (!csa::hca_decode_supported(Tq, nq, N, T_raw, H, d, W))
-    return attend_common(q, k_cmp, v_cmp, nullptr, k_raw, v_raw, raw_base, q_pos, B, Tq, N, T_raw, H,
-                         d, 0, m, W, scale, out, out_dtype, lse, ws, ws_bytes, stream);
-  st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES + hca_part_bytes(B, Tq, N, H, d, W));
-  if (st != CSA_OK) return st;
-  csa::AttendArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.q = q;
-  a.k_cmp = k_cmp;
-  a.v_cmp = v_cmp;
-  a.k_raw = k_raw;
-  a.v_raw = v_raw;
-  a.raw_base = raw_base;
-  a.q_pos = q_pos;
-  a.B = B;
-  a.Tq = Tq;
-  a.N = N;
-  a.T_raw = T_raw;
-  a.H = H;
-  a.d = d;
-  a.W = W;
-  a.m = m;
-  a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(d));
-  a.out = out;
-  a.out_f32 = out_dtype == CSA_F32;
-  a.lse = lse;
-  a.part = reinterpret_cast<float*>(static_cast<char*>(ws) + CSA_WS_HEADER_BYTES);
-  a.errw = err_word(ws);
-  return cuda_status(csa::launch_hca_decode(a, g_wait_budget, static_cast<cudaStream_t>(stream)));
+  return attend_common(q, k_cmp, v_cmp, nullptr, k_raw, v_raw, raw_base, q_pos, B, Tq, N, T_raw, H,
+                       d, 0, m, W, scale, out, out_dtype, lse, ws, ws_bytes, stream);
 }
 
 // ---------------------------------------------------------------- layer
@@ -400,7 +382,7 @@ csa_status csa_layer_workspace(const csa_layer_args* a, size_t* bytes) {
   if (!a || !bytes || a->B <= 0 || a->Tq <= 0 || a->N <= 0 || a->k <= 0) return CSA_ERR_INVALID;
   size_t total = CSA_WS_HEADER_BYTES + scores_bytes(a->B, a->Tq, a->N) + topk_bytes(a->B, a->Tq, a->N);
   if (!a->idx_out) total += align_up(static_cast<size_t>(a->B) * a->Tq * a->k * 4, kAlignWs);
-  total += attend_part_bytes(a->B, a->Tq, a->k + a->W, a->H, a->d);
+  total += attn_part_bytes(true, a->B, a->Tq, a->N, a->k, a->W, a->H, a->d);
   *bytes = total;
   return CSA_OK;
 }
@@ -530,10 +512,8 @@ csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* s
   }
   st = index_then_topk(ia, ta, tk, s);
   if (st != CSA_OK) return st;
-  const int n_keys_max = a->k + a->W;
-  const csa::AttendPlan plan =
-      csa::plan_attend(a->Tq, static_cast<long long>(a->B) * a->Tq, n_keys_max, a->H, a->d);
   csa::AttendArgs at;
+  std::memset(&at, 0, sizeof(at));
   at.q = a->q;
   at.k_cmp = a->k_cmp;
   at.v_cmp = a->v_cmp;
@@ -557,7 +537,7 @@ csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* s
   at.lse = a->lse;
   at.part = reinterpret_cast<float*>(base);
   at.errw = err_word(ws);
-  return cuda_status(csa::launch_attend(at, plan, s));
+  return cuda_status(launch_attention(at, s));
 }
 
 }  // extern "C"

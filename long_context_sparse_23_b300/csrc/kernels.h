@@ -116,14 +116,21 @@ cudaError_t launch_attend(const AttendArgs& a, const AttendPlan& plan, cudaStrea
 // merge nsplit partials per (query, head) from a.part, in split order, into a.out / a.lse
 cudaError_t launch_attend_combine(const AttendArgs& a, int nsplit, cudaStream_t s);
 
-// ---- dense HCA attention for decode-shaped calls on tcgen05 ------------------
-// One CTA per (query, range of up to kHcaTiles 128-key tiles); the ranges of a
-// query merge through workspace partials when there are several.
-constexpr int kHcaTiles = 4;
-bool hca_decode_supported(int Tq, long long nq, int N, int T_raw, int H, int d, int W);
-int hca_decode_nsplit(int N, int W);
-size_t hca_decode_part_bytes(long long nq, int N, int W, int H, int d);
-cudaError_t launch_hca_decode(const AttendArgs& a, long long wait_budget, cudaStream_t s);
+// ---- decode attention on tcgen05 (H = 64, d = 128, Tq < 16) -----------------
+// CSA (a.idx != nullptr): the k listed rows and the W window rows, gathered
+// with cp.async; HCA (a.idx == nullptr): every visible entry and the window as
+// TMA tiles.  One CTA per (query, range of up to kTcTiles 128-key tiles); the
+// ranges of a query merge through workspace partials when there are several.
+constexpr int kTcTiles = 4;
+struct TcPlan {
+  int nsplit;  // ranges per query
+  int tpr;     // tiles per range
+};
+int attend_tc_tiles(bool csa, int N, int k, int W);  // tiles of the longest key list
+TcPlan attend_tc_plan(int n_tiles);
+bool attend_tc_supported(bool csa, int Tq, long long nq, int N, int T_raw, int k, int H, int d, int W);
+size_t attend_tc_part_bytes(long long nq, int H, int d, const TcPlan& p);
+cudaError_t launch_attend_tc(const AttendArgs& a, long long wait_budget, cudaStream_t s);
 
 // ---- fused decode tail: long-row top-k + attention, one cluster per query -------
 constexpr int kTailCluster = 16;    // CTAs per query

@@ -56,8 +56,16 @@ def test_workspace_sizes(L):
     assert need.value == 256                       # short rows: selected in shared memory
     assert L.csa_index_topk_workspace(1, 1, 5, 64, 128, 4, ctypes.byref(need)) == 0
     assert need.value == 256 + 256                # 8 floats rounded up to 256 bytes
+    # decode, H = 64, d = 128 (tensor-core kernel): 1024 + 128 slots = 9 tiles -> 3
+    # ranges of 3 tiles, H x (d + 1) floats of partials per range
     assert L.csa_attend_workspace(64, 1, 64, 128, 1024, 128, ctypes.byref(need)) == 0
-    assert need.value == 256                       # decode: splits merge inside a thread-block cluster
+    assert need.value == 256 + (64 * 3 * 64 * 129 * 4 + 255) // 256 * 256
+    # one range (up to 4 tiles): no partials
+    assert L.csa_attend_workspace(64, 1, 64, 128, 384, 128, ctypes.byref(need)) == 0
+    assert need.value == 256
+    # other head counts: the general decode kernel merges its splits inside a cluster
+    assert L.csa_attend_workspace(64, 1, 32, 128, 1024, 128, ctypes.byref(need)) == 0
+    assert need.value == 256
     assert L.csa_attend_workspace(1, 8192, 16, 128, 1024, 128, ctypes.byref(need)) == 0
     assert need.value == 256                       # prefill: no split partials
     # HCA decode, H = 64, d = 128 (tensor-core kernel): ranges of 4 128-key tiles,
