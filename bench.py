@@ -262,7 +262,20 @@ def e2e_decode(ds: DecodeStep, steps: int, warmup: int):
     dt = (time.perf_counter() - t0) / steps
     h2d = hq.numel() * 2 + hqi.numel() * 2
     d2h = hout.numel() * 2
-    return ds.B * ds.Tq / dt, h2d, d2h
+    return dt * 1e3, h2d, d2h
+
+
+def combine_over_ranks(ms: float, units_per_rank: int, world: int, device) -> tuple:
+    """The step time of the slowest rank and the whole-job rate: every rank
+    processes its own ``units_per_rank`` units per step (independent
+    sequences, no data-path collective), so the job's rate is the units of all
+    ranks over the slowest rank's time.  Returns (ms, units per second)."""
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+        ms = float(t.item())
+    return ms, units_per_rank * world / (ms * 1e-3)
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -560,15 +573,11 @@ def main():
     stages = {"csa_layer_plain_launches": layer_time(ds, max(20, min(args.steps, 400)), 5, stream),
               "step_with_indexer_events": ms_marked, "indexer_in_graph": ms_idx}
     torch.cuda.synchronize()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.barrier()
-        ms = float(t.item())
-    qps = ds.B * ds.Tq * world / (ms * 1e-3)
+    ms, qps = combine_over_ranks(ms, ds.B * ds.Tq, world, dev)
 
     launches = args.steps * ds.kernels_per_step()
-    e2e_qps, h2d, d2h = e2e_decode(ds, max(20, min(args.steps, 500)), 10)
+    e2e_ms, h2d, d2h = e2e_decode(ds, max(20, min(args.steps, 500)), 10)
+    _, e2e_qps = combine_over_ranks(e2e_ms, ds.B * ds.Tq, world, dev)
 
     peaks, src = _peaks()
     ibytes, n_vis = ds.indexer_bytes()
