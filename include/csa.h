@@ -54,7 +54,7 @@ extern "C" {
 typedef enum csa_status {
     CSA_OK = 0,
     CSA_ERR_INVALID = 1,      /* null pointer, bad size, misaligned tensor       */
-    CSA_ERR_UNSUPPORTED = 2,  /* valid, but a shape this build does not handle   */
+    CSA_ERR_UNSUPPORTED = 2,  /* valid, but a shape the library does not handle */
     CSA_ERR_WORKSPACE = 3,    /* workspace missing, misaligned or too small      */
     CSA_ERR_CUDA = 4,         /* a CUDA call or kernel launch failed             */
     CSA_ERR_TIMEOUT = 5,      /* device: a bounded wait ran out                  */
