@@ -91,6 +91,22 @@ def test_workspace_sizes(L):
     assert L.csa_attend_workspace(0, 1, 64, 128, 16, 8, ctypes.byref(need)) == _lib.CSA_ERR_INVALID
 
 
+def test_layer_workspace_holds_the_attention_partials(L):
+    """csa_layer's workspace = header + scores + top-k scratch + index lists +
+    attention partials; only the last part depends on H.  At the 128K decode
+    shape (B = 64, 32768 entries, top-1024, W = 128) H = 64, d = 128 runs the
+    tensor-core attention with 3 ranges per query; H = 32 merges its splits
+    inside a cluster and needs none."""
+    def size(H):
+        la = _lib.csa_layer_args()
+        for name, v in dict(B=64, Tq=1, N=32768, m=4, H=H, d=128, H_I=64, d_I=128, k=1024, W=128).items():
+            setattr(la, name, v)
+        need = ctypes.c_size_t(0)
+        assert L.csa_layer_workspace(ctypes.byref(la), ctypes.byref(need)) == 0
+        return need.value
+    assert size(64) - size(32) == (64 * 3 * 64 * 129 * 4 + 255) // 256 * 256
+
+
 def test_validation_before_any_launch(L):
     P3 = ctypes.c_void_p * 3
     D = (ctypes.c_int * 3)(64, 64, 32)
