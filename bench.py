@@ -228,40 +228,56 @@ def layer_time(ds: DecodeStep, steps: int, warmup: int, stream):
     return tot / steps
 
 
-def e2e_decode(ds: DecodeStep, steps: int, warmup: int):
-    """Queries/s through csa_layer with pinned host inputs (q, q_idx) copied in
-    and the output copied back every step; the caches stay resident."""
-    csa, wl = ds.csa, ds.wl
-    i = ds.inp
+def e2e_decode(ds: DecodeStep, steps: int, warmup: int, depth: int = 2):
+    """Queries/s through csa_layer, the user's call, with every step's inputs
+    (q, q_idx) copied in from pinned host memory and its output copied back
+    to pinned host memory.  ``depth`` steps are in flight, each on its own
+    stream with its own device buffers and workspace, as a serving loop runs
+    them: the host waits for step s's output before it reuses step s's
+    buffers for step s + depth.  Returns (ms per step, H2D bytes per step,
+    D2H bytes per step)."""
+    csa, wl, i = ds.csa, ds.wl, ds.inp
     hq = i["q"].cpu().pin_memory()
     hqi = i["q_idx"].cpu().pin_memory()
-    hout = torch.empty(ds.out.shape, dtype=ds.out.dtype).pin_memory()
-    dq, dqi = torch.empty_like(i["q"]), torch.empty_like(i["q_idx"])
-    a = csa.layer_args(B=ds.B, Tq=ds.Tq, N=wl.N, m=wl.m, H=wl.H, d=wl.d, H_I=wl.H_I, d_I=wl.d_I, k=wl.k,
-                       W=wl.W, T_raw=wl.raw_len, k_cmp=i["k_cmp"], v_cmp=i["v_cmp"], i_cmp=i["i_cmp"],
-                       k_win=i["k_raw"], v_win=i["v_raw"], raw_base=i["raw_base"], q=dq, q_idx=dqi,
-                       w=i["w"], q_pos=i["q_pos"], out=ds.out)
-    need = ctypes.c_size_t(0)
-    ds.L.csa_layer_workspace(ctypes.byref(a), ctypes.byref(need))
-    ws = csa.Workspace(need.value)
-    st = torch.cuda.current_stream()
+    slots = []
+    for _ in range(depth):
+        dq, dqi = torch.empty_like(i["q"]), torch.empty_like(i["q_idx"])
+        out = torch.empty_like(ds.out)
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        a = csa.layer_args(B=ds.B, Tq=ds.Tq, N=wl.N, m=wl.m, H=wl.H, d=wl.d, H_I=wl.H_I, d_I=wl.d_I, k=wl.k,
+                           W=wl.W, T_raw=wl.raw_len, k_cmp=i["k_cmp"], v_cmp=i["v_cmp"], i_cmp=i["i_cmp"],
+                           k_win=i["k_raw"], v_win=i["v_raw"], raw_base=i["raw_base"], q=dq, q_idx=dqi,
+                           w=i["w"], q_pos=i["q_pos"], out=out)
+        need = ctypes.c_size_t(0)
+        ds.L.csa_layer_workspace(ctypes.byref(a), ctypes.byref(need))
+        ws = csa.Workspace(need.value)
+        slots.append([dq, dqi, out, hout, a, ws, torch.cuda.Stream(), torch.cuda.Event()])
+    torch.cuda.synchronize()
 
-    def one():
-        dq.copy_(hq, non_blocking=True)
-        dqi.copy_(hqi, non_blocking=True)
-        r = ds.L.csa_layer(ctypes.byref(a), ws.ptr, ws.nbytes, st.cuda_stream)
-        assert r == 0, r
-        hout.copy_(ds.out, non_blocking=True)
-        st.synchronize()
+    def issue(n):
+        dq, dqi, out, hout, a, ws, st, ev = slots[n % depth]
+        with torch.cuda.stream(st):
+            dq.copy_(hq, non_blocking=True)
+            dqi.copy_(hqi, non_blocking=True)
+            r = ds.L.csa_layer(ctypes.byref(a), ws.ptr, ws.nbytes, st.cuda_stream)
+            assert r == 0, r
+            hout.copy_(out, non_blocking=True)
+            ev.record(st)
 
-    for _ in range(warmup):
-        one()
+    def run(n):
+        for s in range(n):
+            if s >= depth:
+                slots[s % depth][7].synchronize()   # step s - depth's output is on the host
+            issue(s)
+        for s in range(max(0, n - depth), n):
+            slots[s % depth][7].synchronize()
+
+    run(warmup)
     t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
+    run(steps)
     dt = (time.perf_counter() - t0) / steps
     h2d = hq.numel() * 2 + hqi.numel() * 2
-    d2h = hout.numel() * 2
+    d2h = slots[0][3].numel() * 2
     return dt * 1e3, h2d, d2h
 
 
