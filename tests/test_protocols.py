@@ -1,0 +1,77 @@
+"""The mbarrier protocols of the tensor-core kernels (indexer_kernel and
+attend_tc_kernel) on the CPU: every random interleaving of the warp roles
+finishes (no wait that nothing completes) and no buffer is refilled while it
+is still read.  The model (tests/_protocol_model.py) restates each role's
+waits and arrivals in the kernel's order; planted mistakes show that the
+checks bite."""
+import random
+
+import pytest
+
+from tests import _protocol_model as M
+
+
+def test_indexer_protocol_completes_without_hazards():
+    rng = random.Random(0)
+    for trial in range(200):
+        ntile = rng.choice([0, 1, 2, 3, 4, 5, 8, 13, 17])
+        stages = rng.choice([2, 3, 5, 8])
+        assert M.indexer(ntile, stages, trial), (ntile, stages)
+
+
+def test_attend_tc_protocol_completes_without_hazards():
+    for ntile in range(1, 5):   # a range with no tile writes its empty result and uses no barrier
+        for trial in range(100):
+            assert M.attend_tc(ntile, trial), ntile
+
+
+def test_planted_mistakes_are_caught(monkeypatch):
+    # a buffer-free wait on the wrong parity: the producer waits for a release
+    # that only follows its own first load
+    def bad_indexer(ntile, stages, seed):
+        full = [M.Bar(1) for _ in range(stages)]
+        empty = [M.Bar(1) for _ in range(stages)]
+        loads = [0] * stages
+
+        def producer():
+            for i in range(ntile):
+                s, ph = i % stages, (i // stages) & 1
+                yield (empty[s], ph)                  # mistake: parity not flipped
+                loads[s] += 1
+                full[s].arrive()
+
+        def mma():
+            for i in range(ntile):
+                s, ph = i % stages, (i // stages) & 1
+                yield (full[s], ph)
+                empty[s].arrive()
+        return M.run([producer(), mma()], seed)
+
+    assert not any(bad_indexer(6, 2, t) for t in range(20))   # the producer never starts: caught as a stall
+
+    # the output MMAs not waiting for the V rows: the model's hazard check fires
+    def bad_attend(ntile, seed):
+        kfull = [M.Bar(1) for _ in range(ntile)]
+        sdone = [M.Bar(1) for _ in range(ntile)]
+        buffer = ["empty"] * ntile
+
+        def producer():
+            for j in range(ntile):
+                buffer[j] = "K"
+                kfull[j].arrive()
+            for j in range(ntile):
+                yield (sdone[j], 0)
+                buffer[j] = "V"
+
+        def mma():
+            for j in range(ntile):
+                yield (kfull[j], 0)
+                sdone[j].arrive()
+            for j in range(ntile):
+                assert buffer[j] == "V", "output MMA read K rows"
+                yield None
+        return M.run([producer(), mma()], seed)
+
+    with pytest.raises(AssertionError):
+        for t in range(50):
+            bad_attend(3, t)
