@@ -364,8 +364,9 @@ __global__ void __launch_bounds__(32 * NW) attend_kernel(AttendArgs a, int nspli
   }
 }
 
-// Decode-shaped calls (few queries per sequence): CTA = (key range, group of
-// 16 heads, query).  The 8 warps own 16 keys each of every 128-key tile, so
+// Decode-shaped calls (few queries per sequence) with head shapes other than
+// the tensor-core kernel's (attend_tc.cu: H = 64, d = 128), and every call of
+// csa_attend_noalloc: CTA = (key range, group of 16 heads, query).  The 8 warps own 16 keys each of every 128-key tile, so
 // a CTA's tiles (at most a few) are gathered up front through a cp.async
 // ring of up to three stages.  The warps' partials merge in shared memory
 // (padded rows, no bank conflicts) into one (O, max, sum) per head, and the
