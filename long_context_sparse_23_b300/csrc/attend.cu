@@ -704,14 +704,9 @@ cudaError_t launch_impl(const AttendArgs& a, const AttendPlan& p, cudaStream_t s
   const long long nq = static_cast<long long>(a.B) * a.Tq;
   const dim3 grid(p.nsplit, static_cast<unsigned>(nq));
   if (p.mode == 2 && p.nsplit > 8) {
-    static bool nonportable_set[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!nonportable_set[dev]) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-      nonportable_set[dev] = true;
-    }
+    static std::atomic<bool> nonportable_set[64] = {};
+    e = ensure_nonportable_cluster(kern, nonportable_set);
+    if (e != cudaSuccess) return e;
   }
   e = launch_k(kern, grid, dim3(32 * NW), smem, s, p.mode == 2 ? p.nsplit : 1, a, p.nsplit, p.tiles_per_split,
                p.mode);
@@ -731,14 +726,9 @@ cudaError_t launch_decode(const AttendArgs& a, const AttendPlan& p, cudaStream_t
   cudaError_t e = ensure_dyn_smem<attend_decode_kernel<D>>(static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (p.nsplit > 8) {
-    static bool nonportable_set[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!nonportable_set[dev]) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-      nonportable_set[dev] = true;
-    }
+    static std::atomic<bool> nonportable_set[64] = {};
+    e = ensure_nonportable_cluster(kern, nonportable_set);
+    if (e != cudaSuccess) return e;
   }
   const long long nq = static_cast<long long>(a.B) * a.Tq;
   const dim3 grid(p.nsplit, (a.H + 15) / 16, static_cast<unsigned>(nq));

@@ -397,6 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_v = 1;
       }
       cp_async_wait<0>();
+      // the query rows' bulk copy has landed before the CTA may exit (the MMA
+      // thread's own wait for it may have given up)
+      if (ptid == 0) mbar_wait_sleep(&bars->q, 0, kDrainBudget, nullptr);
     }
   } else {
     // ---- epilogue: warp -> (TMEM lane quarter, half of the heads)

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace csa {
 
 // ----------------------------------------------------------------------------
@@ -333,15 +335,33 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 
 // Raise a kernel's dynamic shared-memory limit, once per device and size:
 // later calls (for example inside a CUDA-graph capture) touch no driver state.
+// The per-device record is atomic: calls from several host threads may both
+// set the attribute (idempotent), never race on the record.
 template <auto Kern>
 inline cudaError_t ensure_dyn_smem(int bytes) {
-  static int done[64] = {};
+  static std::atomic<int> done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && done[dev] >= bytes) return cudaSuccess;
+  if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
   e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = bytes;
+  if (e == cudaSuccess && dev >= 0 && dev < 64) {
+    int cur = done[dev].load(std::memory_order_relaxed);
+    while (cur < bytes && !done[dev].compare_exchange_weak(cur, bytes, std::memory_order_acq_rel)) {
+    }
+  }
+  return e;
+}
+
+// Allow clusters of more than 8 CTAs for ``kern``, once per device (atomic
+// per-device record, as above).
+template <typename K>
+inline cudaError_t ensure_nonportable_cluster(K kern, std::atomic<bool> (&set)[64]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (set[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) set[dev].store(true, std::memory_order_release);
   return e;
 }
 

@@ -46,6 +46,10 @@ constexpr int kC = kTailCluster;  // CTAs per query (one cluster)
 constexpr int kCandR = 512;     // candidates of one rank staged in shared memory
 constexpr int kRun = 64;        // consecutive scores per thread in the candidate scan
 constexpr int kBulk = 16384;    // bytes per bulk copy
+// A wait that ran out of the call's budget is reported and then continued
+// with this budget (about one second), so that no bulk copy is still writing
+// this CTA's shared memory when the buffer is refilled or the CTA exits.
+constexpr long long kDrainBudget = 1LL << 31;
 
 // Shared-memory layout (bytes), the same on host and device.
 struct TailLayout {
@@ -123,9 +127,14 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     mbar_fence_init();
   }
   __syncthreads();
-  // wait for the bulk copies on ``bar`` (bounded; a timeout is reported)
+  // wait for the bulk copies on ``bar``: bounded by the call's budget (a
+  // timeout is reported), then drained, so the copies have landed before the
+  // buffer is read, refilled or given up at exit
   auto bulk_wait = [&]() {
-    if (!mbar_wait(&bar, bar_phase, a.budget, nullptr)) raise_flag(at.errw, kFlagTimeout);
+    if (!mbar_wait(&bar, bar_phase, a.budget, nullptr)) {
+      raise_flag(at.errw, kFlagTimeout);
+      mbar_wait(&bar, bar_phase, kDrainBudget, nullptr);
+    }
     bar_phase ^= 1u;
   };
 
@@ -182,8 +191,8 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
       // the histogram does not describe the row (uniform): report and write
       // nothing, once this CTA's copy of the query has landed
       if (r == 0 && tid == 0) raise_flag(at.errw, kFlagIndex);
-      if (r < A) mbar_wait(&bar_q, 0, a.budget, nullptr);
-      if (lo < hi) mbar_wait(&bar, 0, a.budget, nullptr);
+      if (r < A) mbar_wait(&bar_q, 0, kDrainBudget, nullptr);
+      if (lo < hi) mbar_wait(&bar, 0, kDrainBudget, nullptr);
       return;
     }
   }
@@ -236,6 +245,10 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     }
   }
   if (tid == 0) n_own_s = n_own;
+  // no slot of this CTA holds a kept block until step 2 says so (with
+  // consistent inputs step 2 fills every slot below k; with a histogram that
+  // does not match the scores, unfilled slots stay empty instead of undefined)
+  for (int j = tid; j < S_r; j += kT) map[j] = -1;
   cluster.sync();  // #1: every rank's candidates and bucket counts are written
 
   // ---- 2. the rule, and this CTA's ranks of the selection (every CTA reads
@@ -392,7 +405,10 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     const int hg = warp & 3, kh = warp >> 2;
     const int g = lane >> 2, c = lane & 3;
     const int h0 = hg * 16 + g, h1 = h0 + 8;
-    if (!mbar_wait(&bar_q, 0, a.budget, nullptr)) raise_flag(at.errw, kFlagTimeout);
+    if (!mbar_wait(&bar_q, 0, a.budget, nullptr)) {
+      raise_flag(at.errw, kFlagTimeout);
+      mbar_wait(&bar_q, 0, kDrainBudget, nullptr);
+    }
     uint32_t qf[D / 16][4];
     {
       const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qs + static_cast<size_t>(h0) * D * 2);
@@ -543,7 +559,7 @@ cudaError_t launch_decode_tail(const TailArgs& a, cudaStream_t s) {
   const int E = tail_chunk(a.N);
   const int S_r = tail_slots(a.k, a.at.W);
   const TailLayout L = tail_layout(S_r, a.at.H, a.at.d, E);
-  static bool attr_set[4][64] = {};
+  static std::atomic<bool> attr_set[4][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   // one tile step of S_r / 2 keys per warp for the common slot count, else steps of 16
@@ -551,13 +567,13 @@ cudaError_t launch_decode_tail(const TailArgs& a, cudaStream_t s) {
   const int which = (a.at.d == 128 ? 0 : 2) + (kh48 ? 1 : 0);
   auto kern = a.at.d == 128 ? (kh48 ? decode_tail_kernel<128, 48> : decode_tail_kernel<128, 16>)
                             : (kh48 ? decode_tail_kernel<64, 48> : decode_tail_kernel<64, 16>);
-  if (!attr_set[which][dev]) {
+  if (!attr_set[which][dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     const TailLayout Lmax = tail_layout(kTailMaxSlots, 64, a.at.d, kT * kRun);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lmax.total);
     if (e != cudaSuccess) return e;
-    attr_set[which][dev] = true;
+    attr_set[which][dev].store(true, std::memory_order_release);
   }
   return launch_k(kern, dim3(kC, static_cast<unsigned>(nq)), dim3(kT), static_cast<size_t>(L.total), s, kC, a,
                   E, S_r);

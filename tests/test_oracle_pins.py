@@ -284,3 +284,65 @@ def test_window_only_is_banded_attention():
     assert list(O.window_rows(1, 4, 0, 100)) == [0, 1]
     with pytest.raises(IndexError):
         O.window_rows(10, 4, 8, 100)
+
+
+# ---------------------------------------------------------------- batched wrappers
+
+def _rand_bf16(rng, shape):
+    return O.round_bf16(rng.standard_normal(shape))
+
+
+def test_batched_wrappers_equal_each_sequence_alone():
+    """B = 3 sequences with different inputs, positions and window offsets:
+    every batched wrapper returns, for sequence b, exactly what it returns for
+    that sequence alone (B = 1, itself pinned by the reductions above), and
+    the three sequences' results differ, so a wrapper that paired one
+    sequence's tensor with another's (or read sequence 0 for all) fails."""
+    rng = np.random.default_rng(11)
+    B, T, m, H, d, HI, dI, k, W = 3, 64, 4, 2, 8, 3, 4, 5, 6
+    N = T // m
+    x, g = _rand_bf16(rng, (B, T, d)), _rand_bf16(rng, (B, T, d))
+    xi, gi = _rand_bf16(rng, (B, T, dI)), _rand_bf16(rng, (B, T, dI))
+    q, qi = _rand_bf16(rng, (B, 2, H, d)), _rand_bf16(rng, (B, 2, HI, dI))
+    w = rng.uniform(0, 1, HI)
+    q_pos = np.array([[63, 50], [61, 45], [59, 47]])
+    T_raw = 24
+    raw_base = np.array([T - T_raw, T - T_raw - 2, T - T_raw - 4])
+    kr, vr = _rand_bf16(rng, (B, T_raw, d)), _rand_bf16(rng, (B, T_raw, d))
+    # window rows must exist for every query: t - W + 1 >= raw_base, t < raw_base + T_raw
+    for b in range(B):
+        for t in q_pos[b]:
+            assert t - W + 1 >= raw_base[b] and t < raw_base[b] + T_raw
+    scale = 0.3
+
+    kc = O.csa_compress(x, g, m)
+    ic = O.csa_compress(xi, gi, m)
+    kcb, icb = O.round_bf16(kc), O.round_bf16(ic)
+    idx, S = O.csa_index_topk(qi, icb, w, q_pos, m, k)
+    Oc, Lc = O.csa_attend(q, kcb, kcb, idx, kr, vr, raw_base, q_pos, W, scale)
+    Oh, Lh = O.hca_attend(q, kcb, kcb, kr, vr, raw_base, q_pos, m, W, scale)
+    for b in range(B):
+        one = slice(b, b + 1)
+        np.testing.assert_array_equal(kc[b], O.csa_compress(x[one], g[one], m)[0])
+        idx1, S1 = O.csa_index_topk(qi[one], icb[one], w, q_pos[one], m, k)
+        np.testing.assert_array_equal(idx[b], idx1[0])
+        for j in range(2):
+            np.testing.assert_array_equal(S[b][j], S1[0][j])
+        o1, l1 = O.csa_attend(q[one], kcb[one], kcb[one], idx[one], kr[one], vr[one], raw_base[one],
+                              q_pos[one], W, scale)
+        np.testing.assert_array_equal(Oc[b], o1[0])
+        np.testing.assert_array_equal(Lc[b], l1[0])
+        o1, l1 = O.hca_attend(q[one], kcb[one], kcb[one], kr[one], vr[one], raw_base[one], q_pos[one], m, W,
+                              scale)
+        np.testing.assert_array_equal(Oh[b], o1[0])
+        np.testing.assert_array_equal(Lh[b], l1[0])
+    for res in (kc, idx, Oc, Oh):
+        assert not np.array_equal(res[0], res[1]) and not np.array_equal(res[1], res[2])
+    # the window really reaches into each sequence's own raw buffer: the HCA
+    # output of query (1, 1) changes when only sequence 1's window rows change
+    vr2 = vr.copy()
+    vr2[1] = _rand_bf16(rng, (T_raw, d))
+    Oh2, _ = O.hca_attend(q, kcb, kcb, kr, vr2, raw_base, q_pos, m, W, scale)
+    assert not np.array_equal(Oh2[1], Oh[1])
+    np.testing.assert_array_equal(Oh2[0], Oh[0])
+    np.testing.assert_array_equal(Oh2[2], Oh[2])
