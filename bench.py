@@ -151,12 +151,32 @@ class DecodeStep:
         n = 2 + (0 if fused_hist else 1)      # zeroing, indexer (+ histogram pass)
         return n + (1 if wl.N > 65536 else 2 + attention)  # fused tail, or select + finish + attention
 
-    # algorithmic work of the indexer launch (per visible entry: its d_I-wide bf16
-    # key read once + one fp32 score written; per query: its H_I x d_I bf16 queries)
-    def indexer_bytes(self):
+    # algorithmic work of the indexer launch: every visible entry's d_I-wide bf16
+    # key read once per sequence (the queries of a sequence share one pass over
+    # the keys), one fp32 score written per (query, visible entry), and each
+    # query's H_I x d_I bf16 indexer queries read once; 2 H_I d_I flops per
+    # (query, visible entry)
+    def indexer_work(self):
         wl = self.wl
-        n_vis = sum(min(wl.N, (int(t) + 1) // wl.m) for t in self.inp["q_pos"].flatten().tolist())
-        return n_vis * (wl.d_I * 2 + 4) + self.B * self.Tq * wl.H_I * wl.d_I * 2, n_vis
+        pos = self.inp["q_pos"].cpu().tolist()
+        nv = [[min(wl.N, (int(t) + 1) // wl.m) for t in row] for row in pos]
+        keys = sum(max(r) for r in nv) * wl.d_I * 2
+        scores = sum(sum(r) for r in nv) * 4
+        queries = self.B * self.Tq * wl.H_I * wl.d_I * 2
+        flops = sum(sum(r) for r in nv) * 2 * wl.H_I * wl.d_I
+        return keys + scores + queries, flops
+
+
+def _step_bytes(self):
+    """Algorithmic bytes of one decode step: the indexer's (keys, scores,
+    queries), then per query the k kept compressed K/V rows and the W window
+    rows (2 d bf16 each), its H x d query and its output."""
+    wl = self.wl
+    per_q = (wl.k + wl.W) * 2 * wl.d * 2 + 2 * wl.H * wl.d * 2
+    return self.indexer_work()[0] + self.B * self.Tq * per_q
+
+
+DecodeStep.step_bytes = _step_bytes
 
 
 def graph_of(fn, st_torch, n=1, marks=None, L=None):
@@ -235,14 +255,17 @@ def layer_time(ds: DecodeStep, steps: int, warmup: int, stream):
     return tot / steps
 
 
-def e2e_decode(ds: DecodeStep, steps: int, warmup: int, depth: int = 2):
-    """Queries/s through csa_layer, the user's call, with every step's inputs
-    (q, q_idx) copied in from pinned host memory and its output copied back
-    to pinned host memory.  ``depth`` steps are in flight, each on its own
-    stream with its own device buffers and workspace, as a serving loop runs
-    them: the host waits for step s's output before it reuses step s's
-    buffers for step s + depth.  Returns (ms per step, H2D bytes per step,
-    D2H bytes per step)."""
+def e2e_decode(ds: DecodeStep, min_steps: int = 500, min_s: float = 1.0, warmup: int = 20, depth: int = 2):
+    """Queries/s through csa_layer_host, the C-ABI call for callers whose step
+    inputs and result live in host memory: every step copies its queries
+    (q, q_idx) in from pinned host memory, runs the layer and copies its
+    output back to pinned host memory, on one stream, inside the timed
+    region.  ``depth`` steps are in flight, each on its own stream with its
+    own device staging buffers, workspace and host output buffer, as a
+    serving loop runs independent batches: the host waits for step s's output
+    before it reuses step s's buffers for step s + depth.  Runs at least
+    ``min_steps`` steps and at least ``min_s`` seconds.  Returns (ms per step,
+    H2D bytes per step, D2H bytes per step, steps timed)."""
     csa, wl, i = ds.csa, ds.wl, ds.inp
     hq = i["q"].cpu().pin_memory()
     hqi = i["q_idx"].cpu().pin_memory()
@@ -258,34 +281,55 @@ def e2e_decode(ds: DecodeStep, steps: int, warmup: int, depth: int = 2):
         need = ctypes.c_size_t(0)
         ds.L.csa_layer_workspace(ctypes.byref(a), ctypes.byref(need))
         ws = csa.Workspace(need.value)
-        slots.append([dq, dqi, out, hout, a, ws, torch.cuda.Stream(), torch.cuda.Event()])
+        st = torch.cuda.Stream()
+        slots.append((ctypes.byref(a), a, hout, ws.ptr, ws.nbytes, st.cuda_stream, st, torch.cuda.Event(), dq, dqi,
+                      out, ws))
     torch.cuda.synchronize()
-
-    def issue(n):
-        dq, dqi, out, hout, a, ws, st, ev = slots[n % depth]
-        with torch.cuda.stream(st):
-            dq.copy_(hq, non_blocking=True)
-            dqi.copy_(hqi, non_blocking=True)
-            r = ds.L.csa_layer(ctypes.byref(a), ws.ptr, ws.nbytes, st.cuda_stream)
-            assert r == 0, r
-            hout.copy_(out, non_blocking=True)
-            ev.record(st)
+    fn = ds.L.csa_layer_host
+    hq_p, hqi_p = hq.data_ptr(), hqi.data_ptr()
 
     def run(n):
         for s in range(n):
+            sl = slots[s % depth]
             if s >= depth:
-                slots[s % depth][7].synchronize()   # step s - depth's output is on the host
-            issue(s)
+                sl[7].synchronize()   # step s - depth's output is on the host
+            r = fn(sl[0], hq_p, hqi_p, sl[2].data_ptr(), sl[3], sl[4], sl[5])
+            if r:
+                raise RuntimeError(f"csa_layer_host: {r}")
+            sl[7].record(sl[6])
         for s in range(max(0, n - depth), n):
             slots[s % depth][7].synchronize()
 
     run(warmup)
-    t0 = time.perf_counter()
-    run(steps)
-    dt = (time.perf_counter() - t0) / steps
+    done, t = 0, 0.0
+    while done < min_steps or t < min_s:
+        t0 = time.perf_counter()
+        run(250)
+        t += time.perf_counter() - t0
+        done += 250
     h2d = hq.numel() * 2 + hqi.numel() * 2
-    d2h = slots[0][3].numel() * 2
-    return dt * 1e3, h2d, d2h
+    d2h = slots[0][2].numel() * slots[0][2].element_size()
+    for sl in slots:     # every slot's output equals the device-resident step's
+        assert torch.equal(sl[2], ds.out.cpu()), "csa_layer_host output differs from csa_layer's"
+    return t / done * 1e3, h2d, d2h, done
+
+
+def host_call_us(ds: DecodeStep, stream, calls: int = 2000):
+    """Host time of one csa_layer call (argument checks, tensor-map encoding
+    and kernel launches; ctypes marshalling included): calls are made in
+    bursts of 100, each timed with perf_counter without waiting for the GPU;
+    the GPU is drained between bursts, outside the timing."""
+    st = stream.cuda_stream
+    tot = 0.0
+    with torch.cuda.stream(stream):
+        for _ in range(calls // 100):
+            stream.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(100):
+                ds.step(st)
+            tot += time.perf_counter() - t0
+        stream.synchronize()
+    return tot / (calls // 100 * 100) * 1e6
 
 
 def combine_over_ranks(ms: float, units_per_rank: int, world: int, device) -> tuple:
@@ -350,15 +394,17 @@ def oracle_rate(name: str, budget_s: float, steps: int = 0, warmup: int = 0):
             done += 1
         return done / tot, threads, (f"{done} whole queries of {name} (sequence 0, t={t}, "
                                      f"{n_vis} visible entries), inputs generated outside the timing; "
-                                     f"host has {os.cpu_count()} logical CPUs")
+                                     f"host has {os.cpu_count()} logical CPUs"), 1e3 * tot / done
     probe = sample(min(n_vis, 16384))
     per_step = budget_s / (steps + warmup)
     n = int(min(n_vis, max(1024, min(n_vis, 16384) * per_step / max(probe, 1e-6))))
     for _ in range(warmup):
         sample(n)
     tot = sum(sample(n) for _ in range(steps))
-    return steps * (n / n_vis) / tot, threads, (f"per step: 1 query of {name} with its indexer over the most "
-                                                 f"recent {n} of {n_vis} visible entries, scaled by n/n_vis")
+    return steps * (n / n_vis) / tot, threads, (
+        f"each timed step is 1 query of {name} (sequence 0) with its indexer over the most recent {n} of "
+        f"{n_vis} visible entries, then top-k and attention; ms_per_step is that step's measured time, and "
+        f"the rate is scaled by n/n_vis to whole queries"), 1e3 * tot / steps
 
 
 # ---------------------------------------------------------------- other workloads
@@ -373,6 +419,35 @@ def time_calls(fn, stream, steps, warmup=3):
         gk = graph_of(fn, stream, n=steps)
     warm(g1, warmup, stream, min_warm_s=0.1)
     return time_steps(gk, steps, stream)
+
+
+def decode_also(name, dev, stream, steps):
+    """Another decode workload: device time per csa_layer step (CUDA graph of
+    ``steps`` calls), the indexer inside a second graph of the same steps
+    (CUDA events around each indexer launch), the indexer's HBM and bf16
+    tensor fractions and the step's fraction of its HBM floor."""
+    ds = DecodeStep(name, dev)
+    ev_b, ev_e = timing_events(steps, stream), timing_events(steps, stream)
+    with torch.cuda.stream(stream):
+        ds.step(stream.cuda_stream)
+        stream.synchronize()
+        g1 = graph_of(ds.step, stream)
+        gk = graph_of(ds.step, stream, n=steps)
+        gm = graph_of(ds.step, stream, n=steps, marks=(ev_b, ev_e), L=ds.L)
+    assert ds.ws.check_error() == 0
+    warm(g1, 10, stream)
+    ms = time_steps(gk, steps, stream)
+    time_steps(gm, steps, stream)
+    ms_idx = sum(b.elapsed_time(e) for b, e in zip(ev_b, ev_e)) / steps
+    peaks, _ = _peaks()
+    ibytes, iflops = ds.indexer_work()
+    sb = ds.step_bytes()
+    return {"queries_per_s": ds.B * ds.Tq / (ms * 1e-3), "ms_per_step": ms, "B": ds.B, "Tq": ds.Tq,
+            "indexer_ms": ms_idx, "indexer_bytes": ibytes, "indexer_flops": iflops,
+            "indexer_frac_of_hbm": ibytes / (ms_idx * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "indexer_frac_of_bf16_peak": iflops / (ms_idx * 1e-3) / 1e12 / peaks["bf16_tflops"],
+            "step_bytes": sb, "step_floor_ms": sb / peaks["hbm_gbs"] / 1e6,
+            "step_frac_of_hbm": sb / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
 
 
 def prefill_8k(dev, stream, steps):
@@ -411,9 +486,48 @@ def prefill_8k(dev, stream, steps):
     flops = sum(min(N, (t + 1) // wl.m) for t in range(T)) * wl.H_I * wl.d_I * 2
     peaks, _ = _peaks()
     tf = flops / (ms_idx * 1e-3) / 1e12
+
+    # each step alone through its own public call (same buffers): compression
+    # of the three streams, indexer + top-k, attention on the kept indices
+    P = ctypes.c_void_p * 3
+    xs = P(i["k_raw"].data_ptr(), i["v_raw"].data_ptr(), i["i_raw"].data_ptr())
+    gs = P(i["g_k"].data_ptr(), i["g_v"].data_ptr(), i["g_i"].data_ptr())
+    os_ = P(kc.data_ptr(), vc.data_ptr(), ic.data_ptr())
+    Ds = (ctypes.c_int * 3)(wl.d, wl.d, wl.d_I)
+    idx = torch.empty(B, T, wl.k, dtype=torch.int32, device=dev)
+    need = ctypes.c_size_t(0)
+    L.csa_index_topk_workspace(B, T, N, wl.H_I, wl.d_I, wl.k, ctypes.byref(need))
+    ws_i = csa.Workspace(need.value, dev)
+    L.csa_attend_workspace(B, T, wl.H, wl.d, wl.k, wl.W, ctypes.byref(need))
+    ws_a = csa.Workspace(need.value, dev)
+
+    def comp(st):
+        assert L.csa_compress(3, xs, gs, os_, Ds, B, T, wl.m, 0, st) == 0
+
+    def itk(st):
+        assert L.csa_index_topk(i["q_idx"].data_ptr(), ic.data_ptr(), i["w"].data_ptr(), 0, i["q_pos"].data_ptr(), B,
+                                T, N, wl.H_I, wl.d_I, wl.m, wl.k, idx.data_ptr(), None, ws_i.ptr, ws_i.nbytes,
+                                st) == 0
+
+    def att(st):
+        assert L.csa_attend(i["q"].data_ptr(), kc.data_ptr(), vc.data_ptr(), idx.data_ptr(), i["k_raw"].data_ptr(),
+                            i["v_raw"].data_ptr(), i["raw_base"].data_ptr(), i["q_pos"].data_ptr(), B, T, N, T,
+                            wl.H, wl.d, wl.k, wl.W, 0.0, out.data_ptr(), 0, None, ws_a.ptr, ws_a.nbytes, st) == 0
+
+    ms_c = time_calls(comp, stream, steps)
+    ms_it = time_calls(itk, stream, steps)
+    ms_a = time_calls(att, stream, steps)
+    keys = sum(min(wl.k, min(N, (t + 1) // wl.m)) + min(wl.W, t + 1) for t in range(T)) * B
+    att_flops = keys * 4 * wl.H * wl.d
+    comp_bytes = B * T * (2 * wl.d + wl.d_I) * 2 * 2 + B * N * (2 * wl.d + wl.d_I) * 2
     return {"tokens_per_s": B * T / (ms * 1e-3), "ms_per_layer": ms, "indexer_ms": ms_idx,
             "indexer_tflops": tf, "indexer_flops": flops,
-            "indexer_frac_of_bf16_peak": tf / peaks["bf16_tflops"], "bf16_peak_tflops": peaks["bf16_tflops"]}
+            "indexer_frac_of_bf16_peak": tf / peaks["bf16_tflops"], "bf16_peak_tflops": peaks["bf16_tflops"],
+            "stages_ms": {"compress": ms_c, "index_topk": ms_it, "topk_after_indexer": ms_it - ms_idx,
+                          "attention": ms_a},
+            "compress_frac_of_hbm": comp_bytes / (ms_c * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "attention_flops": att_flops, "attention_kernel": "attend_kernel (mma.sync)",
+            "attention_frac_of_bf16_peak": att_flops / (ms_a * 1e-3) / 1e12 / peaks["bf16_tflops"]}
 
 
 def hca_decode_1m(dev, stream, steps):
@@ -542,9 +656,10 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        rate, threads, what = oracle_rate(args.workload, budget_s=90.0, steps=args.steps, warmup=args.warmup)
+        rate, threads, what, ms_step = oracle_rate(args.workload, budget_s=60.0, steps=args.steps,
+                                                   warmup=args.warmup)
         line = {"impl": "reference", "metric": metric, "value": rate, "unit": "queries/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * wl.B * wl.Tq / rate,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": workload_config(args.workload),
                 "cpu_baseline": {"value": rate, "unit": "queries/s", "cores": threads, "kind": "oracle", "sample": what},
@@ -595,15 +710,16 @@ def main():
         return
     stages = {"csa_layer_plain_launches": layer_time(ds, max(20, min(args.steps, 400)), 5, stream),
               "step_with_indexer_events": ms_marked, "indexer_in_graph": ms_idx}
+    host_us = host_call_us(ds, stream)
     torch.cuda.synchronize()
     ms, qps = combine_over_ranks(ms, ds.B * ds.Tq, world, dev)
 
     launches = args.steps * ds.kernels_per_step()
-    e2e_ms, h2d, d2h = e2e_decode(ds, max(20, min(args.steps, 500)), 10)
+    e2e_ms, h2d, d2h, e2e_steps = e2e_decode(ds)
     _, e2e_qps = combine_over_ranks(e2e_ms, ds.B * ds.Tq, world, dev)
 
     peaks, src = _peaks()
-    ibytes, n_vis = ds.indexer_bytes()
+    ibytes, _ = ds.indexer_work()
     achieved = ibytes / (ms_idx * 1e-3) / 1e9
     sha = _src_sha("indexer.cu", "common.cuh")
     traffic = TRAFFIC["indexer"]["bytes"] if TRAFFIC["indexer"]["src_sha"] == sha else None
@@ -611,21 +727,16 @@ def main():
             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
             "traffic": traffic, "algorithmic_bytes": ibytes, "launch_us": round(ms_idx * 1e3, 2),
             "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.4 TB/s"}
+    step_bytes = ds.step_bytes()
+    step_roof = {"bytes": step_bytes, "floor_us": round(step_bytes / peaks["hbm_gbs"] / 1e3, 2),
+                 "frac": round(step_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
 
     extra = {}
     del ds, g1, gk, gm
     torch.cuda.empty_cache()
-    ds2 = DecodeStep("decode_128k", dev)
-    K2 = max(10, args.steps // 4)
-    with torch.cuda.stream(stream):
-        ds2.step(stream.cuda_stream)
-        stream.synchronize()
-        g1 = graph_of(ds2.step, stream)
-        gk = graph_of(ds2.step, stream, n=K2)
-    warm(g1, 10, stream)
-    ms2 = time_steps(gk, K2, stream)
-    extra["decode_128k"] = {"queries_per_s": ds2.B * ds2.Tq / (ms2 * 1e-3), "ms_per_step": ms2}
-    del ds2, g1, gk
+    extra["decode_128k"] = decode_also("decode_128k", dev, stream, max(10, args.steps // 4))
+    torch.cuda.empty_cache()
+    extra["decode_1m_tail"] = decode_also("decode_1m_tail", dev, stream, max(10, args.steps // 8))
     torch.cuda.empty_cache()
     extra["prefill_8k"] = prefill_8k(dev, stream, max(5, args.steps // 100))
     torch.cuda.empty_cache()
@@ -637,10 +748,14 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": workload_config(args.workload),
             "clocks": clocks, "gpu_launches": launches, "roofline": roof,
-            "e2e": {"value": e2e_qps, "unit": "queries/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "stages_ms": {k: round(v, 5) for k, v in stages.items()}, "also": extra}
+            "e2e": {"value": e2e_qps, "unit": "queries/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "call": "csa_layer_host (pinned host q, q_idx in; out back to pinned host memory)",
+                    "in_flight": 2, "steps_timed": e2e_steps, "ms_per_step": round(e2e_ms, 5)},
+            "step_roofline": step_roof,
+            "stages_ms": {k: round(v, 5) for k, v in stages.items()},
+            "host_us_per_csa_layer_call": round(host_us, 2), "also": extra}
     if rank == 0:
-        rate, threads, what = oracle_rate(HEADLINE, budget_s=args.cpu_budget)
+        rate, threads, what, _ = oracle_rate(HEADLINE, budget_s=args.cpu_budget)
         line["cpu_baseline"] = {"value": rate, "unit": "queries/s", "cores": threads, "kind": "oracle", "sample": what}
     if world > 1:
         torch.distributed.destroy_process_group()

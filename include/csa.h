@@ -101,13 +101,41 @@ csa_status csa_compress(int n_streams, const void* const* x, const void* const* 
                         int out_dtype, void* stream);
 
 /* --------------------------------------------------------------------------
+ * (1') Decode-time compression and cache append.  Octagono "Hybrid Attention:
+ * CSA and HCA" and the technical review, section 2.1: every m tokens become
+ * one compressed entry.  During decoding the raw tokens of the newest
+ * positions live in a window buffer; a query at position t = q_pos[n, j] with
+ * (t + 1) % m == 0 completes block b = (t + 1) / m - 1 (tokens t-m+1 .. t),
+ * and this call writes
+ *     out_i[n, b, c] = sum_{j<m} softmax_j(g_i[n, r0+j, c]) * x_i[n, r0+j, c],
+ *     r0 = t - m + 1 - raw_base[n],
+ * exactly as csa_compress folds that block (bit-identical to compressing the
+ * whole prefix).  Positions that complete no block leave the caches alone, so
+ * the partial block stays raw in the window buffer.
+ *   x_win[i], g_win[i] : [B, T_raw, D[i]] bf16 (row r holds token raw_base[n] + r)
+ *   out[i]             : [B, N, D[i]] bf16 caches (capacity N entries)
+ *   raw_base [B], q_pos [B, Tq] int32
+ * A block whose rows are outside the window buffer, or whose entry is >= N,
+ * is skipped and flagged with CSA_FLAG_INDEX.  D[i] multiple of 8, <= 512;
+ * 1 <= m <= 4096; T_raw >= m.  Workspace: CSA_WS_HEADER_BYTES.
+ * ------------------------------------------------------------------------ */
+csa_status csa_append(int n_streams, const void* const* x_win, const void* const* g_win,
+                      void* const* out, const int* D, const int32_t* raw_base,
+                      const int32_t* q_pos, int B, int Tq, int T_raw, int N, int m,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
  * (2) Lightning Indexer scores.  Octagono "Hybrid Attention: CSA and HCA" and
  * the technical review, section 2.1: every query gets indexer queries that
  * are scored against the compressed entries; 64 heads of width 128.
- *     S[n, j, b] = sum_h w[h] * ReLU(q_idx[n, j, h, :] . k_idx[n, b, :])
+ *     S[n, j, b] = sum_h w[n, j, h] * ReLU(q_idx[n, j, h, :] . k_idx[n, b, :])
  * for the visible blocks b < n_vis = min(N, floor((q_pos[n, j] + 1) / m)).
  *   q_idx  [B, Tq, H_I, d_I] bf16     k_idx [B, N, d_I] bf16
- *   w      [H_I] fp32                 q_pos [B, Tq] int32 (absolute positions)
+ *   q_pos  [B, Tq] int32 (absolute positions)
+ *   w      fp32 head weights: w_stride == 0 -> one [H_I] vector shared by
+ *          every query (w[n, j, h] = w[h]); w_stride >= H_I -> one vector per
+ *          query, w[n, j, h] = w[(n * Tq + j) * w_stride + h] (produced per
+ *          token, as the DSA-style indexer of the pages does; any sign)
  *   scores [B, Tq, ld_scores] fp32, ld_scores >= N and a multiple of 4;
  *          entries b >= n_vis are left untouched.
  * Computed on the tcgen05 tensor cores (bf16 products, fp32 accumulation).
@@ -115,7 +143,7 @@ csa_status csa_compress(int n_streams, const void* const* x, const void* const* 
  * CSA_WS_HEADER_BYTES.
  * ------------------------------------------------------------------------ */
 csa_status csa_index_scores(const void* q_idx, const void* k_idx, const float* w,
-                            const int32_t* q_pos, int B, int Tq, int N, int H_I, int d_I,
+                            int64_t w_stride, const int32_t* q_pos, int B, int Tq, int N, int H_I, int d_I,
                             int m, float* scores, int64_t ld_scores,
                             void* ws, size_t ws_bytes, void* stream);
 
@@ -142,7 +170,7 @@ csa_status csa_topk(const float* scores, int64_t ld_scores, const int32_t* q_pos
 csa_status csa_index_topk_workspace(int B, int Tq, int N, int H_I, int d_I, int k,
                                     size_t* bytes);
 csa_status csa_index_topk(const void* q_idx, const void* k_idx, const float* w,
-                          const int32_t* q_pos, int B, int Tq, int N, int H_I, int d_I,
+                          int64_t w_stride, const int32_t* q_pos, int B, int Tq, int N, int H_I, int d_I,
                           int m, int k, int32_t* idx_out, float* score_out,
                           void* ws, size_t ws_bytes, void* stream);
 
@@ -249,16 +277,39 @@ typedef struct csa_layer_args {
     const int32_t* raw_base;       /* [B]                                       */
     const void* q;                 /* [B, Tq, H, d]                             */
     const void* q_idx;             /* [B, Tq, H_I, d_I]                         */
-    const float* w;                /* [H_I]                                     */
+    const float* w;                /* [H_I], or per query (w_stride)            */
     const int32_t* q_pos;          /* [B, Tq]                                   */
     int32_t* idx_out;              /* [B, Tq, k] or NULL (kept in workspace)    */
     void* out;                     /* [B, Tq, H, d]                             */
     int out_dtype;
     float* lse;                    /* [B, Tq, H] or NULL                        */
+    /* Decode-time append (all four non-NULL, or all NULL): before step (2)
+     * every block that a query position completes ((t + 1) % m == 0) is
+     * compressed into the caches from the window rows, as csa_append does
+     * with the raw streams k_win, v_win, i_win and these gate logits.  Not
+     * combined with step (1) (g_k, g_v, g_i must then be NULL). */
+    const void* i_win;             /* raw indexer keys of the window rows [B, T_raw, d_I] */
+    const void *gk_win, *gv_win, *gi_win;  /* their gate logits [B, T_raw, d / d / d_I] */
+    long long w_stride;            /* 0: w is [H_I]; >= H_I: w is per query, see (2) */
 } csa_layer_args;
 
 csa_status csa_layer_workspace(const csa_layer_args* a, size_t* bytes);
 csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* stream);
+
+/* csa_layer for a caller whose step inputs and result live in HOST memory:
+ * on ``stream`` it copies q_host ([B, Tq, H, d] bf16) into a->q and
+ * q_idx_host ([B, Tq, H_I, d_I] bf16) into a->q_idx, enqueues the layer
+ * exactly as csa_layer does, then copies a->out into out_host
+ * ([B, Tq, H, d] of a->out_dtype).  The compressed caches, the window buffer
+ * and the weights stay resident on the device; a->q, a->q_idx and a->out are
+ * the caller's device staging buffers.  The host buffers should be
+ * page-locked (cudaHostAlloc, or torch's pin_memory) so that the copies are
+ * asynchronous; out_host holds the result once the stream reaches the end
+ * of the call (synchronise on it, or on an event recorded after the call).
+ * All checks of csa_layer run before the first copy is enqueued; a NULL host
+ * pointer is CSA_ERR_INVALID. */
+csa_status csa_layer_host(const csa_layer_args* a, const void* q_host, const void* q_idx_host,
+                          void* out_host, void* ws, size_t ws_bytes, void* stream);
 
 /* Test hook: the clock64 budget of every bounded device-side wait issued by
  * later calls in this process (default ~2^31 cycles, about one second).

@@ -6,6 +6,7 @@ stream.  Tensors must be CUDA, contiguous, bf16 where the C ABI says bf16,
 int32 for positions and indices, fp32 for the indexer weights.
 
     csa_compress     (1) block compression of up to three streams
+    csa_append       (1') decode-time compression of completed blocks into the caches
     csa_index_scores (2) Lightning-Indexer scores
     csa_topk         (3) per-query top-k of given scores
     csa_index_topk   (2)+(3)
@@ -24,7 +25,7 @@ import torch
 from . import _lib
 from ._lib import CSA_BF16, CSA_F32, CsaError, check, csa_layer_args
 
-__all__ = ["csa_compress", "csa_index_scores", "csa_topk", "csa_index_topk", "csa_attend",
+__all__ = ["csa_compress", "csa_append", "csa_index_scores", "csa_topk", "csa_index_topk", "csa_attend",
            "hca_attend", "csa_layer", "Workspace", "CsaError", "scores_ld"]
 
 
@@ -120,7 +121,33 @@ def csa_compress(xs: Sequence[torch.Tensor], gs: Sequence[torch.Tensor], m: int,
     return list(outs)
 
 
+def csa_append(x_wins: Sequence[torch.Tensor], g_wins: Sequence[torch.Tensor], outs: Sequence[torch.Tensor],
+               raw_base: torch.Tensor, q_pos: torch.Tensor, m: int, ws: Optional[Workspace] = None) -> None:
+    """Decode-time compression: the blocks completed by the positions q_pos,
+    from the window rows x_wins / g_wins ([B, T_raw, D]) into the caches outs
+    ([B, N, D] bf16), in place."""
+    n = len(x_wins)
+    B, T_raw = x_wins[0].shape[0], x_wins[0].shape[1]
+    P = ctypes.c_void_p * 3
+    D = (ctypes.c_int * 3)(*[x.shape[2] for x in x_wins] + [0] * (3 - n))
+    w_ = _ws(_lib.CSA_WS_HEADER_BYTES, ws)
+    st = _lib.lib().csa_append(n, P(*[_ptr(x) for x in x_wins]), P(*[_ptr(g) for g in g_wins]),
+                               P(*[_ptr(o) for o in outs]), D, _ptr(raw_base), _ptr(q_pos), B, q_pos.shape[1],
+                               T_raw, outs[0].shape[1], m, w_.ptr, w_.nbytes, _stream())
+    check("csa_append", st)
+
+
 # ---------------------------------------------------------------- (2), (3)
+
+def _w_stride(w: torch.Tensor, B: int, Tq: int, H_I: int) -> int:
+    """0 for one [H_I] weight vector shared by every query; H_I for per-query
+    weights [B, Tq, H_I]."""
+    if w.dim() == 1:
+        return 0
+    if tuple(w.shape) != (B, Tq, H_I):
+        raise ValueError("indexer weights must be [H_I] or [B, Tq, H_I]")
+    return H_I
+
 
 def csa_index_scores(q_idx: torch.Tensor, k_idx: torch.Tensor, w: torch.Tensor, q_pos: torch.Tensor,
                      m: int, scores: Optional[torch.Tensor] = None,
@@ -130,7 +157,8 @@ def csa_index_scores(q_idx: torch.Tensor, k_idx: torch.Tensor, w: torch.Tensor, 
     if scores is None:
         scores = torch.full((B, Tq, scores_ld(N)), float("nan"), dtype=torch.float32, device=q_idx.device)
     w_ = _ws(_lib.CSA_WS_HEADER_BYTES, ws)
-    st = _lib.lib().csa_index_scores(_ptr(q_idx), _ptr(k_idx), _ptr(w), _ptr(q_pos), B, Tq, N, H_I, d_I, m,
+    st = _lib.lib().csa_index_scores(_ptr(q_idx), _ptr(k_idx), _ptr(w), _w_stride(w, B, Tq, H_I), _ptr(q_pos),
+                                     B, Tq, N, H_I, d_I, m,
                                      _ptr(scores), scores.shape[-1], w_.ptr, w_.nbytes, _stream())
     check("csa_index_scores", st)
     return scores
@@ -160,7 +188,8 @@ def csa_index_topk(q_idx: torch.Tensor, k_idx: torch.Tensor, w: torch.Tensor, q_
     w_ = _ws(need.value, ws)
     idx = torch.empty(B, Tq, k, dtype=torch.int32, device=q_idx.device)
     sel = torch.empty(B, Tq, k, dtype=torch.float32, device=q_idx.device) if with_scores else None
-    st = _lib.lib().csa_index_topk(_ptr(q_idx), _ptr(k_idx), _ptr(w), _ptr(q_pos), B, Tq, N, H_I, d_I, m, k,
+    st = _lib.lib().csa_index_topk(_ptr(q_idx), _ptr(k_idx), _ptr(w), _w_stride(w, B, Tq, H_I), _ptr(q_pos),
+                                   B, Tq, N, H_I, d_I, m, k,
                                    _ptr(idx), _ptr(sel), w_.ptr, w_.nbytes, _stream())
     check("csa_index_topk", st)
     return (idx, sel) if with_scores else idx
@@ -208,16 +237,19 @@ def hca_attend(q, k_cmp, v_cmp, k_raw, v_raw, raw_base, q_pos, m: int, W: int, s
 def layer_args(*, B, Tq, N, m, H, d, H_I, d_I, k, W, T=0, T_raw=0, scale=0.0, x_k=None, x_v=None, x_i=None,
                g_k=None, g_v=None, g_i=None, k_cmp=None, v_cmp=None, i_cmp=None, k_win=None, v_win=None,
                raw_base=None, q=None, q_idx=None, w=None, q_pos=None, idx_out=None, out=None,
-               out_dtype=torch.bfloat16, lse=None) -> csa_layer_args:
+               out_dtype=torch.bfloat16, lse=None, i_win=None, gk_win=None, gv_win=None,
+               gi_win=None) -> csa_layer_args:
     a = csa_layer_args()
     for name, v in dict(B=B, Tq=Tq, N=N, m=m, H=H, d=d, H_I=H_I, d_I=d_I, k=k, W=W, T=T, T_raw=T_raw).items():
         setattr(a, name, int(v))
     a.scale = float(scale)
     for name, t in dict(x_k=x_k, x_v=x_v, x_i=x_i, g_k=g_k, g_v=g_v, g_i=g_i, k_cmp=k_cmp, v_cmp=v_cmp,
                         i_cmp=i_cmp, k_win=k_win, v_win=v_win, raw_base=raw_base, q=q, q_idx=q_idx, w=w,
-                        q_pos=q_pos, idx_out=idx_out, out=out, lse=lse).items():
+                        q_pos=q_pos, idx_out=idx_out, out=out, lse=lse, i_win=i_win, gk_win=gk_win,
+                        gv_win=gv_win, gi_win=gi_win).items():
         setattr(a, name, _ptr(t))
     a.out_dtype = _odt(out_dtype)
+    a.w_stride = 0 if w is None or w.dim() == 1 else int(w.shape[-1])
     return a
 
 

@@ -31,6 +31,8 @@ class csa_layer_args(ctypes.Structure):
         ("k_win", c_vp), ("v_win", c_vp),
         ("raw_base", c_vp), ("q", c_vp), ("q_idx", c_vp), ("w", c_vp), ("q_pos", c_vp),
         ("idx_out", c_vp), ("out", c_vp), ("out_dtype", c_int), ("lse", c_vp),
+        ("i_win", c_vp), ("gk_win", c_vp), ("gv_win", c_vp), ("gi_win", c_vp),
+        ("w_stride", ctypes.c_longlong),
     ]
 
 
@@ -42,14 +44,17 @@ SIGNATURES = {
     "csa_check_error": (c_int, [c_vp, c_u32p, c_int, c_vp]),
     "csa_compress": (c_int, [c_int, ctypes.POINTER(c_vp), ctypes.POINTER(c_vp), ctypes.POINTER(c_vp),
                              ctypes.POINTER(c_int), c_int, c_int, c_int, c_int, c_vp]),
-    "csa_index_scores": (c_int, [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_int,
-                                 c_vp, ctypes.c_int64, c_vp, c_size, c_vp]),
+    "csa_append": (c_int, [c_int, ctypes.POINTER(c_vp), ctypes.POINTER(c_vp), ctypes.POINTER(c_vp),
+                           ctypes.POINTER(c_int), c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_vp, c_size,
+                           c_vp]),
+    "csa_index_scores": (c_int, [c_vp, c_vp, c_vp, ctypes.c_int64, c_vp, c_int, c_int, c_int, c_int, c_int,
+                                 c_int, c_vp, ctypes.c_int64, c_vp, c_size, c_vp]),
     "csa_topk": (c_int, [c_vp, ctypes.c_int64, c_vp, c_int, c_int, c_int, c_int, c_int, c_vp, c_vp,
                          c_vp, c_size, c_vp]),
     "csa_topk_workspace": (c_int, [c_int, c_int, c_int, c_int, c_sizep]),
     "csa_index_topk_workspace": (c_int, [c_int, c_int, c_int, c_int, c_int, c_int, c_sizep]),
-    "csa_index_topk": (c_int, [c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
-                               c_vp, c_vp, c_vp, c_size, c_vp]),
+    "csa_index_topk": (c_int, [c_vp, c_vp, c_vp, ctypes.c_int64, c_vp, c_int, c_int, c_int, c_int, c_int, c_int,
+                               c_int, c_vp, c_vp, c_vp, c_size, c_vp]),
     "csa_attend_workspace": (c_int, [c_int, c_int, c_int, c_int, c_int, c_int, c_sizep]),
     "csa_attend": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_int, c_int, c_int, c_int,
                            c_int, c_int, c_int, c_int, c_float, c_vp, c_int, c_vp, c_vp, c_size, c_vp]),
@@ -60,6 +65,7 @@ SIGNATURES = {
                            c_int, c_int, c_int, c_float, c_vp, c_int, c_vp, c_vp, c_size, c_vp]),
     "csa_layer_workspace": (c_int, [ctypes.POINTER(csa_layer_args), c_sizep]),
     "csa_layer": (c_int, [ctypes.POINTER(csa_layer_args), c_vp, c_size, c_vp]),
+    "csa_layer_host": (c_int, [ctypes.POINTER(csa_layer_args), c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
     "csa_set_wait_budget": (None, [c_ll]),
     "csa_set_indexer_events": (None, [c_vp, c_vp]),
 }

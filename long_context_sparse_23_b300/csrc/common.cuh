@@ -353,6 +353,19 @@ inline cudaError_t ensure_dyn_smem(int bytes) {
   return e;
 }
 
+// Number of SMs of the current device (asked once per device).
+inline int sm_count() {
+  static std::atomic<int> n[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  int v = n[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    n[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
 // Allow clusters of more than 8 CTAs for ``kern``, once per device (atomic
 // per-device record, as above).
 template <typename K>

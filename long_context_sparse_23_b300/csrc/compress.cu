@@ -118,6 +118,57 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
   }
 }
 
+// Decode-time append: one thread per (query, 16-byte channel vector, stream).
+// A query at position t with (t + 1) % m == 0 completes block (t + 1) / m - 1,
+// whose m raw rows t - m + 1 .. t sit in the window buffer; they are folded
+// exactly as compress_kernel folds a block (same chunks, same order), so the
+// appended entry is bit-identical to the prefill compression of that block.
+template <int R>
+__global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
+  pdl_wait_then_release();
+  const int sidx = blockIdx.y;
+  const int D = sidx == 0 ? a.D[0] : (sidx == 1 ? a.D[1] : a.D[2]);
+  const void* xsel = sidx == 0 ? a.x[0] : (sidx == 1 ? a.x[1] : a.x[2]);
+  const void* gsel = sidx == 0 ? a.g[0] : (sidx == 1 ? a.g[1] : a.g[2]);
+  void* osel = sidx == 0 ? a.out[0] : (sidx == 1 ? a.out[1] : a.out[2]);
+  const int G = D >> 3;
+  const long long nwork = static_cast<long long>(a.B) * a.Tq * G;
+  const size_t row_bytes = static_cast<size_t>(D) * 2;
+  for (long long wi = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; wi < nwork;
+       wi += static_cast<long long>(gridDim.x) * kThreads) {
+    const int cg = static_cast<int>(wi % G);
+    const long long qi = wi / G;
+    const int b = static_cast<int>(qi / a.Tq);
+    const int t = a.q_pos[qi];
+    if (t < 0 || (t + 1) % a.m != 0) continue;
+    const int blk = (t + 1) / a.m - 1;
+    const long long r0 = static_cast<long long>(t) - a.m + 1 - a.raw_base[b];
+    if (blk >= a.N || r0 < 0 || r0 + a.m > a.T_raw) {
+      if (cg == 0) raise_flag(a.errw, kFlagIndex);
+      continue;
+    }
+    const size_t off = (static_cast<size_t>(b) * a.T_raw + static_cast<size_t>(r0)) * row_bytes +
+                       static_cast<size_t>(cg) * 16;
+    float M[8], L[8], A[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      M[c] = -INFINITY;
+      L[c] = 0.f;
+      A[c] = 0.f;
+    }
+    for (int j0 = 0; j0 < a.m; j0 += R)
+      fold_rows<R>(static_cast<const char*>(xsel) + off + static_cast<size_t>(j0) * row_bytes,
+                   static_cast<const char*>(gsel) + off + static_cast<size_t>(j0) * row_bytes, row_bytes, M, L, A);
+    uint4 v;
+    v.x = pack_bf16x2(A[0] / L[0], A[1] / L[1]);
+    v.y = pack_bf16x2(A[2] / L[2], A[3] / L[3]);
+    v.z = pack_bf16x2(A[4] / L[4], A[5] / L[5]);
+    v.w = pack_bf16x2(A[6] / L[6], A[7] / L[7]);
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(osel) + (static_cast<size_t>(b) * a.N + blk) * D +
+                              static_cast<size_t>(cg) * 8) = v;
+  }
+}
+
 template <int R>
 cudaError_t launch_r(const CompressArgs& a, dim3 grid, cudaStream_t s) {
   if (a.out_f32) return launch_k(compress_kernel<R, true>, grid, dim3(kThreads), 0, s, 1, a);
@@ -141,6 +192,22 @@ cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s) {
   if (a.m % 4 == 0) return launch_r<4>(a, grid, s);
   if (a.m % 2 == 0) return launch_r<2>(a, grid, s);
   return launch_r<1>(a, grid, s);
+}
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
+  long long maxwork = 0;
+  for (int i = 0; i < a.n_streams; ++i) {
+    const long long w = static_cast<long long>(a.B) * a.Tq * (a.D[i] / 8);
+    maxwork = w > maxwork ? w : maxwork;
+  }
+  if (maxwork == 0) return cudaSuccess;
+  long long blocks = (maxwork + kThreads - 1) / kThreads;
+  if (blocks > 148LL * 8) blocks = 148LL * 8;
+  const dim3 grid(static_cast<unsigned>(blocks), a.n_streams);
+  if (a.m % 8 == 0) return launch_k(append_kernel<8>, grid, dim3(kThreads), 0, s, 1, a);
+  if (a.m % 4 == 0) return launch_k(append_kernel<4>, grid, dim3(kThreads), 0, s, 1, a);
+  if (a.m % 2 == 0) return launch_k(append_kernel<2>, grid, dim3(kThreads), 0, s, 1, a);
+  return launch_k(append_kernel<1>, grid, dim3(kThreads), 0, s, 1, a);
 }
 
 }  // namespace csa

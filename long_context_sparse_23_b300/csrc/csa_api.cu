@@ -233,18 +233,50 @@ csa_status csa_compress(int n_streams, const void* const* x, const void* const* 
   return cuda_status(csa::launch_compress(a, static_cast<cudaStream_t>(stream)));
 }
 
+csa_status csa_append(int n_streams, const void* const* x_win, const void* const* g_win, void* const* out,
+                      const int* D, const int32_t* raw_base, const int32_t* q_pos, int B, int Tq, int T_raw,
+                      int N, int m, void* ws, size_t ws_bytes, void* stream) {
+  if (n_streams < 1 || n_streams > 3 || !x_win || !g_win || !out || !D) return CSA_ERR_INVALID;
+  if (!raw_base || !q_pos || !al4(raw_base) || !al4(q_pos)) return CSA_ERR_INVALID;
+  if (B <= 0 || Tq <= 0 || N <= 0 || m < 1 || m > 4096 || T_raw < m) return CSA_ERR_INVALID;
+  csa::AppendArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int i = 0; i < n_streams; ++i) {
+    if (D[i] <= 0 || D[i] % 8 != 0 || D[i] > 512) return CSA_ERR_INVALID;
+    if (!x_win[i] || !g_win[i] || !out[i] || !al16(x_win[i]) || !al16(g_win[i]) || !al16(out[i]))
+      return CSA_ERR_INVALID;
+    a.x[i] = x_win[i];
+    a.g[i] = g_win[i];
+    a.out[i] = out[i];
+    a.D[i] = D[i];
+  }
+  const csa_status st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES);
+  if (st != CSA_OK) return st;
+  a.n_streams = n_streams;
+  a.raw_base = raw_base;
+  a.q_pos = q_pos;
+  a.B = B;
+  a.Tq = Tq;
+  a.T_raw = T_raw;
+  a.N = N;
+  a.m = m;
+  a.errw = err_word(ws);
+  return cuda_status(csa::launch_append(a, static_cast<cudaStream_t>(stream)));
+}
+
 // ---------------------------------------------------------------- (2)
-csa_status csa_index_scores(const void* q_idx, const void* k_idx, const float* w,
+csa_status csa_index_scores(const void* q_idx, const void* k_idx, const float* w, int64_t w_stride,
                             const int32_t* q_pos, int B, int Tq, int N, int H_I, int d_I, int m,
                             float* scores, int64_t ld_scores, void* ws, size_t ws_bytes,
                             void* stream) {
   csa_status st = check_index_args(q_idx, k_idx, w, q_pos, B, Tq, N, H_I, d_I, m);
   if (st != CSA_OK) return st;
+  if (w_stride != 0 && w_stride < H_I) return CSA_ERR_INVALID;
   if (!scores || !al16(scores) || ld_scores < N || ld_scores % 4 != 0) return CSA_ERR_INVALID;
   st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES);
   if (st != CSA_OK) return st;
   csa::IndexerArgs a{q_idx, k_idx, w, q_pos, scores, ld_scores, B, Tq, N, H_I, d_I, m,
-                     err_word(ws), g_wait_budget, nullptr, 0};
+                     err_word(ws), g_wait_budget, nullptr, 0, w_stride};
   return cuda_status(launch_indexer_marked(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -279,12 +311,13 @@ csa_status csa_index_topk_workspace(int B, int Tq, int N, int H_I, int d_I, int 
   return CSA_OK;
 }
 
-csa_status csa_index_topk(const void* q_idx, const void* k_idx, const float* w,
+csa_status csa_index_topk(const void* q_idx, const void* k_idx, const float* w, int64_t w_stride,
                           const int32_t* q_pos, int B, int Tq, int N, int H_I, int d_I, int m,
                           int k, int32_t* idx_out, float* score_out, void* ws, size_t ws_bytes,
                           void* stream) {
   csa_status st = check_index_args(q_idx, k_idx, w, q_pos, B, Tq, N, H_I, d_I, m);
   if (st != CSA_OK) return st;
+  if (w_stride != 0 && w_stride < H_I) return CSA_ERR_INVALID;
   st = check_topk_args(q_pos, B, Tq, N, m, k, idx_out, score_out);
   if (st != CSA_OK) return st;
   size_t need = 0;
@@ -294,7 +327,8 @@ csa_status csa_index_topk(const void* q_idx, const void* k_idx, const float* w,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* S = reinterpret_cast<float*>(static_cast<char*>(ws) + CSA_WS_HEADER_BYTES);
   const long long ld = scores_ld(N);
-  csa::IndexerArgs ia{q_idx, k_idx, w, q_pos, S, ld, B, Tq, N, H_I, d_I, m, err_word(ws), g_wait_budget, nullptr, 0};
+  csa::IndexerArgs ia{q_idx, k_idx, w, q_pos, S, ld, B, Tq, N, H_I, d_I, m, err_word(ws), g_wait_budget, nullptr, 0,
+                      w_stride};
   csa::TopkArgs ta{S, ld, q_pos, B, Tq, N, m, k, idx_out, score_out, nullptr, nullptr, nullptr, nullptr, nullptr};
   return index_then_topk(ia, ta, reinterpret_cast<char*>(S) + scores_bytes(B, Tq, N), s);
 }
@@ -387,9 +421,24 @@ csa_status csa_layer_workspace(const csa_layer_args* a, size_t* bytes) {
   return CSA_OK;
 }
 
-csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* stream) {
+// Every argument check of csa_layer (nothing is enqueued).
+static bool layer_appends(const csa_layer_args* a) {
+  return a->i_win || a->gk_win || a->gv_win || a->gi_win;
+}
+
+static csa_status layer_check(const csa_layer_args* a, const void* ws, size_t ws_bytes) {
   if (!a) return CSA_ERR_INVALID;
   const bool do_compress = a->g_k || a->g_v || a->g_i;
+  if (layer_appends(a)) {
+    if (do_compress) return CSA_ERR_INVALID;  // a prefill compresses every block itself
+    if (!a->i_win || !a->gk_win || !a->gv_win || !a->gi_win || !a->k_win || !a->v_win) return CSA_ERR_INVALID;
+    if (!al16(a->i_win) || !al16(a->gk_win) || !al16(a->gv_win) || !al16(a->gi_win) || !a->k_cmp ||
+        !a->v_cmp || !a->i_cmp || !al16(a->k_cmp) || !al16(a->v_cmp) || !al16(a->i_cmp))
+      return CSA_ERR_INVALID;
+    if (a->d % 8 != 0 || a->d_I % 8 != 0 || a->d > 512 || a->d_I > 512 || a->m < 1 || a->m > 4096 ||
+        a->T_raw < a->m)
+      return CSA_ERR_INVALID;
+  }
   if (do_compress) {
     if (!a->g_k || !a->g_v || !a->g_i || !a->x_k || !a->x_v || !a->x_i) return CSA_ERR_INVALID;
     if (a->m <= 0 || a->T < 0 || a->T / a->m != a->N) return CSA_ERR_INVALID;
@@ -398,6 +447,7 @@ csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* s
   csa_status st = check_index_args(a->q_idx, a->i_cmp, a->w, a->q_pos, a->B, a->Tq, a->N, a->H_I,
                                    a->d_I, a->m);
   if (st != CSA_OK) return st;
+  if (a->w_stride != 0 && a->w_stride < a->H_I) return CSA_ERR_INVALID;
   int32_t* idx = a->idx_out;
   st = idx ? check_topk_args(a->q_pos, a->B, a->Tq, a->N, a->m, a->k, idx, nullptr)
            : check_topk_shape(a->q_pos, a->B, a->Tq, a->N, a->m, a->k);
@@ -411,10 +461,43 @@ csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* s
     return CSA_ERR_INVALID;
   size_t need = 0;
   csa_layer_workspace(a, &need);
-  st = check_ws(ws, ws_bytes, need);
-  if (st != CSA_OK) return st;
+  return check_ws(ws, ws_bytes, need);
+}
 
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+// Enqueue steps (1)-(4) of an already checked call.
+static csa_status layer_enqueue(const csa_layer_args* a, void* ws, cudaStream_t s) {
+  const bool do_compress = a->g_k || a->g_v || a->g_i;
+  int32_t* idx = a->idx_out;
+  csa_status st = CSA_OK;
+  if (layer_appends(a)) {
+    // the blocks this step's positions complete enter the caches before the
+    // indexer reads them (the next kernels start only after this one ends)
+    csa::AppendArgs ap;
+    std::memset(&ap, 0, sizeof(ap));
+    ap.x[0] = a->k_win;
+    ap.x[1] = a->v_win;
+    ap.x[2] = a->i_win;
+    ap.g[0] = a->gk_win;
+    ap.g[1] = a->gv_win;
+    ap.g[2] = a->gi_win;
+    ap.out[0] = a->k_cmp;
+    ap.out[1] = a->v_cmp;
+    ap.out[2] = a->i_cmp;
+    ap.D[0] = a->d;
+    ap.D[1] = a->d;
+    ap.D[2] = a->d_I;
+    ap.n_streams = 3;
+    ap.raw_base = a->raw_base;
+    ap.q_pos = a->q_pos;
+    ap.B = a->B;
+    ap.Tq = a->Tq;
+    ap.T_raw = a->T_raw;
+    ap.N = a->N;
+    ap.m = a->m;
+    ap.errw = err_word(ws);
+    st = cuda_status(csa::launch_append(ap, s));
+    if (st != CSA_OK) return st;
+  }
   char* base = static_cast<char*>(ws) + CSA_WS_HEADER_BYTES;
   float* S = reinterpret_cast<float*>(base);
   base += scores_bytes(a->B, a->Tq, a->N);
@@ -449,7 +532,7 @@ csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* s
   }
   const long long ld = scores_ld(a->N);
   csa::IndexerArgs ia{a->q_idx, a->i_cmp, a->w, a->q_pos, S, ld, a->B, a->Tq, a->N, a->H_I, a->d_I,
-                      a->m, err_word(ws), g_wait_budget, nullptr, 0};
+                      a->m, err_word(ws), g_wait_budget, nullptr, 0, a->w_stride};
   csa::TopkArgs ta{S, ld, a->q_pos, a->B, a->Tq, a->N, a->m, a->k, idx, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   if (!do_compress && csa::tail_supported(a->Tq, a->N, a->k, a->W, a->H, a->d)) {
     // decode: indexer (+ bucket histogram), then one fused top-k + attention kernel
@@ -538,6 +621,31 @@ csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* s
   at.part = reinterpret_cast<float*>(base);
   at.errw = err_word(ws);
   return cuda_status(launch_attention(at, s));
+}
+
+csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* stream) {
+  const csa_status st = layer_check(a, ws, ws_bytes);
+  if (st != CSA_OK) return st;
+  return layer_enqueue(a, ws, static_cast<cudaStream_t>(stream));
+}
+
+csa_status csa_layer_host(const csa_layer_args* a, const void* q_host, const void* q_idx_host,
+                          void* out_host, void* ws, size_t ws_bytes, void* stream) {
+  csa_status st = layer_check(a, ws, ws_bytes);
+  if (st != CSA_OK) return st;
+  if (!q_host || !q_idx_host || !out_host) return CSA_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t nq = static_cast<size_t>(a->B) * a->Tq;
+  const size_t q_bytes = nq * a->H * a->d * 2;
+  const size_t qi_bytes = nq * a->H_I * a->d_I * 2;
+  const size_t out_bytes = nq * a->H * a->d * (a->out_dtype == CSA_F32 ? 4 : 2);
+  if (cudaMemcpyAsync(const_cast<void*>(a->q), q_host, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(const_cast<void*>(a->q_idx), q_idx_host, qi_bytes, cudaMemcpyHostToDevice, s) !=
+          cudaSuccess)
+    return CSA_ERR_CUDA;
+  st = layer_enqueue(a, ws, s);
+  if (st != CSA_OK) return st;
+  return cuda_status(cudaMemcpyAsync(out_host, a->out, out_bytes, cudaMemcpyDeviceToHost, s));
 }
 
 }  // extern "C"

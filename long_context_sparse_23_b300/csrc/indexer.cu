@@ -29,15 +29,19 @@ namespace csa {
 
 namespace {
 
-constexpr int kEpiGroups = 2;                       // epilogue warp groups, alternating tiles
-constexpr int kThreads = 64 + 128 * kEpiGroups;    // producer, MMA, epilogue warps
+constexpr int kEpiGroups = 2;                      // epilogue warp groups, alternating tiles
+constexpr int kEpiWarp0 = 3;                       // first epilogue warp
+constexpr int kThreads = 32 * kEpiWarp0 + 128 * kEpiGroups;  // 3 role warps + 8 epilogue warps
 constexpr int kTileKeys = 128;
 constexpr int kHalfBytes = kTileKeys * 128;  // one 64-wide K half of a key tile
-constexpr int kSmemBudget = 220 * 1024;
+constexpr int kMaxG = 64;                    // queries per group (H_I >= 4, G * H_I <= 256)
+constexpr int kSmemLimit = 227 * 1024;       // dynamic + static shared memory per CTA
+constexpr int kStaticSmem = 4 * 1024;        // upper bound of the kernel's static shared memory
 constexpr long long kDrainBudget = 1LL << 31;
 
 struct KParams {
   const float* w;
+  long long w_stride;  // 0: one [HI] vector for every query; else w[(n * Tq + j) * w_stride + h]
   const int32_t* q_pos;
   float* S;
   long long ld;
@@ -49,21 +53,82 @@ struct KParams {
   int n_groups;       // ceil(Tq / G)
   int items_per_group;
   int tiles_per_item;
+  int items;          // B * n_groups * items_per_group
   int tmem_cols;
   uint32_t* errw;
   long long budget;
   uint32_t* hist;  // [B*Tq][kTopkBins] (G == 1 only), or nullptr
   int after_zero;  // see IndexerArgs::after_zero
+  const void* q_base;  // the indexer queries (for the L2 prefetch of the next item's rows)
+  int q_row_bytes;     // d_I * 2
 };
 
 struct __align__(8) Bars {
-  uint64_t full[8];
-  uint64_t empty[8];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
-  uint64_t qfull;
+  uint64_t full[8];    // key stage loaded
+  uint64_t empty[8];   // key stage consumed by the MMAs
+  uint64_t tfull[2];   // accumulator buffer written by the MMAs
+  uint64_t tempty[2];  // accumulator buffer read by its epilogue group
+  uint64_t qfull;      // the item's queries loaded
+  uint64_t qfree;      // the item's MMAs done: the query buffer may be refilled
+  uint64_t wfull[2];   // head weights / visibility of an item written
+  uint64_t wfree[2];   // both epilogue groups are done with an item's weights
 };
 
+// One work item: a group of G queries of sequence b against the key tiles
+// [tile_lo, tile_lo + ntile) (ntile <= 0: nothing of that range is visible).
+struct Item {
+  int b, j0, tile_lo, ntile;
+};
+
+// Item of rank r, rank 0 the heaviest: query groups from the last (longest
+// visible prefix) to the first; the sequences and tile ranges of one group
+// next to each other.
+__device__ __forceinline__ Item item_of(const KParams& p, int r) {
+  Item it;
+  const int per_g = p.B * p.items_per_group;
+  const int g = p.n_groups - 1 - r / per_g;
+  const int rem = r % per_g;
+  it.b = rem / p.items_per_group;
+  const int sub = rem % p.items_per_group;
+  it.j0 = g * p.G;
+  const int jn = min(p.G, p.Tq - it.j0);
+  int nv_max = 0;
+  for (int jj = 0; jj < jn; ++jj) {
+    const int t = p.q_pos[static_cast<long long>(it.b) * p.Tq + it.j0 + jj];
+    const int nv = t >= 0 ? (t + 1) / p.m : 0;
+    nv_max = max(nv_max, min(nv, p.N));
+  }
+  const int n_tiles_all = (p.N + kTileKeys - 1) / kTileKeys;
+  const int tiles_vis = (nv_max + kTileKeys - 1) / kTileKeys;
+  it.tile_lo = sub * p.tiles_per_item;
+  it.ntile = min(min(it.tile_lo + p.tiles_per_item, n_tiles_all), tiles_vis) - it.tile_lo;
+  return it;
+}
+
+// Rank of this CTA's k-th item, or -1: rounds of gridDim.x ranks, taken in
+// alternating direction (snake order), so every CTA gets a similar share of
+// heavy and light items.
+__device__ __forceinline__ int rank_of(int k, const KParams& p) {
+  const int n = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  const long long r = static_cast<long long>(k) * n + ((k & 1) ? n - 1 - c : c);
+  return r < p.items ? static_cast<int>(r) : -1;
+}
+
+__device__ __forceinline__ void group_bar(int g) {
+  asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
+}
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
+
+// Persistent kernel: one CTA per SM walks its items; the key ring, the TMEM
+// accumulator pair and the item buffers run on across item boundaries.
+// Warp roles (352 threads):
+//   warp 0      key producer: TMA key tiles into the S-stage ring;
+//   warp 1      allocates TMEM; one lane issues the MMAs;
+//   warp 2      item producer: per item, the head weights and visibility
+//               (double-buffered) and the query rows (TMA, one buffer, loaded
+//               once the previous item's MMAs are done; the next item's rows
+//               are prefetched into L2 meanwhile);
+//   warps 3-10  epilogue, two groups of four alternating tiles.
 template <int HI>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
@@ -79,33 +144,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   char* qs = smem;                                      // [kh][NC][128 B]
   char* ks = qs + p.kh * p.NC * 128;                    // [stages][kh][128][128 B]
   Bars* bars = reinterpret_cast<Bars*>(ks + p.stages * p.kh * kHalfBytes);
-  // top-k bucket histogram of this CTA's scores (one query per group)
+  // top-k bucket histogram of the current item's scores (one query per group)
   uint32_t* hist_s = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(bars) + sizeof(Bars));
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
-  __shared__ float w_s[HI];
-  __shared__ int nvis_s[256];
+  __shared__ float w_s[2][256];      // [item parity][G][HI] head weights of each query of the item
+  __shared__ int nvis_s[2][kMaxG];   // [item parity][G] visible blocks of each query
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // ---- which (sequence, query group, tile range) this CTA owns; heavy first
-  const int item = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
-  const int grp = item / p.items_per_group;
-  const int sub = item % p.items_per_group;
-  const int b = grp / p.n_groups;
-  const int j0 = (grp % p.n_groups) * p.G;
-  const int n_tiles_all = (p.N + kTileKeys - 1) / kTileKeys;
-
-  for (int jj = tid; jj < p.G; jj += kThreads) {
-    int nv = 0;
-    if (j0 + jj < p.Tq) {
-      const int t = p.q_pos[static_cast<long long>(b) * p.Tq + j0 + jj];
-      nv = t >= 0 ? (t + 1) / p.m : 0;
-      nv = nv < p.N ? nv : p.N;
-    }
-    nvis_s[jj] = nv;
-  }
-  for (int h = tid; h < HI; h += kThreads) w_s[h] = p.w[h];
   if (p.hist)
     for (int i = tid; i < kTopkBins; i += kThreads) hist_s[i] = 0u;
   if (tid == 0) {
@@ -117,18 +164,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->tfull[i], 1);
       mbar_init(&bars->tempty[i], 4);
+      mbar_init(&bars->wfull[i], 1);
+      mbar_init(&bars->wfree[i], kEpiGroups);
     }
     mbar_init(&bars->qfull, 1);
+    mbar_init(&bars->qfree, 1);
     mbar_fence_init();
   }
+  // does this CTA own any visible tile? (the same answer in every thread)
+  bool any = false;
+  for (int k = 0; !any; ++k) {
+    const int r = rank_of(k, p);
+    if (r < 0) break;
+    any = item_of(p, r).ntile > 0;
+  }
   __syncthreads();
-  int nv_max = 0;
-  for (int jj = 0; jj < p.G; ++jj) nv_max = max(nv_max, nvis_s[jj]);
-  const int tiles_vis = (nv_max + kTileKeys - 1) / kTileKeys;
-  const int tile_lo = sub * p.tiles_per_item;
-  const int tile_hi = min(min(tile_lo + p.tiles_per_item, n_tiles_all), tiles_vis);
-  const int ntile = tile_hi - tile_lo;
-  if (ntile <= 0) return;  // uniform: nothing visible in this range
+  if (!any) return;
 
   if (warp == 1) {
     tmem_alloc(&tmem_base, p.tmem_cols);
@@ -139,54 +190,70 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = tmem_base;
   volatile int* abort_v = &abort_flag;
+  auto fail = [&]() {
+    if (!*abort_v) raise_flag(p.errw, kFlagTimeout);
+    *abort_v = 1;
+  };
 
   if (warp == 0) {
+    // ---- key producer
     if (lane == 0) {
       tma_prefetch_desc(&tmk);
-      tma_prefetch_desc(&tmq);
-      const int qrow = (b * p.Tq + j0) * HI;
-      // the keys are read once: evict-first, so the scores this kernel writes
-      // stay in L2 for the top-k that reads them next
+      // the keys are read once per query group: evict-first, so the scores
+      // this kernel writes stay in L2 for the top-k that reads them next
       const uint64_t key_policy = l2_policy_evict_first();
-      mbar_expect_tx(&bars->qfull, p.kh * p.NC * 128);
-      for (int h = 0; h < p.kh; ++h) tma_load_2d(qs + h * p.NC * 128, &tmq, &bars->qfull, h * 64, qrow);
-      int issued = 0;
-      for (int i = 0; i < ntile; ++i) {
-        const int s = i % p.stages;
-        const uint32_t ph = (i / p.stages) & 1;
-        if (!mbar_wait(&bars->empty[s], ph ^ 1, p.budget, abort_v)) {
-          if (!*abort_v) raise_flag(p.errw, kFlagTimeout);
-          *abort_v = 1;
-          break;
+      int gt = 0;  // key tiles issued
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int r = rank_of(k, p);
+        if (r < 0) break;
+        const Item I = item_of(p, r);
+        for (int i = 0; i < I.ntile; ++i) {
+          const int s = gt % p.stages;
+          const uint32_t ph = (gt / p.stages) & 1;
+          if (!mbar_wait(&bars->empty[s], ph ^ 1, p.budget, abort_v)) {
+            fail();
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&bars->full[s], p.kh * kHalfBytes);
+          char* dst = ks + s * p.kh * kHalfBytes;
+          for (int h = 0; h < p.kh; ++h)
+            tma_load_3d_hint(dst + h * kHalfBytes, &tmk, &bars->full[s], h * 64, (I.tile_lo + i) * kTileKeys, I.b,
+                             key_policy);
+          ++gt;
         }
-        mbar_expect_tx(&bars->full[s], p.kh * kHalfBytes);
-        char* dst = ks + s * p.kh * kHalfBytes;
-        for (int h = 0; h < p.kh; ++h)
-          tma_load_3d_hint(dst + h * kHalfBytes, &tmk, &bars->full[s], h * 64, (tile_lo + i) * kTileKeys, b,
-                           key_policy);
-        issued = i + 1;
       }
       // drain: every issued copy has landed before the CTA may exit
-      for (int s = 0; s < p.stages && s < issued; ++s) {
-        const int last = issued - 1 - ((issued - 1 - s) % p.stages);
+      for (int s = 0; s < p.stages && s < gt; ++s) {
+        const int last = gt - 1 - ((gt - 1 - s) % p.stages);
         mbar_wait(&bars->full[s], (last / p.stages) & 1, kDrainBudget, nullptr);
       }
-      mbar_wait(&bars->qfull, 0, kDrainBudget, nullptr);
     }
   } else if (warp == 1) {
+    // ---- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, p.NC);
-      int issued = 0;
-      if (mbar_wait(&bars->qfull, 0, p.budget, abort_v)) {
-        for (int i = 0; i < ntile; ++i) {
-          const int s = i % p.stages;
-          const uint32_t ph = (i / p.stages) & 1;
-          const int acc = i & 1;
-          const uint32_t aph = (i >> 1) & 1;
+      int gt = 0, it = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int r = rank_of(k, p);
+        if (r < 0) break;
+        const Item I = item_of(p, r);
+        if (I.ntile <= 0) continue;
+        if (!mbar_wait(&bars->qfull, it & 1, p.budget, abort_v)) {
+          fail();
+          break;
+        }
+        for (int i = 0; i < I.ntile; ++i) {
+          const int s = gt % p.stages;
+          const uint32_t ph = (gt / p.stages) & 1;
+          const int acc = gt & 1;
+          const uint32_t aph = (gt >> 1) & 1;
           if (!mbar_wait(&bars->tempty[acc], aph ^ 1, p.budget, abort_v) ||
               !mbar_wait(&bars->full[s], ph, p.budget, abort_v)) {
-            if (!*abort_v) raise_flag(p.errw, kFlagTimeout);
-            *abort_v = 1;
+            fail();
+            ok = false;
             break;
           }
           tc_fence_after();
@@ -201,82 +268,184 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           umma_commit(&bars->empty[s]);
           umma_commit(&bars->tfull[acc]);
-          issued = i + 1;
+          ++gt;
         }
-      } else {
-        if (!*abort_v) raise_flag(p.errw, kFlagTimeout);
-        *abort_v = 1;
+        if (!ok) break;
+        umma_commit(&bars->qfree);  // the query buffer is free once this item's MMAs are done
+        ++it;
       }
       // drain: the last MMAs have finished reading shared memory / writing TMEM
-      if (issued > 0) {
-        const int i = issued - 1;
-        mbar_wait(&bars->tfull[i & 1], (i >> 1) & 1, kDrainBudget, nullptr);
-      }
+      if (gt > 0) mbar_wait(&bars->tfull[(gt - 1) & 1], ((gt - 1) >> 1) & 1, kDrainBudget, nullptr);
     }
-  } else {
-    // ---- epilogue warps 2..: TMEM lane quarter = warp % 4; group e handles
-    // the tiles i = e (mod kEpiGroups), i.e. TMEM accumulator buffer e
-    const int quarter = warp & 3;
-    const int egroup = (warp - 2) >> 2;
-    const int row = quarter * 32 + lane;
-    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
-    for (int i = egroup; i < ntile; i += kEpiGroups) {
-      const int acc = i & 1;
-      const uint32_t aph = (i >> 1) & 1;
-      if (!mbar_wait(&bars->tfull[acc], aph, p.budget, abort_v)) {
-        if (!*abort_v) raise_flag(p.errw, kFlagTimeout);
-        *abort_v = 1;
+  } else if (warp == 2) {
+    // ---- item producer: head weights, visibility and query rows
+    if (lane == 0) tma_prefetch_desc(&tmq);
+    int it = 0, q_issued = 0;
+    for (int k = 0;; ++k) {
+      const int r = rank_of(k, p);
+      if (r < 0) break;
+      const Item I = item_of(p, r);
+      if (I.ntile <= 0) continue;
+      const int ib = it & 1;
+      // the weight buffer of parity ib was last read for item it - 2
+      bool ok = true;
+      if (it >= 2 && lane == 0) ok = mbar_wait(&bars->wfree[ib], ((it - 2) >> 1) & 1, p.budget, abort_v);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) fail();
         break;
       }
-      tc_fence_after();
-      const int key = (tile_lo + i) * kTileKeys + row;
-      const uint32_t col0 = lane_addr + static_cast<uint32_t>(acc * p.NC);
-      if constexpr (HI >= 16) {
-        for (int jj = 0; jj < p.G; ++jj) {
-          // all of the query's head columns in flight at once, one wait
-          uint32_t r[HI / 16][16];
+      for (int i = lane; i < p.G * HI; i += 32) {
+        const int jj = i / HI, h = i % HI;
+        w_s[ib][i] = p.w_stride == 0
+                         ? p.w[h]
+                         : (I.j0 + jj < p.Tq
+                                ? p.w[(static_cast<long long>(I.b) * p.Tq + I.j0 + jj) * p.w_stride + h]
+                                : 0.f);
+      }
+      for (int jj = lane; jj < p.G; jj += 32) {
+        int nv = 0;
+        if (I.j0 + jj < p.Tq) {
+          const int t = p.q_pos[static_cast<long long>(I.b) * p.Tq + I.j0 + jj];
+          nv = t >= 0 ? (t + 1) / p.m : 0;
+          nv = nv < p.N ? nv : p.N;
+        }
+        nvis_s[ib][jj] = nv;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars->wfull[ib]);
+        // the query rows, once the MMAs of the previous item are done
+        ok = it == 0 || mbar_wait(&bars->qfree, (it - 1) & 1, p.budget, abort_v);
+        if (ok) {
+          mbar_expect_tx(&bars->qfull, p.kh * p.NC * 128);
+          const int qrow = (I.b * p.Tq + I.j0) * HI;
+          for (int h = 0; h < p.kh; ++h) tma_load_2d(qs + h * p.NC * 128, &tmq, &bars->qfull, h * 64, qrow);
+          q_issued = it + 1;
+          // the next item's query rows into L2 while this item runs
+          const int rn = rank_of(k + 1, p);
+          if (rn >= 0) {
+            const Item J = item_of(p, rn);
+            const int jn = min(p.G, p.Tq - J.j0);
+            const uint32_t bytes = static_cast<uint32_t>(jn * HI * p.q_row_bytes);
+            const char* src = static_cast<const char*>(p.q_base) +
+                              (static_cast<size_t>(J.b) * p.Tq + J.j0) * HI * p.q_row_bytes;
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+          }
+        } else {
+          fail();
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ++it;
+    }
+    // drain: the last query copy has landed before the CTA may exit
+    if (lane == 0 && q_issued > 0) mbar_wait(&bars->qfull, (q_issued - 1) & 1, kDrainBudget, nullptr);
+  } else {
+    // ---- epilogue warps: TMEM lane quarter = warp % 4; group e handles the
+    // CTA's tiles gt = e (mod 2), i.e. TMEM accumulator buffer e
+    const int ew = warp - kEpiWarp0;
+    const int egroup = ew >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t col0 = lane_addr + static_cast<uint32_t>(egroup * p.NC);
+    int gt = 0, it = 0;
+    bool waited_zero = false;
+    for (int k = 0;; ++k) {
+      const int r = rank_of(k, p);
+      if (r < 0) break;
+      const Item I = item_of(p, r);
+      if (I.ntile <= 0) continue;
+      const int ib = it & 1;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->wfull[ib], (it >> 1) & 1, p.budget, abort_v));
+      if (!ok && lane == 0) fail();
+      const float* wi = w_s[ib];
+      const int* nvi = nvis_s[ib];
+      const long long srow0 = static_cast<long long>(I.b) * p.Tq + I.j0;
+      for (int i = 0; i < I.ntile; ++i) {
+        const int g2 = gt + i;
+        if ((g2 & 1) != egroup) continue;
+        const uint32_t aph = (g2 >> 1) & 1;
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->tfull[egroup], aph, p.budget, abort_v));
+        if (!ok) {
+          if (lane == 0) fail();
+        } else {
+          tc_fence_after();
+          const int key = (I.tile_lo + i) * kTileKeys + row;
+          if constexpr (HI >= 16) {
+            for (int jj = 0; jj < p.G; ++jj) {
+              // all of the query's head columns in flight at once, one wait
+              uint32_t rr[HI / 16][16];
 #pragma unroll
-          for (int hc = 0; hc < HI / 16; ++hc) tmem_ld16(col0 + jj * HI + hc * 16, r[hc]);
-          tmem_ld_wait();
-          float sum = 0.f;
+              for (int hc = 0; hc < HI / 16; ++hc) tmem_ld16(col0 + jj * HI + hc * 16, rr[hc]);
+              tmem_ld_wait();
+              const float* wq = wi + jj * HI;
+              float sum = 0.f;
 #pragma unroll
-          for (int hc = 0; hc < HI / 16; ++hc)
+              for (int hc = 0; hc < HI / 16; ++hc)
 #pragma unroll
-            for (int e = 0; e < 16; ++e) sum = fmaf(w_s[hc * 16 + e], fmaxf(__uint_as_float(r[hc][e]), 0.f), sum);
-          const bool vis = key < nvis_s[jj];
-          if (vis) p.S[(static_cast<long long>(b) * p.Tq + j0 + jj) * p.ld + key] = sum;
-          if (p.hist) {
-            // bucket = top 12 bits of the order-preserving key of sum (sum >= 0 unless w < 0)
-            uint32_t u = __float_as_uint(sum);
-            u = u == 0x80000000u ? 0u : u;
-            u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-            const unsigned am = __ballot_sync(0xffffffffu, vis);
-            if (vis) {
-              const unsigned peers = __match_any_sync(am, u >> 20);
-              if (lane == __ffs(peers) - 1) atomicAdd(&hist_s[u >> 20], static_cast<uint32_t>(__popc(peers)));
+                for (int e = 0; e < 16; ++e) sum = fmaf(wq[hc * 16 + e], fmaxf(__uint_as_float(rr[hc][e]), 0.f), sum);
+              const bool vis = key < nvi[jj];
+              if (vis) p.S[(srow0 + jj) * p.ld + key] = sum;
+              if (p.hist) {
+                // bucket = top 12 bits of the order-preserving key of sum
+                uint32_t u = __float_as_uint(sum);
+                u = u == 0x80000000u ? 0u : u;
+                u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+                const unsigned am = __ballot_sync(0xffffffffu, vis);
+                if (vis) {
+                  const unsigned peers = __match_any_sync(am, u >> 20);
+                  if (lane == __ffs(peers) - 1) atomicAdd(&hist_s[u >> 20], static_cast<uint32_t>(__popc(peers)));
+                }
+              }
+            }
+          } else {
+            constexpr int QPC = 16 / HI;  // queries per 16-column chunk
+            for (int c0 = 0; c0 < p.NC; c0 += 16) {
+              uint32_t rr[16];
+              tmem_ld16(col0 + c0, rr);
+              tmem_ld_wait();
+#pragma unroll
+              for (int qq = 0; qq < QPC; ++qq) {
+                const int jj = c0 / HI + qq;
+                const float* wq = wi + (jj < p.G ? jj : 0) * HI;
+                float sum = 0.f;
+#pragma unroll
+                for (int e = 0; e < HI; ++e) sum = fmaf(wq[e], fmaxf(__uint_as_float(rr[qq * HI + e]), 0.f), sum);
+                if (jj < p.G && key < nvi[jj]) p.S[(srow0 + jj) * p.ld + key] = sum;
+              }
             }
           }
         }
-      } else {
-        constexpr int QPC = 16 / HI;  // queries per 16-column chunk
-        for (int c0 = 0; c0 < p.NC; c0 += 16) {
-          uint32_t r[16];
-          tmem_ld16(col0 + c0, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int qq = 0; qq < QPC; ++qq) {
-            const int jj = c0 / HI + qq;
-            float sum = 0.f;
-#pragma unroll
-            for (int e = 0; e < HI; ++e) sum = fmaf(w_s[e], fmaxf(__uint_as_float(r[qq * HI + e]), 0.f), sum);
-            if (jj < p.G && key < nvis_s[jj])
-              p.S[(static_cast<long long>(b) * p.Tq + j0 + jj) * p.ld + key] = sum;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->tempty[egroup]);
+      }
+      gt += I.ntile;
+      // this group is done with the item's weights and visibility
+      group_bar(egroup);
+      if ((ew & 3) == 0 && lane == 0) mbar_arrive(&bars->wfree[ib]);
+      if (p.hist) {
+        // both groups' counts of the item are in: flush them (once the
+        // histogram has been zeroed), then clear for the next item
+        epi_bar();
+        if (p.after_zero && !waited_zero) {
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          waited_zero = true;
+        }
+        uint32_t* g = p.hist + srow0 * kTopkBins;
+        for (int i = ew * 32 + lane; i < kTopkBins; i += 32 * 4 * kEpiGroups) {
+          const uint32_t v = hist_s[i];
+          if (v) {
+            atomicAdd(g + i, v);
+            hist_s[i] = 0u;
           }
         }
+        epi_bar();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+      ++it;
     }
   }
 
@@ -287,18 +456,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tbase, p.tmem_cols);
   }
-  if (p.after_zero) asm volatile("griddepcontrol.wait;" ::: "memory");  // the histogram is zeroed
-  if (p.hist) {
-    uint32_t* g = p.hist + (static_cast<long long>(b) * p.Tq + j0) * kTopkBins;
-    for (int i = tid; i < kTopkBins; i += kThreads)
-      if (hist_s[i]) atomicAdd(g + i, hist_s[i]);
-  }
 }
 
 template <int HI>
 cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   KParams p;
   p.w = a.w;
+  p.w_stride = a.w_stride;
   p.q_pos = a.q_pos;
   p.S = a.scores;
   p.ld = a.ld;
@@ -315,25 +479,32 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   p.tmem_cols = cols;
   const int q_bytes = p.kh * p.NC * 128;
   const int stage_bytes = p.kh * kHalfBytes;
-  const int hist_bytes = (a.hist != nullptr && p.G == 1 && HI >= 16) ? kTopkBins * 4 : 0;
-  int stages = (kSmemBudget - 1024 - q_bytes - static_cast<int>(sizeof(Bars)) - hist_bytes) / stage_bytes;
+  const bool fill_hist = a.hist != nullptr && p.G == 1 && HI >= 16;
+  const int hist_bytes = fill_hist ? kTopkBins * 4 : 0;
+  const int dyn_limit = kSmemLimit - kStaticSmem;
+  int stages = (dyn_limit - 1024 - q_bytes - static_cast<int>(sizeof(Bars)) - hist_bytes) / stage_bytes;
   stages = stages > 8 ? 8 : stages;
   if (stages < 2) return cudaErrorNotSupported;
   p.stages = stages;
   const int n_tiles_all = (a.N + kTileKeys - 1) / kTileKeys;
   const long long groups = static_cast<long long>(a.B) * p.n_groups;
-  // one wave of one CTA per SM when the groups alone cannot fill the GPU
-  int ipg = static_cast<int>(148 / (groups > 0 ? groups : 1));
+  const int n_sm = sm_count();
+  // tile ranges per group: one item per SM when the groups alone cannot fill the GPU
+  int ipg = static_cast<int>(n_sm / (groups > 0 ? groups : 1));
   ipg = ipg < 1 ? 1 : (ipg > n_tiles_all ? n_tiles_all : ipg);
   p.tiles_per_item = (n_tiles_all + ipg - 1) / ipg;
   p.items_per_group = (n_tiles_all + p.tiles_per_item - 1) / p.tiles_per_item;
   p.errw = a.errw;
   p.budget = a.budget;
-  p.hist = (a.hist != nullptr && p.G == 1 && HI >= 16) ? a.hist : nullptr;
+  p.hist = fill_hist ? a.hist : nullptr;
   p.after_zero = p.hist != nullptr && a.after_zero;
+  p.q_base = a.q_idx;
+  p.q_row_bytes = a.d_I * 2;
   const long long items = groups * p.items_per_group;
   if (items == 0 || n_tiles_all == 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorNotSupported;
+  p.items = static_cast<int>(items);
+  const int grid = static_cast<int>(items < n_sm ? items : n_sm);
 
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
@@ -364,7 +535,7 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   const size_t smem = 1024 + q_bytes + static_cast<size_t>(stages) * stage_bytes + sizeof(Bars) + hist_bytes;
   cudaError_t e = ensure_dyn_smem<indexer_kernel<HI>>(static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_k(indexer_kernel<HI>, dim3(static_cast<unsigned>(items)), dim3(kThreads), smem, s, 1, tmk, tmq,
+  return launch_k(indexer_kernel<HI>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, s, 1, tmk, tmq,
                   p);
 }
 

@@ -27,11 +27,26 @@ struct CompressArgs {
 };
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s);
 
+// decode-time append: the blocks completed by the queries' positions, from
+// the raw window rows into the caches (bf16)
+struct AppendArgs {
+  const void* x[3];  // [B, T_raw, D[i]] raw window rows
+  const void* g[3];  // [B, T_raw, D[i]] their gate logits
+  void* out[3];      // [B, N, D[i]] caches
+  int D[3];
+  int n_streams;
+  const int32_t* raw_base;  // [B]
+  const int32_t* q_pos;     // [B, Tq]
+  int B, Tq, T_raw, N, m;
+  uint32_t* errw;
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+
 // ---- (2) indexer scores ----------------------------------------------------
 struct IndexerArgs {
   const void* q_idx;  // [B, Tq, H_I, d_I] bf16
   const void* k_idx;  // [B, N, d_I] bf16
-  const float* w;     // [H_I]
+  const float* w;     // [H_I] (w_stride == 0) or per query: w[(n * Tq + j) * w_stride + h]
   const int32_t* q_pos;
   float* scores;
   long long ld;
@@ -43,6 +58,7 @@ struct IndexerArgs {
   // kernel, which itself waited for every earlier kernel: the indexer then
   // streams at once and waits for the zeroing only before its histogram flush
   int after_zero;
+  long long w_stride;
 };
 // returns cudaErrorNotSupported for shapes outside the instantiated set
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s);

@@ -101,6 +101,26 @@ def compress(x: np.ndarray, g: np.ndarray, m: int) -> np.ndarray:
     return (P * X).sum(axis=1)
 
 
+def append_blocks(x_win: np.ndarray, g_win: np.ndarray, raw_base: int, positions: Sequence[int],
+                  m: int) -> Dict[int, np.ndarray]:
+    """Decode-time compression of one sequence: every m tokens become one
+    entry, so a query at position t with (t+1) mod m == 0 completes block
+    b = (t+1)/m - 1 (tokens t-m+1 .. t), which is compressed from the raw rows
+    the window buffer holds (row r = token raw_base + r) exactly as ``compress``
+    folds a block.  x_win, g_win [T_raw, D].  Returns {b: float64 [D]} for the
+    positions that complete a block (none for the others)."""
+    out = {}
+    for t in positions:
+        t = int(t)
+        if t < 0 or (t + 1) % m != 0:
+            continue
+        r0 = t - m + 1 - raw_base
+        if r0 < 0 or r0 + m > x_win.shape[0]:
+            raise IndexError("block rows outside the window buffer")
+        out[(t + 1) // m - 1] = compress(x_win[r0:r0 + m], g_win[r0:r0 + m], m)[0]
+    return out
+
+
 # --------------------------------------------------------------------------
 # (2) Lightning Indexer scores, (3) top-k
 # --------------------------------------------------------------------------
@@ -191,14 +211,23 @@ def csa_compress(x_bits, g_bits, m: int) -> np.ndarray:
     return np.stack([compress(x[b], g[b], m) for b in range(x.shape[0])])
 
 
+def csa_append(x_win_bits, g_win_bits, raw_base, q_pos, m: int) -> List[Dict[int, np.ndarray]]:
+    """[B, T_raw, D] bf16 bits -> per sequence {block: float64 [D]}."""
+    x = bf16_to_f64(x_win_bits)
+    g = bf16_to_f64(g_win_bits)
+    return [append_blocks(x[b], g[b], int(raw_base[b]), q_pos[b], m) for b in range(x.shape[0])]
+
+
 def csa_index_scores(q_idx_bits, k_idx_bits, w, q_pos, m: int) -> List[List[np.ndarray]]:
-    """Per (b, query) float64 score vectors over the visible prefix."""
+    """Per (b, query) float64 score vectors over the visible prefix.  ``w`` is
+    one [H_I] vector shared by every query, or [B, Tq, H_I]: each query's own
+    head weights (the DSA-style indexer produces them per token)."""
     qi = bf16_to_f64(q_idx_bits)
     ki = bf16_to_f64(k_idx_bits)
     w = np.asarray(w, dtype=np.float64)
     out = []
     for b in range(qi.shape[0]):
-        out.append([indexer_scores(qi[b, j], ki[b], w, int(q_pos[b][j]), m)
+        out.append([indexer_scores(qi[b, j], ki[b], w if w.ndim == 1 else w[b, j], int(q_pos[b][j]), m)
                     for j in range(qi.shape[1])])
     return out
 

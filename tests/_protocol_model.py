@@ -59,44 +59,102 @@ def named_barrier(bar: Bar, use: int):
 
 
 # ---------------------------------------------------------------------------
-# indexer_kernel: TMA producer -> stage ring -> MMA -> two TMEM accumulators ->
-# two epilogue groups of four warps alternating tiles (one item per CTA)
+# indexer_kernel (persistent): a CTA walks a list of items (query group x tile
+# range; ntile may be 0 = nothing visible, skipped by every role).  Key
+# producer -> stage ring -> MMA -> two TMEM accumulators -> two epilogue groups
+# of four warps alternating the CTA's tiles; an item producer fills the
+# double-buffered head weights (wfull / wfree) and the single query buffer
+# (qfull, refilled once the MMAs of the previous item are done: qfree); with
+# the histogram both groups meet at every item's end (two named barriers).
 
-def indexer(ntile: int, stages: int, seed: int) -> bool:
+def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "") -> bool:
+    """``plant`` names a wait to leave out ("qfree", "wfree"), for the tests
+    that show the hazard checks catch a missing wait."""
     full = [Bar(1) for _ in range(stages)]
     empty = [Bar(1) for _ in range(stages)]
     tfull, tempty = [Bar(1), Bar(1)], [Bar(4), Bar(4)]
-    qfull = Bar(1)
+    qfull, qfree = Bar(1), Bar(1)
+    wfull, wfree = [Bar(1), Bar(1)], [Bar(2), Bar(2)]
+    group_bar = [Bar(4), Bar(4)]
+    epi_bar = Bar(8)
+    live = [n for n in items if n > 0]
     loads = [0] * stages
+    q_item = [-1]                 # the item whose query rows the buffer holds
+    w_item = [-1, -1]             # the item whose weights each buffer holds
+    mma_items_done = [0]          # items whose MMAs have completed
+    epi_done = [[0, 0], [0, 0]]   # [buffer][group]: items of that buffer parity finished by the group
 
-    def producer():
-        qfull.arrive()
-        for i in range(ntile):
-            s, ph = i % stages, (i // stages) & 1
-            yield (empty[s], ph ^ 1)
-            assert empty[s].done >= i // stages, "stage refilled before its MMAs read it"
-            loads[s] += 1
-            full[s].arrive()
+    def key_producer():
+        gt = 0
+        for n in items:
+            for _ in range(max(n, 0)):
+                s, ph = gt % stages, (gt // stages) & 1
+                yield (empty[s], ph ^ 1)
+                assert empty[s].done >= gt // stages, "stage refilled before its MMAs read it"
+                loads[s] += 1
+                full[s].arrive()
+                gt += 1
+
+    def item_producer():
+        for it in range(len(live)):
+            ib = it & 1
+            if it >= 2 and plant != "wfree":
+                yield (wfree[ib], ((it - 2) >> 1) & 1)
+                assert min(epi_done[ib]) >= (it - 2) // 2 + 1, "weights refilled while a group still reads them"
+            w_item[ib] = it
+            yield None
+            wfull[ib].arrive()
+            if it >= 1 and plant != "qfree":
+                yield (qfree, (it - 1) & 1)
+                assert mma_items_done[0] >= it, "query rows refilled before the previous item's MMAs ended"
+            q_item[0] = it
+            yield None
+            qfull.arrive()
 
     def mma():
-        yield (qfull, 0)
-        for i in range(ntile):
-            s, ph = i % stages, (i // stages) & 1
-            acc, aph = i & 1, (i >> 1) & 1
-            yield (tempty[acc], aph ^ 1)
-            yield (full[s], ph)
-            assert loads[s] == i // stages + 1, "MMA read a stage that holds another tile"
-            assert tempty[acc].done >= i >> 1, "accumulator overwritten before the epilogue read it"
-            empty[s].arrive()
-            tfull[acc].arrive()
+        gt = 0
+        for it, n in enumerate(live):
+            yield (qfull, it & 1)
+            for _ in range(n):
+                s, ph = gt % stages, (gt // stages) & 1
+                acc, aph = gt & 1, (gt >> 1) & 1
+                yield (tempty[acc], aph ^ 1)
+                yield (full[s], ph)
+                assert loads[s] == gt // stages + 1, "MMA read a stage that holds another tile"
+                assert tempty[acc].done >= gt >> 1, "accumulator overwritten before the epilogue read it"
+                assert q_item[0] == it, "MMA read another item's query rows"
+                empty[s].arrive()
+                tfull[acc].arrive()
+                gt += 1
+            mma_items_done[0] += 1    # the commit completes once these MMAs are done
+            qfree.arrive()
 
-    def epilogue(group: int):
-        for i in range(group, ntile, 2):
-            acc, aph = i & 1, (i >> 1) & 1
-            yield (tfull[acc], aph)
-            tempty[acc].arrive()
+    def epilogue(group: int, first: bool):
+        gt = 0
+        uses = 0
+        for it, n in enumerate(live):
+            ib = it & 1
+            yield (wfull[ib], (it >> 1) & 1)
+            assert w_item[ib] == it, "epilogue read another item's weights"
+            for i in range(n):
+                g2 = gt + i
+                if (g2 & 1) != group:
+                    continue
+                yield (tfull[group], (g2 >> 1) & 1)
+                tempty[group].arrive()
+            gt += n
+            yield from named_barrier(group_bar[group], it)
+            if first:
+                epi_done[ib][group] += 1
+                wfree[ib].arrive()
+            if hist:
+                yield from named_barrier(epi_bar, uses)
+                yield from named_barrier(epi_bar, uses + 1)
+                uses += 2
 
-    return run([producer(), mma()] + [epilogue(g) for g in (0, 1) for _ in range(4)], seed)
+    roles = [key_producer(), item_producer(), mma()]
+    roles += [epilogue(g, w == 0) for g in (0, 1) for w in range(4)]
+    return run(roles, seed)
 
 
 # ---------------------------------------------------------------------------

@@ -119,18 +119,23 @@ def test_validation_before_any_launch(L):
     assert L.csa_compress(1, ok, ok, ok, D, 1, 256, 4, 7, None) == _lib.CSA_ERR_INVALID
     assert L.csa_compress(1, ok, ok, ok, D, 1, 256, 0, 0, None) == _lib.CSA_ERR_INVALID
     # indexer: unsupported head count / width, bad leading dimension, workspace
-    args = [A16, A16, A16, A16, 1, 4, 64, 64, 128, 4, A16, 64, A16, 256, None]
-    a = list(args); a[7] = 48
+    args = [A16, A16, A16, 0, A16, 1, 4, 64, 64, 128, 4, A16, 64, A16, 256, None]
+    a = list(args); a[8] = 48
     assert L.csa_index_scores(*a) == _lib.CSA_ERR_UNSUPPORTED
-    a = list(args); a[8] = 96
+    a = list(args); a[9] = 96
     assert L.csa_index_scores(*a) == _lib.CSA_ERR_UNSUPPORTED
-    a = list(args); a[11] = 62
+    a = list(args); a[12] = 62
     assert L.csa_index_scores(*a) == _lib.CSA_ERR_INVALID
-    a = list(args); a[13] = 100
+    a = list(args); a[14] = 100
     assert L.csa_index_scores(*a) == _lib.CSA_ERR_WORKSPACE
-    a = list(args); a[12] = A16 + 16
+    a = list(args); a[13] = A16 + 16
     assert L.csa_index_scores(*a) == _lib.CSA_ERR_WORKSPACE
     a = list(args); a[0] = None
+    assert L.csa_index_scores(*a) == _lib.CSA_ERR_INVALID
+    # per-query weights: the stride must cover the H_I heads
+    a = list(args); a[3] = 32
+    assert L.csa_index_scores(*a) == _lib.CSA_ERR_INVALID
+    a = list(args); a[3] = -64
     assert L.csa_index_scores(*a) == _lib.CSA_ERR_INVALID
     # top-k: k range, too many entries
     targs = [A16, 64, A16, 1, 1, 64, 4, 16, A16, None, A16, 256, None]

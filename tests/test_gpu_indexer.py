@@ -12,21 +12,25 @@ from tests._parity import assert_scores_close, bits, check_topk_near_tie, index_
 pytestmark = pytest.mark.gpu
 
 
-def _inputs(seed, B, Tq, N, H_I, d_I, device):
+def _inputs(seed, B, Tq, N, H_I, d_I, device, per_query_w=False):
     q = S.normal_bf16(seed, 2, (B, Tq, H_I, d_I), device)
     k = S.normal_bf16(seed, 12, (B, N, d_I), device)
-    w = S.uniform_f32(seed, 9, (H_I,), device)
+    if per_query_w:
+        # each query's own head weights, of either sign, U(-1, 1)
+        w = S.uniform_f32(seed, 9, (B, Tq, H_I), device) * 2 - 1
+    else:
+        w = S.uniform_f32(seed, 9, (H_I,), device)
     return q, k, w
 
 
-def _case(seed, B, Tq, N, H_I, d_I, m, k, q_pos, check_rows=None):
+def _case(seed, B, Tq, N, H_I, d_I, m, k, q_pos, check_rows=None, per_query_w=False):
     import long_context_sparse_23_b300 as csa
-    qg, kg, wg = _inputs(seed, B, Tq, N, H_I, d_I, "cuda")
+    qg, kg, wg = _inputs(seed, B, Tq, N, H_I, d_I, "cuda", per_query_w)
     qp = torch.from_numpy(np.asarray(q_pos, np.int32)).cuda()
     scores = csa.csa_index_scores(qg, kg, wg, qp, m)
     idx = csa.csa_index_topk(qg, kg, wg, qp, m, k)
     torch.cuda.synchronize()
-    qc, kc, wc = _inputs(seed, B, Tq, N, H_I, d_I, "cpu")
+    qc, kc, wc = _inputs(seed, B, Tq, N, H_I, d_I, "cpu", per_query_w)
     q64, k64, w64 = O.bf16_to_f64(bits(qc)), O.bf16_to_f64(bits(kc)), wc.double().numpy()
     sc = scores.cpu().numpy()
     ix = idx.cpu().numpy()
@@ -34,9 +38,10 @@ def _case(seed, B, Tq, N, H_I, d_I, m, k, q_pos, check_rows=None):
     rows = check_rows if check_rows is not None else [(b, j) for b in range(B) for j in range(Tq)]
     for b, j in rows:
         t = int(q_pos[b][j])
-        ref = O.indexer_scores(q64[b, j], k64[b], w64, t, m)
+        wq = w64 if w64.ndim == 1 else w64[b, j]
+        ref = O.indexer_scores(q64[b, j], k64[b], wq, t, m)
         n = ref.shape[0]
-        assert_scores_close(sc[b, j, :n], ref, index_scale(q64[b, j], k64[b, :n], w64), f"b={b} j={j}")
+        assert_scores_close(sc[b, j, :n], ref, index_scale(q64[b, j], k64[b, :n], wq), f"b={b} j={j}")
         swaps += check_topk_near_tie(ix[b, j], O.topk(ref, k), ref, k, f"b={b} j={j}")
     return swaps
 
@@ -71,3 +76,16 @@ def test_indexer_prefill_8k_sampled():
     rng = np.random.default_rng(1)
     rows = [(0, int(j)) for j in np.concatenate([np.arange(12), rng.integers(0, 8192, 136), np.arange(8180, 8192)])]
     _case(1, 1, 8192, 2048, 64, 128, 4, 1024, np.arange(8192)[None], check_rows=rows)
+
+
+@pytest.mark.parametrize("B,Tq,N,H_I,d_I,m,k,pos", [
+    (1, 256, 64, 4, 32, 4, 16, np.arange(256)[None]),                     # 64 queries per group
+    (2, 7, 1001, 64, 128, 4, 64, np.array([[3, 100, 1999, 2000, 4003, 4010, 5000]] * 2)),
+    (4, 1, 32768, 64, 128, 4, 1024, np.full((4, 1), 131071)),            # decode, histogram fused
+    (2, 4, 262144, 64, 128, 4, 1024, np.array([list(range((1 << 20) - 4, 1 << 20))] * 2)),
+])
+def test_indexer_per_query_weights(B, Tq, N, H_I, d_I, m, k, pos):
+    """Per-query head weights [B, Tq, H_I] of either sign (negative scores
+    included): scores against the oracle element by element, indices by the
+    near-tie rule."""
+    _case(7, B, Tq, N, H_I, d_I, m, k, pos, per_query_w=True)

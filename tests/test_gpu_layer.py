@@ -164,3 +164,26 @@ def test_layer_decode_tail_ties_and_short_visibility():
     np.testing.assert_array_equal(gi[2, 0], np.concatenate([np.arange(500), -np.ones(k - 500, np.int32)]))
     cpu = {key: v.cpu() for key, v in g.items()}
     _decode_check(wl, cpu, idx, out, [(0, 0), (1, 0), (2, 0)])
+
+
+def test_layer_decode_per_query_weights():
+    """csa_layer with per-query indexer weights at 1M context (the fused
+    top-k + attention kernel): the indices equal csa_index_topk's with the
+    same weights, and the output matches the oracle on those indices."""
+    import long_context_sparse_23_b300 as csa
+    wl = S.WORKLOADS["decode_1m"].replace(B=2)
+    inp = S.make_inputs(wl, "cuda")
+    w = S.uniform_f32(9, S.TID["w"], (wl.B, 1, wl.H_I), "cuda") * 2 - 1
+    inp["w"] = w
+    idx, out = _decode_layer(inp, wl, out_dtype=torch.float32)
+    idx_s = csa.csa_index_topk(inp["q_idx"], inp["i_cmp"], w, inp["q_pos"], wl.m, wl.k)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx_s)
+    c = {k: (bits(v) if v.dtype == torch.bfloat16 else v.cpu().numpy()) for k, v in inp.items()}
+    t = wl.q_positions[0]
+    for b in range(wl.B):
+        win = O.window_rows(t, wl.W, wl.raw_base, wl.raw_len)
+        o, _ = O.attend_one(O.bf16_to_f64(c["q"][b, 0]), O.bf16_to_f64(c["k_cmp"][b]), O.bf16_to_f64(c["v_cmp"][b]),
+                            idx[b, 0].cpu().numpy(), O.bf16_to_f64(c["k_raw"][b]), O.bf16_to_f64(c["v_raw"][b]), win,
+                            1 / math.sqrt(wl.d))
+        assert_attention_close(out[b, 0].cpu().numpy(), o, f"b={b}")

@@ -346,3 +346,81 @@ def test_batched_wrappers_equal_each_sequence_alone():
     assert not np.array_equal(Oh2[1], Oh[1])
     np.testing.assert_array_equal(Oh2[0], Oh[0])
     np.testing.assert_array_equal(Oh2[2], Oh[2])
+
+
+# ---------------------------------------------------------------- decode-time append
+
+def test_append_golden_m2(golden_dir):
+    """A window whose last two tokens complete a block reproduces the
+    hand-worked m = 2 values; a position that completes no block appends
+    nothing."""
+    for ln in _load(golden_dir, "compress_m2.txt"):
+        p = ln.split("|")
+        x = np.array([[float(v) for v in p[0].split()], [float(v) for v in p[1].split()]])
+        g = np.array([[float(v) for v in p[2].split()], [float(v) for v in p[3].split()]])
+        want = np.array([float(v) for v in p[4].split()])
+        # window rows hold tokens 10, 11 (raw_base 10); t = 11 completes block 5
+        got = O.append_blocks(x, g, 10, [11], 2)
+        assert list(got) == [5]
+        np.testing.assert_allclose(got[5], want, rtol=0, atol=1e-14)
+        assert O.append_blocks(x, g, 10, [10], 2) == {}
+
+
+def test_append_equals_prefill_compression_of_the_same_block():
+    """Every block a decode step completes equals the entry that compressing
+    the whole stream gives for it (the prefill path), for windows at several
+    offsets and a step with several queries."""
+    rng = np.random.default_rng(5)
+    T, D, m, T_raw = 96, 8, 4, 20
+    x, g = rng.standard_normal((T, D)), rng.standard_normal((T, D)) * 2
+    full = O.compress(x, g, m)
+    for t_last in (19, 43, 44, 63, 95):
+        raw_base = t_last + 1 - T_raw
+        pos = [t_last - 5, t_last - 2, t_last]      # a step of three queries
+        got = O.append_blocks(x[raw_base:t_last + 1], g[raw_base:t_last + 1], raw_base, pos, m)
+        assert sorted(got) == sorted((t + 1) // m - 1 for t in pos if (t + 1) % m == 0)
+        for b, v in got.items():
+            np.testing.assert_array_equal(v, full[b])
+
+
+# ---------------------------------------------------------------- per-query indexer weights
+
+def test_per_query_weights():
+    """[B, Tq, H_I] weights: a query whose weights equal the shared vector
+    scores as with the shared vector; a one-hot weight vector scores
+    ReLU(q_h . k) of that head alone (closed form); weights of mixed sign give
+    sum_h w_h ReLU(.) with negative scores allowed, and top-k still keeps the
+    largest (ties to the lower index, checked by brute force)."""
+    rng = np.random.default_rng(21)
+    B, Tq, HI, dI, N, m = 2, 3, 4, 8, 40, 4
+    qi = O.round_bf16(rng.standard_normal((B, Tq, HI, dI)))
+    ki = O.round_bf16(rng.standard_normal((B, N, dI)))
+    q_pos = np.array([[159, 100, 57], [159, 120, 3]])
+    w_shared = rng.uniform(0, 1, HI)
+    w_q = np.broadcast_to(w_shared, (B, Tq, HI)).copy()
+    S_shared = O.csa_index_scores(qi, ki, w_shared, q_pos, m)
+    S_q = O.csa_index_scores(qi, ki, w_q, q_pos, m)
+    for b in range(B):
+        for j in range(Tq):
+            np.testing.assert_array_equal(S_q[b][j], S_shared[b][j])
+    # one-hot per query: head j % HI of query j
+    w_oh = np.zeros((B, Tq, HI))
+    for j in range(Tq):
+        w_oh[:, j, j % HI] = 1.0
+    S_oh = O.csa_index_scores(qi, ki, w_oh, q_pos, m)
+    q64, k64 = O.bf16_to_f64(qi), O.bf16_to_f64(ki)
+    for b in range(B):
+        for j in range(Tq):
+            n = O.n_visible(int(q_pos[b, j]), m, N)
+            want = [max(0.0, sum(q64[b, j, j % HI, c] * k64[b, i, c] for c in range(dI))) for i in range(n)]
+            np.testing.assert_allclose(S_oh[b][j], want, rtol=1e-12, atol=1e-12)
+    # mixed signs: some scores negative; top-k by brute force over the key order
+    w_mix = rng.uniform(-1, 1, (B, Tq, HI))
+    S_mix = O.csa_index_scores(qi, ki, w_mix, q_pos, m)
+    assert min(v.min() for row in S_mix for v in row if v.size) < 0
+    for row in S_mix:
+        for v in row:
+            k = 5
+            order = sorted(range(len(v)), key=lambda i: (-v[i], i))[:k]
+            got = O.topk(v, k)
+            assert list(got[got >= 0]) == sorted(order)

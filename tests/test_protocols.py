@@ -12,11 +12,25 @@ from tests import _protocol_model as M
 
 
 def test_indexer_protocol_completes_without_hazards():
+    """The persistent indexer: random item lists (empty items included),
+    stage counts and interleavings, with and without the per-item histogram
+    flush."""
     rng = random.Random(0)
-    for trial in range(200):
-        ntile = rng.choice([0, 1, 2, 3, 4, 5, 8, 13, 17])
-        stages = rng.choice([2, 3, 5, 8])
-        assert M.indexer(ntile, stages, trial), (ntile, stages)
+    for trial in range(400):
+        items = [rng.choice([0, 1, 2, 3, 4, 5, 8, 13, 17]) for _ in range(rng.randint(1, 6))]
+        stages = rng.choice([2, 3, 4, 5, 8])
+        hist = rng.random() < 0.5
+        assert M.indexer(items, stages, trial, hist), (items, stages, hist)
+
+
+@pytest.mark.parametrize("plant", ["qfree", "wfree"])
+def test_indexer_missing_item_waits_are_caught(plant):
+    """Without the wait for the previous item's MMAs (query rows) or for both
+    epilogue groups (head weights), some interleaving refills a buffer that is
+    still read, and the model's hazard check fires."""
+    with pytest.raises(AssertionError):
+        for t in range(300):
+            M.indexer([3, 2, 4, 1, 5], 3, t, plant=plant)
 
 
 def test_attend_tc_protocol_completes_without_hazards():
