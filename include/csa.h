@@ -148,6 +148,37 @@ csa_status csa_index_scores(const void* q_idx, const void* k_idx, const float* w
                             void* ws, size_t ws_bytes, void* stream);
 
 /* --------------------------------------------------------------------------
+ * (2') FP8 indexer.  "DeepSeek V4 technical review", section 5, and
+ * dataforcee "Muon Optimizer and FP4 QAT": the indexer's QK product runs in
+ * low precision.  Rows (one compressed indexer key, or one indexer query
+ * head) are stored as OCP FP8 E4M3 codes with one power-of-two scale per row:
+ * scale = 2^e, e the smallest integer with max|row| <= 448 * 2^e (in
+ * [-126, 120]; an all-zero row gets 1), code = round-to-nearest-even of
+ * row / scale.  The division is exact, so the code rounding is the only
+ * inexact step and the result is fixed bit for bit.
+ *
+ * csa_quantize_fp8: x [rows, D] bf16 -> codes [rows, D] (one byte each),
+ * scales [rows] fp32.  D in {32, 64, 128, 256}.
+ *
+ * csa_index_scores_fp8: the scores of (2) on the dequantised rows,
+ *     S[n, j, b] = sum_h w[n, j, h] * ReLU((qs_h q8_h) . (ks_b k8_b))
+ *                = ks_b * sum_h (w[n, j, h] qs_h) * ReLU(q8_h . k8_b),
+ * computed as E4M3 x E4M3 products on the tcgen05 tensor cores (kind::f8f6f4,
+ * fp32 accumulation) with the scales applied in the epilogue.
+ *   q8 [B, Tq, H_I, d_I] codes, q_scale [B * Tq * H_I] fp32,
+ *   k8 [B, N, d_I] codes, k_scale [B, N] fp32; the rest as csa_index_scores.
+ * d_I = 128; N % 4 == 0; H_I in {16, 32, 64, 128}.  Workspace:
+ * CSA_WS_HEADER_BYTES.  Keys take 128 + 4 bytes per entry instead of 256.
+ * ------------------------------------------------------------------------ */
+csa_status csa_quantize_fp8(const void* x, int64_t rows, int D, void* codes, float* scales,
+                            void* stream);
+csa_status csa_index_scores_fp8(const void* q8, const float* q_scale, const void* k8,
+                                const float* k_scale, const float* w, int64_t w_stride,
+                                const int32_t* q_pos, int B, int Tq, int N, int H_I, int d_I,
+                                int m, float* scores, int64_t ld_scores, void* ws,
+                                size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------------
  * (3) Top-k.  Technical review, section 2.1: keep the top-k compressed blocks
  * per query (k = 1024).  Among the n_vis visible scores of each query keep
  * the min(k, n_vis) largest; equal scores go to the lower block index.
@@ -291,6 +322,12 @@ typedef struct csa_layer_args {
     const void* i_win;             /* raw indexer keys of the window rows [B, T_raw, d_I] */
     const void *gk_win, *gv_win, *gi_win;  /* their gate logits [B, T_raw, d / d / d_I] */
     long long w_stride;            /* 0: w is [H_I]; >= H_I: w is per query, see (2) */
+    /* FP8 indexer keys (NULL: bf16): i_cmp holds E4M3 codes [B, N, d_I] made
+     * by csa_quantize_fp8 and i_scale [B, N] their row scales; the step's
+     * q_idx (bf16) is quantised the same way inside the call and step (2)
+     * runs as csa_index_scores_fp8.  Decode calls on given caches only (no
+     * step (1), no append); d_I = 128, N % 4 == 0, H_I in {16, 32, 64, 128}. */
+    const float* i_scale;
 } csa_layer_args;
 
 csa_status csa_layer_workspace(const csa_layer_args* a, size_t* bytes);

@@ -10,6 +10,7 @@ int32 for positions and indices, fp32 for the indexer weights.
     csa_index_scores (2) Lightning-Indexer scores
     csa_topk         (3) per-query top-k of given scores
     csa_index_topk   (2)+(3)
+    csa_quantize_fp8, csa_index_scores_fp8   (2') the indexer on E4M3 rows
     csa_attend       (4) attention over selected entries + sliding window
     hca_attend       dense HCA mode + sliding window
     csa_layer        (1)->(4) in one call
@@ -164,6 +165,34 @@ def csa_index_scores(q_idx: torch.Tensor, k_idx: torch.Tensor, w: torch.Tensor, 
     return scores
 
 
+def csa_quantize_fp8(x: torch.Tensor):
+    """Rows of x (bf16, last dimension D) -> (E4M3 codes as uint8, same shape;
+    fp32 power-of-two scale per row, shape x.shape[:-1])."""
+    D = x.shape[-1]
+    rows = x.numel() // D
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    check("csa_quantize_fp8", _lib.lib().csa_quantize_fp8(_ptr(x), rows, D, _ptr(codes), _ptr(scales), _stream()))
+    return codes, scales
+
+
+def csa_index_scores_fp8(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tensor, k_scale: torch.Tensor,
+                         w: torch.Tensor, q_pos: torch.Tensor, m: int, scores: Optional[torch.Tensor] = None,
+                         ws: Optional[Workspace] = None) -> torch.Tensor:
+    """(2) on E4M3 rows: q8 [B, Tq, H_I, d_I] / q_scale [B, Tq, H_I] and
+    k8 [B, N, d_I] / k_scale [B, N] as made by csa_quantize_fp8."""
+    B, Tq, H_I, d_I = q8.shape
+    N = k8.shape[1]
+    if scores is None:
+        scores = torch.full((B, Tq, scores_ld(N)), float("nan"), dtype=torch.float32, device=q8.device)
+    w_ = _ws(_lib.CSA_WS_HEADER_BYTES, ws)
+    st = _lib.lib().csa_index_scores_fp8(_ptr(q8), _ptr(q_scale), _ptr(k8), _ptr(k_scale), _ptr(w),
+                                         _w_stride(w, B, Tq, H_I), _ptr(q_pos), B, Tq, N, H_I, d_I, m,
+                                         _ptr(scores), scores.shape[-1], w_.ptr, w_.nbytes, _stream())
+    check("csa_index_scores_fp8", st)
+    return scores
+
+
 def csa_topk(scores: torch.Tensor, q_pos: torch.Tensor, N: int, m: int, k: int,
              with_scores: bool = False, ws: Optional[Workspace] = None):
     B, Tq, ld = scores.shape
@@ -238,7 +267,7 @@ def layer_args(*, B, Tq, N, m, H, d, H_I, d_I, k, W, T=0, T_raw=0, scale=0.0, x_
                g_k=None, g_v=None, g_i=None, k_cmp=None, v_cmp=None, i_cmp=None, k_win=None, v_win=None,
                raw_base=None, q=None, q_idx=None, w=None, q_pos=None, idx_out=None, out=None,
                out_dtype=torch.bfloat16, lse=None, i_win=None, gk_win=None, gv_win=None,
-               gi_win=None) -> csa_layer_args:
+               gi_win=None, i_scale=None) -> csa_layer_args:
     a = csa_layer_args()
     for name, v in dict(B=B, Tq=Tq, N=N, m=m, H=H, d=d, H_I=H_I, d_I=d_I, k=k, W=W, T=T, T_raw=T_raw).items():
         setattr(a, name, int(v))
@@ -246,7 +275,7 @@ def layer_args(*, B, Tq, N, m, H, d, H_I, d_I, k, W, T=0, T_raw=0, scale=0.0, x_
     for name, t in dict(x_k=x_k, x_v=x_v, x_i=x_i, g_k=g_k, g_v=g_v, g_i=g_i, k_cmp=k_cmp, v_cmp=v_cmp,
                         i_cmp=i_cmp, k_win=k_win, v_win=v_win, raw_base=raw_base, q=q, q_idx=q_idx, w=w,
                         q_pos=q_pos, idx_out=idx_out, out=out, lse=lse, i_win=i_win, gk_win=gk_win,
-                        gv_win=gv_win, gi_win=gi_win).items():
+                        gv_win=gv_win, gi_win=gi_win, i_scale=i_scale).items():
         setattr(a, name, _ptr(t))
     a.out_dtype = _odt(out_dtype)
     a.w_stride = 0 if w is None or w.dim() == 1 else int(w.shape[-1])

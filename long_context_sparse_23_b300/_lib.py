@@ -32,7 +32,7 @@ class csa_layer_args(ctypes.Structure):
         ("raw_base", c_vp), ("q", c_vp), ("q_idx", c_vp), ("w", c_vp), ("q_pos", c_vp),
         ("idx_out", c_vp), ("out", c_vp), ("out_dtype", c_int), ("lse", c_vp),
         ("i_win", c_vp), ("gk_win", c_vp), ("gv_win", c_vp), ("gi_win", c_vp),
-        ("w_stride", ctypes.c_longlong),
+        ("w_stride", ctypes.c_longlong), ("i_scale", c_vp),
     ]
 
 
@@ -49,6 +49,9 @@ SIGNATURES = {
                            c_vp]),
     "csa_index_scores": (c_int, [c_vp, c_vp, c_vp, ctypes.c_int64, c_vp, c_int, c_int, c_int, c_int, c_int,
                                  c_int, c_vp, ctypes.c_int64, c_vp, c_size, c_vp]),
+    "csa_quantize_fp8": (c_int, [c_vp, ctypes.c_int64, c_int, c_vp, c_vp, c_vp]),
+    "csa_index_scores_fp8": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.c_int64, c_vp, c_int, c_int, c_int, c_int,
+                                     c_int, c_int, c_vp, ctypes.c_int64, c_vp, c_size, c_vp]),
     "csa_topk": (c_int, [c_vp, ctypes.c_int64, c_vp, c_int, c_int, c_int, c_int, c_int, c_vp, c_vp,
                          c_vp, c_size, c_vp]),
     "csa_topk_workspace": (c_int, [c_int, c_int, c_int, c_int, c_sizep]),

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcsa.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["compress.cu", "indexer.cu", "topk.cu", "attend.cu", "decode_tail.cu", "attend_tc.cu", "csa_api.cu", "noalloc.cu"]
+SOURCES = ["compress.cu", "indexer.cu", "topk.cu", "attend.cu", "decode_tail.cu", "attend_tc.cu", "csa_api.cu", "noalloc.cu", "fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O3",
                 "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]

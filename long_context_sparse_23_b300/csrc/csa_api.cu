@@ -280,6 +280,31 @@ csa_status csa_index_scores(const void* q_idx, const void* k_idx, const float* w
   return cuda_status(launch_indexer_marked(a, static_cast<cudaStream_t>(stream)));
 }
 
+csa_status csa_quantize_fp8(const void* x, int64_t rows, int D, void* codes, float* scales, void* stream) {
+  if (!x || !codes || !scales || rows <= 0) return CSA_ERR_INVALID;
+  if (D != 32 && D != 64 && D != 128 && D != 256) return CSA_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(x) & 1u) || (reinterpret_cast<uintptr_t>(codes) & 1u) || !al4(scales))
+    return CSA_ERR_INVALID;
+  return cuda_status(csa::launch_quantize_fp8(x, rows, D, codes, scales, static_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_index_scores_fp8(const void* q8, const float* q_scale, const void* k8, const float* k_scale,
+                                const float* w, int64_t w_stride, const int32_t* q_pos, int B, int Tq, int N,
+                                int H_I, int d_I, int m, float* scores, int64_t ld_scores, void* ws,
+                                size_t ws_bytes, void* stream) {
+  csa_status st = check_index_args(q8, k8, w, q_pos, B, Tq, N, H_I, d_I, m);
+  if (st != CSA_OK) return st;
+  if (!q_scale || !k_scale || !al16(q_scale) || !al16(k_scale)) return CSA_ERR_INVALID;
+  if (!csa::indexer_fp8_supported(H_I, d_I, N)) return CSA_ERR_UNSUPPORTED;
+  if (w_stride != 0 && w_stride < H_I) return CSA_ERR_INVALID;
+  if (!scores || !al16(scores) || ld_scores < N || ld_scores % 4 != 0) return CSA_ERR_INVALID;
+  st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES);
+  if (st != CSA_OK) return st;
+  csa::IndexerArgs a{q8, k8, w, q_pos, scores, ld_scores, B, Tq, N, H_I, d_I, m,
+                     err_word(ws), g_wait_budget, nullptr, 0, w_stride, 1, q_scale, k_scale};
+  return cuda_status(launch_indexer_marked(a, static_cast<cudaStream_t>(stream)));
+}
+
 // ---------------------------------------------------------------- (3)
 csa_status csa_topk(const float* scores, int64_t ld_scores, const int32_t* q_pos, int B, int Tq,
                     int N, int m, int k, int32_t* idx_out, float* score_out, void* ws,
@@ -412,10 +437,19 @@ csa_status hca_attend(const void* q, const void* k_cmp, const void* v_cmp, const
 }
 
 // ---------------------------------------------------------------- layer
+// FP8 indexer: the step's indexer queries as E4M3 codes, then their scales
+static size_t fp8_query_codes_bytes(const csa_layer_args* a) {
+  return align_up(static_cast<size_t>(a->B) * a->Tq * a->H_I * a->d_I, kAlignWs);
+}
+static size_t fp8_query_bytes(const csa_layer_args* a) {
+  return fp8_query_codes_bytes(a) + align_up(static_cast<size_t>(a->B) * a->Tq * a->H_I * 4, kAlignWs);
+}
+
 csa_status csa_layer_workspace(const csa_layer_args* a, size_t* bytes) {
   if (!a || !bytes || a->B <= 0 || a->Tq <= 0 || a->N <= 0 || a->k <= 0) return CSA_ERR_INVALID;
   size_t total = CSA_WS_HEADER_BYTES + scores_bytes(a->B, a->Tq, a->N) + topk_bytes(a->B, a->Tq, a->N);
   if (!a->idx_out) total += align_up(static_cast<size_t>(a->B) * a->Tq * a->k * 4, kAlignWs);
+  if (a->i_scale) total += fp8_query_bytes(a);
   total += attn_part_bytes(true, a->B, a->Tq, a->N, a->k, a->W, a->H, a->d);
   *bytes = total;
   return CSA_OK;
@@ -429,6 +463,12 @@ static bool layer_appends(const csa_layer_args* a) {
 static csa_status layer_check(const csa_layer_args* a, const void* ws, size_t ws_bytes) {
   if (!a) return CSA_ERR_INVALID;
   const bool do_compress = a->g_k || a->g_v || a->g_i;
+  if (a->i_scale) {
+    // FP8 indexer keys: decode calls on given caches only
+    if (do_compress || layer_appends(a)) return CSA_ERR_UNSUPPORTED;
+    if (!al16(a->i_scale)) return CSA_ERR_INVALID;
+    if (!csa::indexer_fp8_supported(a->H_I, a->d_I, a->N)) return CSA_ERR_UNSUPPORTED;
+  }
   if (layer_appends(a)) {
     if (do_compress) return CSA_ERR_INVALID;  // a prefill compresses every block itself
     if (!a->i_win || !a->gk_win || !a->gv_win || !a->gi_win || !a->k_win || !a->v_win) return CSA_ERR_INVALID;
@@ -507,6 +547,13 @@ static csa_status layer_enqueue(const csa_layer_args* a, void* ws, cudaStream_t 
     idx = reinterpret_cast<int32_t*>(base);
     base += align_up(static_cast<size_t>(a->B) * a->Tq * a->k * 4, kAlignWs);
   }
+  void* q8 = nullptr;
+  float* q8_scale = nullptr;
+  if (a->i_scale) {
+    q8 = base;
+    q8_scale = reinterpret_cast<float*>(base + fp8_query_codes_bytes(a));
+    base += fp8_query_bytes(a);
+  }
   if (do_compress) {
     csa::CompressArgs c;
     std::memset(&c, 0, sizeof(c));
@@ -533,6 +580,16 @@ static csa_status layer_enqueue(const csa_layer_args* a, void* ws, cudaStream_t 
   const long long ld = scores_ld(a->N);
   csa::IndexerArgs ia{a->q_idx, a->i_cmp, a->w, a->q_pos, S, ld, a->B, a->Tq, a->N, a->H_I, a->d_I,
                       a->m, err_word(ws), g_wait_budget, nullptr, 0, a->w_stride};
+  if (a->i_scale) {
+    // this step's indexer queries to E4M3 codes (one scale per head row)
+    st = cuda_status(csa::launch_quantize_fp8(a->q_idx, static_cast<long long>(a->B) * a->Tq * a->H_I, a->d_I,
+                                              q8, q8_scale, s));
+    if (st != CSA_OK) return st;
+    ia.q_idx = q8;
+    ia.fp8 = 1;
+    ia.q_scale = q8_scale;
+    ia.k_scale = a->i_scale;
+  }
   csa::TopkArgs ta{S, ld, a->q_pos, a->B, a->Tq, a->N, a->m, a->k, idx, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   if (!do_compress && csa::tail_supported(a->Tq, a->N, a->k, a->W, a->H, a->d)) {
     // decode: indexer (+ bucket histogram), then one fused top-k + attention kernel

@@ -60,7 +60,8 @@ struct KParams {
   uint32_t* hist;  // [B*Tq][kTopkBins] (G == 1 only), or nullptr
   int after_zero;  // see IndexerArgs::after_zero
   const void* q_base;  // the indexer queries (for the L2 prefetch of the next item's rows)
-  int q_row_bytes;     // d_I * 2
+  int q_row_bytes;     // bytes of one query head's row
+  const float* q_scale;  // FP8: [B * Tq * HI] scale of each query head's codes
 };
 
 struct __align__(8) Bars {
@@ -72,6 +73,7 @@ struct __align__(8) Bars {
   uint64_t qfree;      // the item's MMAs done: the query buffer may be refilled
   uint64_t wfull[2];   // head weights / visibility of an item written
   uint64_t wfree[2];   // both epilogue groups are done with an item's weights
+  uint64_t sfree[8];   // FP8: the key scales of a stage read by the epilogue
 };
 
 // One work item: a group of G queries of sequence b against the key tiles
@@ -129,10 +131,13 @@ __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 3, 256;" ::: 
 //               once the previous item's MMAs are done; the next item's rows
 //               are prefetched into L2 meanwhile);
 //   warps 3-10  epilogue, two groups of four alternating tiles.
-template <int HI>
+// F8: keys and queries are E4M3 codes (one 128-byte row per key / query head,
+// one power-of-two scale per row); the MMAs are kind::f8f6f4 and the
+// epilogue applies the scales: sum_h (w_h s_q,h) ReLU(acc_h) * s_k.
+template <int HI, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
-                   KParams p) {
+                   const __grid_constant__ CUtensorMap tms, KParams p) {
   if (p.after_zero) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   } else {
@@ -143,7 +148,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   char* qs = smem;                                      // [kh][NC][128 B]
   char* ks = qs + p.kh * p.NC * 128;                    // [stages][kh][128][128 B]
-  Bars* bars = reinterpret_cast<Bars*>(ks + p.stages * p.kh * kHalfBytes);
+  // FP8: [stages][128] scales of the stage's keys
+  float* ksc = reinterpret_cast<float*>(ks + p.stages * p.kh * kHalfBytes);
+  Bars* bars = reinterpret_cast<Bars*>(reinterpret_cast<char*>(ksc) + (F8 ? p.stages * kTileKeys * 4 : 0));
   // top-k bucket histogram of the current item's scores (one query per group)
   uint32_t* hist_s = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(bars) + sizeof(Bars));
   __shared__ uint32_t tmem_base;
@@ -160,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
+      mbar_init(&bars->sfree[s], 4);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->tfull[i], 1);
@@ -199,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- key producer
     if (lane == 0) {
       tma_prefetch_desc(&tmk);
+      if (F8) tma_prefetch_desc(&tms);
       // the keys are read once per query group: evict-first, so the scores
       // this kernel writes stay in L2 for the top-k that reads them next
       const uint64_t key_policy = l2_policy_evict_first();
@@ -211,16 +220,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < I.ntile; ++i) {
           const int s = gt % p.stages;
           const uint32_t ph = (gt / p.stages) & 1;
-          if (!mbar_wait(&bars->empty[s], ph ^ 1, p.budget, abort_v)) {
+          if (!mbar_wait(&bars->empty[s], ph ^ 1, p.budget, abort_v) ||
+              (F8 && !mbar_wait(&bars->sfree[s], ph ^ 1, p.budget, abort_v))) {
             fail();
             ok = false;
             break;
           }
-          mbar_expect_tx(&bars->full[s], p.kh * kHalfBytes);
+          mbar_expect_tx(&bars->full[s], p.kh * kHalfBytes + (F8 ? kTileKeys * 4 : 0));
           char* dst = ks + s * p.kh * kHalfBytes;
           for (int h = 0; h < p.kh; ++h)
             tma_load_3d_hint(dst + h * kHalfBytes, &tmk, &bars->full[s], h * 64, (I.tile_lo + i) * kTileKeys, I.b,
                              key_policy);
+          if (F8) tma_load_2d(ksc + s * kTileKeys, &tms, &bars->full[s], (I.tile_lo + i) * kTileKeys, I.b);
           ++gt;
         }
       }
@@ -233,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, p.NC);
+      const uint32_t idesc = F8 ? idesc_e4m3_f32(128, p.NC) : idesc_bf16_f32(128, p.NC);
       int gt = 0, it = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
@@ -264,7 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int h = kk >> 2, w = kk & 3;
             const uint64_t ad = sdesc_kmajor_sw128(a0 + h * kHalfBytes + w * 32);
             const uint64_t bd = sdesc_kmajor_sw128(b0 + h * p.NC * 128 + w * 32);
-            umma_f16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            if constexpr (F8)
+              umma_f8(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            else
+              umma_f16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
           }
           umma_commit(&bars->empty[s]);
           umma_commit(&bars->tfull[acc]);
@@ -297,11 +311,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int i = lane; i < p.G * HI; i += 32) {
         const int jj = i / HI, h = i % HI;
-        w_s[ib][i] = p.w_stride == 0
-                         ? p.w[h]
-                         : (I.j0 + jj < p.Tq
-                                ? p.w[(static_cast<long long>(I.b) * p.Tq + I.j0 + jj) * p.w_stride + h]
-                                : 0.f);
+        const long long qrow = static_cast<long long>(I.b) * p.Tq + I.j0 + jj;
+        float wv = p.w_stride == 0 ? p.w[h] : (I.j0 + jj < p.Tq ? p.w[qrow * p.w_stride + h] : 0.f);
+        // FP8: the query head's scale (a power of two) folds into its weight
+        if (F8) wv = I.j0 + jj < p.Tq ? wv * p.q_scale[qrow * HI + h] : 0.f;
+        w_s[ib][i] = wv;
       }
       for (int jj = lane; jj < p.G; jj += 32) {
         int nv = 0;
@@ -368,7 +382,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g2 = gt + i;
         if ((g2 & 1) != egroup) continue;
         const uint32_t aph = (g2 >> 1) & 1;
+        const int st = g2 % p.stages;
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->tfull[egroup], aph, p.budget, abort_v));
+        // FP8: the key's scale, read before the stage's scale slot is released
+        // (the stage's load phase is complete, so this wait returns at once and
+        // makes the copy's writes visible to this thread)
+        float kscale = 1.f;
+        if (F8 && ok) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->full[st], (g2 / p.stages) & 1, p.budget, abort_v));
+          if (ok) kscale = ksc[st * kTileKeys + row];
+        }
+        if (F8) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->sfree[st]);
+        }
         if (!ok) {
           if (lane == 0) fail();
         } else {
@@ -387,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int hc = 0; hc < HI / 16; ++hc)
 #pragma unroll
                 for (int e = 0; e < 16; ++e) sum = fmaf(wq[hc * 16 + e], fmaxf(__uint_as_float(rr[hc][e]), 0.f), sum);
+              if (F8) sum *= kscale;
               const bool vis = key < nvi[jj];
               if (vis) p.S[(srow0 + jj) * p.ld + key] = sum;
               if (p.hist) {
@@ -458,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int HI>
+template <int HI, bool F8>
 cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   KParams p;
   p.w = a.w;
@@ -472,7 +500,7 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   p.m = a.m;
   p.G = a.Tq < 256 / HI ? a.Tq : 256 / HI;
   p.NC = ((p.G * HI + 15) / 16) * 16;
-  p.kh = (a.d_I + 63) / 64;
+  p.kh = F8 ? 1 : (a.d_I + 63) / 64;  // 128-byte rows: 64 bf16 or 128 E4M3 values
   p.n_groups = (a.Tq + p.G - 1) / p.G;
   int cols = 32;
   while (cols < 2 * p.NC) cols *= 2;
@@ -482,7 +510,8 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   const bool fill_hist = a.hist != nullptr && p.G == 1 && HI >= 16;
   const int hist_bytes = fill_hist ? kTopkBins * 4 : 0;
   const int dyn_limit = kSmemLimit - kStaticSmem;
-  int stages = (dyn_limit - 1024 - q_bytes - static_cast<int>(sizeof(Bars)) - hist_bytes) / stage_bytes;
+  int stages = (dyn_limit - 1024 - q_bytes - static_cast<int>(sizeof(Bars)) - hist_bytes) /
+               (stage_bytes + (F8 ? kTileKeys * 4 : 0));
   stages = stages > 8 ? 8 : stages;
   if (stages < 2) return cudaErrorNotSupported;
   p.stages = stages;
@@ -499,7 +528,8 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   p.hist = fill_hist ? a.hist : nullptr;
   p.after_zero = p.hist != nullptr && a.after_zero;
   p.q_base = a.q_idx;
-  p.q_row_bytes = a.d_I * 2;
+  p.q_row_bytes = a.d_I * (F8 ? 1 : 2);
+  p.q_scale = a.q_scale;
   const long long items = groups * p.items_per_group;
   if (items == 0 || n_tiles_all == 0) return cudaSuccess;
   if (items > 0x7fffffffLL) return cudaErrorNotSupported;
@@ -508,35 +538,50 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
 
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
-  CUtensorMap tmk, tmq;
+  const CUtensorMapDataType dt = F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int esz = F8 ? 1 : 2;
+  const cuuint32_t box_x = F8 ? 128 : 64;  // one 128-byte swizzle row
+  CUtensorMap tmk, tmq, tms;
   {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.d_I), static_cast<cuuint64_t>(a.N),
                           static_cast<cuuint64_t>(a.B)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.d_I) * 2,
-                             static_cast<cuuint64_t>(a.N) * a.d_I * 2};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTileKeys), 1};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.d_I) * esz,
+                             static_cast<cuuint64_t>(a.N) * a.d_I * esz};
+    cuuint32_t box[3] = {box_x, static_cast<cuuint32_t>(kTileKeys), 1};
     cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&tmk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.k_idx), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (enc(&tmk, dt, 3, const_cast<void*>(a.k_idx), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
   {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.d_I),
                           static_cast<cuuint64_t>(a.B) * a.Tq * HI};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.d_I) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(p.NC)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.d_I) * esz};
+    cuuint32_t box[2] = {box_x, static_cast<cuuint32_t>(p.NC)};
     cuuint32_t es[2] = {1, 1};
-    if (enc(&tmq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.q_idx), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (enc(&tmq, dt, 2, const_cast<void*>(a.q_idx), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const size_t smem = 1024 + q_bytes + static_cast<size_t>(stages) * stage_bytes + sizeof(Bars) + hist_bytes;
-  cudaError_t e = ensure_dyn_smem<indexer_kernel<HI>>(static_cast<int>(smem));
+  tms = tmq;  // bf16: the key-scale map is never read
+  if (F8) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.N), static_cast<cuuint64_t>(a.B)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.N) * 4};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileKeys), 1};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&tms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(a.k_scale), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const size_t smem = 1024 + q_bytes + static_cast<size_t>(stages) * (stage_bytes + (F8 ? kTileKeys * 4 : 0)) +
+                     sizeof(Bars) + hist_bytes;
+  cudaError_t e = ensure_dyn_smem<indexer_kernel<HI, F8>>(static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_k(indexer_kernel<HI>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, s, 1, tmk, tmq,
-                  p);
+  return launch_k(indexer_kernel<HI, F8>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, s, 1, tmk, tmq,
+                  tms, p);
 }
 
 }  // namespace
@@ -557,14 +602,27 @@ EncodeTiledFn encode_fn() {
 
 bool indexer_fills_hist(int Tq, int H_I) { return Tq == 1 && H_I >= 16; }
 
+bool indexer_fp8_supported(int H_I, int d_I, int N) {
+  return (H_I == 16 || H_I == 32 || H_I == 64 || H_I == 128) && d_I == 128 && N % 4 == 0;
+}
+
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s) {
+  if (a.fp8) {
+    if (!indexer_fp8_supported(a.H_I, a.d_I, a.N)) return cudaErrorNotSupported;
+    switch (a.H_I) {
+      case 16: return launch_hi<16, true>(a, s);
+      case 32: return launch_hi<32, true>(a, s);
+      case 64: return launch_hi<64, true>(a, s);
+      default: return launch_hi<128, true>(a, s);
+    }
+  }
   switch (a.H_I) {
-    case 4: return launch_hi<4>(a, s);
-    case 8: return launch_hi<8>(a, s);
-    case 16: return launch_hi<16>(a, s);
-    case 32: return launch_hi<32>(a, s);
-    case 64: return launch_hi<64>(a, s);
-    case 128: return launch_hi<128>(a, s);
+    case 4: return launch_hi<4, false>(a, s);
+    case 8: return launch_hi<8, false>(a, s);
+    case 16: return launch_hi<16, false>(a, s);
+    case 32: return launch_hi<32, false>(a, s);
+    case 64: return launch_hi<64, false>(a, s);
+    case 128: return launch_hi<128, false>(a, s);
     default: return cudaErrorNotSupported;
   }
 }

@@ -59,7 +59,16 @@ struct IndexerArgs {
   // streams at once and waits for the zeroing only before its histogram flush
   int after_zero;
   long long w_stride;
+  // FP8 indexer: q_idx and k_idx hold E4M3 codes ([B, Tq, H_I, d_I] and
+  // [B, N, d_I], one byte each), q_scale [B * Tq * H_I] and k_scale [B, N]
+  // the power-of-two scale of each row (d_I == 128, N % 4 == 0)
+  int fp8;
+  const float* q_scale;
+  const float* k_scale;
 };
+// rows [rows][D] bf16 -> E4M3 codes [rows][D] and one power-of-two scale per row
+cudaError_t launch_quantize_fp8(const void* x, long long rows, int D, void* codes, float* scales, cudaStream_t s);
+bool indexer_fp8_supported(int H_I, int d_I, int N);
 // returns cudaErrorNotSupported for shapes outside the instantiated set
 cudaError_t launch_indexer(const IndexerArgs& a, cudaStream_t s);
 // whether launch_indexer fills IndexerArgs::hist for this shape (else it is ignored)

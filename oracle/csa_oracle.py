@@ -147,6 +147,72 @@ def indexer_scores(q_idx: np.ndarray, k_idx: np.ndarray, w: np.ndarray,
     return np.maximum(dots, 0.0) @ w
 
 
+# --------------------------------------------------------------------------
+# (2') FP8 indexer: e4m3 codes, one power-of-two scale per row
+# --------------------------------------------------------------------------
+# "DeepSeek V4 technical review", section 5 (and "Muon Optimizer and FP4 QAT"
+# on dataforcee): the indexer's QK product runs in low precision.  Reading
+# taken here: keys and indexer queries are stored as OCP FP8 E4M3 codes (max
+# 448, round to nearest even) with one power-of-two scale per row (one
+# compressed entry, or one (query, head)); the scale 2^e is the smallest with
+# max|row| <= 448 * 2^e, so the division by it is exact and rounding to the
+# code is the only inexact step.  Scores are the float64 definition applied to
+# the dequantised rows.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_round(y) -> np.ndarray:
+    """float64 -> the nearest E4M3 value (ties to even), |y| <= 448.  Normal
+    values have 3 fraction bits (exponents -6 .. 8), below 2^-6 the step is
+    2^-9 (subnormals)."""
+    y = np.asarray(y, dtype=np.float64)
+    a = np.abs(y)
+    if np.any(a > E4M3_MAX):
+        raise ValueError("e4m3_round: value beyond 448")
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))      # a = f * 2^ex, 0.5 <= f < 1: leading bit 2^(ex-1)
+    q = np.maximum(ex - 4, -9)                      # quantum: 2^(ex-1-3), at least 2^-9
+    v = np.ldexp(np.round(np.ldexp(a, -q)), q)      # np.round: half to even
+    return np.copysign(v, y)
+
+
+def e4m3_code(v: np.ndarray, sign_of: np.ndarray) -> np.ndarray:
+    """Byte codes (sign, 4 exponent bits bias 7, 3 mantissa bits) of E4M3
+    values ``v``; the sign bit is taken from ``sign_of`` (so -0 is 0x80)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))
+    lead = ex - 1                                   # a = 1.mmm * 2^lead for normal values
+    normal = a >= 2.0 ** -6
+    e_field = np.where(normal, lead + 7, 0)
+    mant = np.where(normal, np.ldexp(a, -lead) * 8 - 8, np.ldexp(a, 9))
+    code = (e_field.astype(np.int64) << 3) | np.rint(mant).astype(np.int64)
+    return (code | np.where(np.signbit(sign_of), 0x80, 0)).astype(np.uint8)
+
+
+def quantize_e4m3_rows(x) -> tuple:
+    """Rows of x (float64 [R, D]) -> (values on the e4m3 grid [R, D], scales
+    [R], byte codes [R, D]); row r is scale[r] * values[r].  scale = 2^e with
+    e the smallest integer such that max|x_r| <= 448 * 2^e (e in [-126, 127];
+    an all-zero row gets scale 1)."""
+    x = np.asarray(x, dtype=np.float64)
+    amax = np.abs(x).max(axis=1)
+    _, ex = np.frexp(np.where(amax > 0, amax, 1.0))
+    e = (ex - 1) - 8
+    e = np.where(amax > np.ldexp(E4M3_MAX, e), e + 1, e)
+    e = np.clip(np.where(amax > 0, e, 0), -126, 127)
+    scale = np.ldexp(1.0, e)
+    v = e4m3_round(x / scale[:, None])
+    return v, scale, e4m3_code(v, x)
+
+
+def indexer_scores_fp8(qv: np.ndarray, q_scale: np.ndarray, kv: np.ndarray, k_scale: np.ndarray,
+                       w: np.ndarray, t: int, m: int) -> np.ndarray:
+    """indexer_scores on the dequantised rows: query head h is q_scale[h] *
+    qv[h], entry b is k_scale[b] * kv[b] (qv [H_I, d_I], kv [N, d_I] e4m3
+    values)."""
+    return indexer_scores(qv * q_scale[:, None], kv * k_scale[:, None], w, t, m)
+
+
 def topk(S: np.ndarray, k: int) -> np.ndarray:
     """Top-k over the visible scores S [n_vis].
 

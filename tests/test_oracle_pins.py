@@ -424,3 +424,73 @@ def test_per_query_weights():
             order = sorted(range(len(v)), key=lambda i: (-v[i], i))[:k]
             got = O.topk(v, k)
             assert list(got[got >= 0]) == sorted(order)
+
+
+# ---------------------------------------------------------------- FP8 (e4m3) indexer
+
+def test_e4m3_rounding_matches_torch():
+    """Round-to-nearest-even onto the E4M3 grid (normals, subnormals, exact
+    ties) and the byte codes, against torch's float8_e4m3fn conversion."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(200000) * np.exp2(rng.uniform(-12, 8.7, 200000))
+    x = np.clip(x, -448, 448).astype(np.float32).astype(np.float64)
+    grid = O.e4m3_round(np.arange(-448, 449, dtype=np.float64))             # all are integers or on the grid
+    ties = (grid[1:] + grid[:-1]) / 2                                       # midpoints: exact ties
+    sub = np.arange(0, 8) * 2.0 ** -9 + 2.0 ** -10                          # subnormal ties
+    x = np.concatenate([x, ties, -ties, sub, -sub, [0.0, -0.0, 448.0, -448.0, 2.0 ** -6, 2.0 ** -9]])
+    t = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn)
+    assert np.array_equal(x.astype(np.float32).astype(np.float64), x)       # every input is exact in fp32
+    np.testing.assert_array_equal(O.e4m3_round(x), t.float().numpy().astype(np.float64))
+    np.testing.assert_array_equal(O.e4m3_code(O.e4m3_round(x), x), t.view(torch.uint8).numpy())
+
+
+def test_e4m3_row_quantisation():
+    """Scale 2^e, the smallest with max|row| <= 448 * 2^e: the largest code
+    magnitude lies in [224, 448] (max|row| / 2^e in (224, 448] before the
+    rounding); dequantised values within half a step
+    (2^-4 relative for normal codes) of the input; an all-zero row keeps
+    scale 1 and zero codes; scales are exact powers of two."""
+    rng = np.random.default_rng(4)
+    x = O.bf16_to_f64(O.round_bf16(rng.standard_normal((300, 128)) * np.exp2(rng.uniform(-20, 20, (300, 1)))))
+    x[7] = 0.0
+    v, s, c = O.quantize_e4m3_rows(x)
+    nz = np.abs(x).max(axis=1) > 0
+    top = np.abs(v).max(axis=1)
+    assert np.all((top[nz] >= 224) & (top[nz] <= 448))
+    pre = np.abs(x).max(axis=1)[nz] / s[nz]
+    assert np.all((pre > 224) & (pre <= 448))
+    assert s[7] == 1.0 and not c[7].any() and not v[7].any()
+    assert np.all(np.frexp(s)[0] == 0.5)                                     # powers of two
+    normal = np.abs(v) >= 2.0 ** -6
+    rel = np.abs(v * s[:, None] - x)[normal] / np.abs(x)[normal]
+    assert rel.max() <= 2.0 ** -4 + 1e-15
+    # the codes decode to the values (torch's e4m3 decoding of the bytes)
+    dec = torch.from_numpy(c).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    np.testing.assert_array_equal(dec, v)
+
+
+def test_fp8_scores_reduce_to_the_definition():
+    """With rows already on the E4M3 grid the quantisation is exact (up to the
+    power-of-two scale), so the FP8 scores equal indexer_scores of the
+    original rows; in general they equal indexer_scores of the dequantised
+    rows (checked against a brute-force double loop)."""
+    rng = np.random.default_rng(6)
+    H, d, N, m, t = 3, 16, 24, 4, 95
+    qg = O.e4m3_round(np.clip(rng.standard_normal((H, d)) * 8, -448, 448))
+    kg = O.e4m3_round(np.clip(rng.standard_normal((N, d)) * 8, -448, 448))
+    w = rng.uniform(0, 1, H)
+    qv, qs, _ = O.quantize_e4m3_rows(qg)
+    kv, ks, _ = O.quantize_e4m3_rows(kg)
+    np.testing.assert_allclose(O.indexer_scores_fp8(qv, qs, kv, ks, w, t, m), O.indexer_scores(qg, kg, w, t, m),
+                               rtol=1e-14, atol=0)
+    q, k = rng.standard_normal((H, d)), rng.standard_normal((N, d))
+    qv, qs, _ = O.quantize_e4m3_rows(q)
+    kv, ks, _ = O.quantize_e4m3_rows(k)
+    got = O.indexer_scores_fp8(qv, qs, kv, ks, w, t, m)
+    n = O.n_visible(t, m, N)
+    for b in range(n):
+        want = 0.0
+        for h in range(H):
+            dot = sum((qs[h] * qv[h, c]) * (ks[b] * kv[b, c]) for c in range(d))
+            want += w[h] * max(dot, 0.0)
+        assert abs(got[b] - want) <= 1e-12 * (1 + abs(want))
