@@ -67,11 +67,15 @@ def named_barrier(bar: Bar, use: int):
 # (qfull, refilled once the MMAs of the previous item are done: qfree); with
 # the histogram both groups meet at every item's end (two named barriers).
 
-def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "") -> bool:
-    """``plant`` names a wait to leave out ("qfree", "wfree"), for the tests
-    that show the hazard checks catch a missing wait."""
+def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "", fp8: bool = False) -> bool:
+    """``plant`` names a wait to leave out ("qfree", "wfree", "sfree"), for the
+    tests that show the hazard checks catch a missing wait.  ``fp8``: the key
+    scales share the stage ring and a stage's scale slot is released by the
+    four warps of the epilogue group that read it (sfree)."""
     full = [Bar(1) for _ in range(stages)]
     empty = [Bar(1) for _ in range(stages)]
+    sfree = [Bar(4) for _ in range(stages)]
+    scale_tile = [-1] * stages    # the tile whose key scales each stage's slot holds
     tfull, tempty = [Bar(1), Bar(1)], [Bar(4), Bar(4)]
     qfull, qfree = Bar(1), Bar(1)
     wfull, wfree = [Bar(1), Bar(1)], [Bar(2), Bar(2)]
@@ -91,6 +95,11 @@ def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "") 
                 s, ph = gt % stages, (gt // stages) & 1
                 yield (empty[s], ph ^ 1)
                 assert empty[s].done >= gt // stages, "stage refilled before its MMAs read it"
+                if fp8 and plant != "sfree":
+                    yield (sfree[s], ph ^ 1)
+                if fp8:
+                    assert gt < stages or sfree[s].done >= gt // stages, "key scales refilled before the epilogue read them"
+                    scale_tile[s] = gt
                 loads[s] += 1
                 full[s].arrive()
                 gt += 1
@@ -141,6 +150,11 @@ def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "") 
                 if (g2 & 1) != group:
                     continue
                 yield (tfull[group], (g2 >> 1) & 1)
+                if fp8:
+                    st = g2 % stages
+                    yield (full[st], (g2 // stages) & 1)
+                    assert scale_tile[st] == g2, "epilogue read another tile's key scales"
+                    sfree[st].arrive()
                 tempty[group].arrive()
             gt += n
             yield from named_barrier(group_bar[group], it)

@@ -20,17 +20,18 @@ def test_indexer_protocol_completes_without_hazards():
         items = [rng.choice([0, 1, 2, 3, 4, 5, 8, 13, 17]) for _ in range(rng.randint(1, 6))]
         stages = rng.choice([2, 3, 4, 5, 8])
         hist = rng.random() < 0.5
-        assert M.indexer(items, stages, trial, hist), (items, stages, hist)
+        fp8 = rng.random() < 0.5
+        assert M.indexer(items, stages, trial, hist, fp8=fp8), (items, stages, hist, fp8)
 
 
-@pytest.mark.parametrize("plant", ["qfree", "wfree"])
+@pytest.mark.parametrize("plant", ["qfree", "wfree", "sfree"])
 def test_indexer_missing_item_waits_are_caught(plant):
     """Without the wait for the previous item's MMAs (query rows) or for both
     epilogue groups (head weights), some interleaving refills a buffer that is
     still read, and the model's hazard check fires."""
     with pytest.raises(AssertionError):
         for t in range(300):
-            M.indexer([3, 2, 4, 1, 5], 3, t, plant=plant)
+            M.indexer([3, 2, 4, 1, 5], 3, t, plant=plant, fp8=True)
 
 
 def test_attend_tc_protocol_completes_without_hazards():
