@@ -348,6 +348,35 @@ csa_status csa_layer(const csa_layer_args* a, void* ws, size_t ws_bytes, void* s
 csa_status csa_layer_host(const csa_layer_args* a, const void* q_host, const void* q_idx_host,
                           void* out_host, void* ws, size_t ws_bytes, void* stream);
 
+/* --------------------------------------------------------------------------
+ * The hybrid layer stack at decode time.  "DeepSeek V4 technical review",
+ * section 2.3: the first two layers attend over a sliding window only, the
+ * following layers alternate CSA and HCA.  The pages give no weights for
+ * this path, so the stack carries the activations from layer to layer
+ * unchanged (identity projections): layer i's output [B, Tq, H, d] is layer
+ * i + 1's query, and for a CSA layer also its indexer query (H_I * d_I must
+ * equal H * d; the same bytes read as [B, Tq, H_I, d_I]).  Each layer has
+ * its own caches and window buffer.
+ *   kind CSA_STACK_SWA: attention over the W newest raw tokens (k_win, v_win,
+ *        T_raw, raw_base, W, q_pos, scale of ``a``);
+ *   kind CSA_STACK_CSA: csa_layer on given caches (no step (1); ``a``'s q,
+ *        q_idx, out and lse are ignored; idx_out, if set, receives the
+ *        layer's kept indices);
+ *   kind CSA_STACK_HCA: hca_attend on the layer's entries (k_cmp, v_cmp, N,
+ *        m) and window.
+ * x is layer 0's input, y receives the last layer's output (out_dtype); the
+ * intermediate activations (bf16) live in the workspace.  Every layer has
+ * the same B, Tq, H, d.  All checks run before anything is enqueued.
+ * ------------------------------------------------------------------------ */
+enum { CSA_STACK_SWA = 0, CSA_STACK_CSA = 1, CSA_STACK_HCA = 2 };
+typedef struct csa_stack_layer {
+    int kind;
+    csa_layer_args a;
+} csa_stack_layer;
+csa_status csa_stack_workspace(const csa_stack_layer* layers, int n_layers, size_t* bytes);
+csa_status csa_stack_decode(const csa_stack_layer* layers, int n_layers, const void* x, void* y,
+                            int out_dtype, void* ws, size_t ws_bytes, void* stream);
+
 /* Test hook: the clock64 budget of every bounded device-side wait issued by
  * later calls in this process (default ~2^31 cycles, about one second).
  * cycles <= 0 restores the default. */

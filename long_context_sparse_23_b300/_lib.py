@@ -36,6 +36,13 @@ class csa_layer_args(ctypes.Structure):
     ]
 
 
+CSA_STACK_SWA, CSA_STACK_CSA, CSA_STACK_HCA = 0, 1, 2
+
+
+class csa_stack_layer(ctypes.Structure):
+    _fields_ = [("kind", c_int), ("a", csa_layer_args)]
+
+
 # name -> (restype, argtypes)
 SIGNATURES = {
     "csa_status_string": (ctypes.c_char_p, [c_int]),
@@ -69,6 +76,8 @@ SIGNATURES = {
     "csa_layer_workspace": (c_int, [ctypes.POINTER(csa_layer_args), c_sizep]),
     "csa_layer": (c_int, [ctypes.POINTER(csa_layer_args), c_vp, c_size, c_vp]),
     "csa_layer_host": (c_int, [ctypes.POINTER(csa_layer_args), c_vp, c_vp, c_vp, c_vp, c_size, c_vp]),
+    "csa_stack_workspace": (c_int, [ctypes.POINTER(csa_stack_layer), c_int, c_sizep]),
+    "csa_stack_decode": (c_int, [ctypes.POINTER(csa_stack_layer), c_int, c_vp, c_vp, c_int, c_vp, c_size, c_vp]),
     "csa_set_wait_budget": (None, [c_ll]),
     "csa_set_indexer_events": (None, [c_vp, c_vp]),
 }

@@ -705,4 +705,107 @@ csa_status csa_layer_host(const csa_layer_args* a, const void* q_host, const voi
   return cuda_status(cudaMemcpyAsync(out_host, a->out, out_bytes, cudaMemcpyDeviceToHost, s));
 }
 
+// ---------------------------------------------------------------- stack
+static size_t stack_act_bytes(const csa_stack_layer* l) {
+  return align_up(static_cast<size_t>(l->a.B) * l->a.Tq * l->a.H * l->a.d * 2, kAlignWs);
+}
+
+// Layer i's arguments with its input and output activations filled in.
+static csa_layer_args stack_args(const csa_stack_layer* l, const void* in, void* out, int out_dtype) {
+  csa_layer_args a = l->a;
+  a.q = in;
+  a.q_idx = in;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.lse = nullptr;
+  return a;
+}
+
+static size_t stack_layer_ws(const csa_stack_layer* l) {
+  size_t need = 0;
+  const csa_layer_args& a = l->a;
+  if (l->kind == CSA_STACK_CSA) {
+    csa_layer_workspace(&a, &need);
+  } else if (l->kind == CSA_STACK_HCA) {
+    hca_attend_workspace(a.B, a.Tq, a.N, a.H, a.d, a.W, &need);
+  } else {
+    csa_attend_workspace(a.B, a.Tq, a.H, a.d, 0, a.W, &need);
+  }
+  return need;
+}
+
+csa_status csa_stack_workspace(const csa_stack_layer* layers, int n_layers, size_t* bytes) {
+  if (!layers || n_layers <= 0 || !bytes) return CSA_ERR_INVALID;
+  size_t need = 0;
+  for (int i = 0; i < n_layers; ++i) {
+    const csa_layer_args& a = layers[i].a;
+    if (a.B <= 0 || a.Tq <= 0 || a.H <= 0 || a.d <= 0) return CSA_ERR_INVALID;
+    const size_t w = stack_layer_ws(&layers[i]);
+    need = need > w ? need : w;
+  }
+  // the layer workspace, then two activation buffers (ping-pong)
+  *bytes = align_up(need, kAlignWs) + 2 * stack_act_bytes(&layers[0]);
+  return CSA_OK;
+}
+
+csa_status csa_stack_decode(const csa_stack_layer* layers, int n_layers, const void* x, void* y, int out_dtype,
+                            void* ws, size_t ws_bytes, void* stream) {
+  size_t need = 0;
+  csa_status st = csa_stack_workspace(layers, n_layers, &need);
+  if (st != CSA_OK) return st;
+  if (!x || !y || !al16(x) || !al16(y)) return CSA_ERR_INVALID;
+  if (out_dtype != CSA_BF16 && out_dtype != CSA_F32) return CSA_ERR_INVALID;
+  st = check_ws(ws, ws_bytes, need);
+  if (st != CSA_OK) return st;
+  const csa_layer_args& a0 = layers[0].a;
+  size_t layer_ws = 0;
+  for (int i = 0; i < n_layers; ++i) {
+    const size_t w = stack_layer_ws(&layers[i]);
+    layer_ws = layer_ws > w ? layer_ws : w;
+  }
+  layer_ws = align_up(layer_ws, kAlignWs);
+  char* act[2] = {static_cast<char*>(ws) + layer_ws, static_cast<char*>(ws) + layer_ws + stack_act_bytes(&layers[0])};
+  // every layer's checks before anything is enqueued: same activation shape
+  // throughout, and a CSA layer's indexer queries are its input activation
+  for (int i = 0; i < n_layers; ++i) {
+    const csa_stack_layer* l = &layers[i];
+    const csa_layer_args& a = l->a;
+    if (a.B != a0.B || a.Tq != a0.Tq || a.H != a0.H || a.d != a0.d) return CSA_ERR_INVALID;
+    const void* in = i == 0 ? x : act[(i - 1) & 1];
+    void* out = i == n_layers - 1 ? y : act[i & 1];
+    const csa_layer_args la = stack_args(l, in, out, i == n_layers - 1 ? out_dtype : CSA_BF16);
+    if (l->kind == CSA_STACK_CSA) {
+      if (a.H_I * a.d_I != a.H * a.d) return CSA_ERR_INVALID;
+      if (a.g_k || a.g_v || a.g_i) return CSA_ERR_INVALID;  // decode: the caches are given
+      st = layer_check(&la, ws, layer_ws);
+    } else if (l->kind == CSA_STACK_HCA || l->kind == CSA_STACK_SWA) {
+      st = check_attend_args(la.q, la.k_cmp, la.v_cmp, la.k_win, la.v_win, la.raw_base, la.q_pos, la.B, la.Tq,
+                             l->kind == CSA_STACK_HCA ? la.N : 0, la.T_raw, la.H, la.d, la.W, la.out,
+                             la.out_dtype, nullptr);
+      if (st == CSA_OK && l->kind == CSA_STACK_HCA && la.m <= 0) st = CSA_ERR_INVALID;
+    } else {
+      st = CSA_ERR_INVALID;
+    }
+    if (st != CSA_OK) return st;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int i = 0; i < n_layers; ++i) {
+    const csa_stack_layer* l = &layers[i];
+    const void* in = i == 0 ? x : act[(i - 1) & 1];
+    void* out = i == n_layers - 1 ? y : act[i & 1];
+    const csa_layer_args la = stack_args(l, in, out, i == n_layers - 1 ? out_dtype : CSA_BF16);
+    if (l->kind == CSA_STACK_CSA) {
+      st = layer_enqueue(&la, ws, s);
+    } else {
+      // SWA: the window alone (no compressed entries); HCA: every visible entry + the window
+      const bool hca = l->kind == CSA_STACK_HCA;
+      st = attend_common(la.q, hca ? la.k_cmp : nullptr, hca ? la.v_cmp : nullptr, hca ? nullptr : la.q_pos,
+                         la.k_win, la.v_win, la.raw_base, la.q_pos, la.B, la.Tq, hca ? la.N : 0, la.T_raw, la.H,
+                         la.d, 0, hca ? la.m : 1, la.W, la.scale, la.out, la.out_dtype, nullptr, ws, layer_ws, s);
+    }
+    if (st != CSA_OK) return st;
+  }
+  return CSA_OK;
+}
+
 }  // extern "C"

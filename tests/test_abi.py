@@ -173,3 +173,32 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(ImportError):
         _lib.lib()
+
+
+def test_stack_validation_before_any_launch(L):
+    """csa_stack_decode refuses, before anything is enqueued, an unknown layer
+    kind, a CSA layer whose indexer query shape is not the activation's, and
+    layers of different activation shapes (fake device pointers: nothing runs)."""
+    def layer(kind, **kw):
+        la = _lib.csa_layer_args()
+        for n, v in dict(B=1, Tq=1, N=1024, m=4, H=64, d=128, H_I=64, d_I=128, k=64, W=8, T=0, T_raw=16).items():
+            setattr(la, n, v)
+        for n in ("k_cmp", "v_cmp", "i_cmp", "k_win", "v_win", "raw_base", "w", "q_pos"):
+            setattr(la, n, A16)
+        for n, v in kw.items():
+            setattr(la, n, v)
+        st = _lib.csa_stack_layer()
+        st.kind, st.a = kind, la
+        return st
+
+    def run(*ls):
+        arr = (_lib.csa_stack_layer * len(ls))(*ls)
+        need = ctypes.c_size_t(0)
+        assert L.csa_stack_workspace(arr, len(ls), ctypes.byref(need)) == 0
+        return L.csa_stack_decode(arr, len(ls), A16, A16, 0, A16, need.value, None)
+
+    assert run(layer(_lib.CSA_STACK_SWA), layer(7)) == _lib.CSA_ERR_INVALID
+    assert run(layer(_lib.CSA_STACK_SWA), layer(_lib.CSA_STACK_CSA, d_I=64)) == _lib.CSA_ERR_INVALID
+    assert run(layer(_lib.CSA_STACK_SWA), layer(_lib.CSA_STACK_HCA, H=32)) == _lib.CSA_ERR_INVALID
+    assert run(layer(_lib.CSA_STACK_HCA, m=0)) == _lib.CSA_ERR_INVALID
+    assert L.csa_stack_decode(None, 1, A16, A16, 0, A16, 1 << 20, None) == _lib.CSA_ERR_INVALID
