@@ -450,6 +450,139 @@ def decode_also(name, dev, stream, steps):
             "step_frac_of_hbm": sb / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
 
 
+def _graph_ms(fn, stream, steps, marks=None, L=None):
+    """ms per call of fn (a graph of ``steps`` calls, after warm-up)."""
+    with torch.cuda.stream(stream):
+        fn(stream.cuda_stream)
+        stream.synchronize()
+        g1 = graph_of(fn, stream)
+        gk = graph_of(fn, stream, n=steps)
+        gm = graph_of(fn, stream, n=steps, marks=marks, L=L) if marks is not None else None
+    warm(g1, 10, stream, min_warm_s=0.1)
+    ms = time_steps(gk, steps, stream)
+    if gm is not None:
+        time_steps(gm, steps, stream)
+    return ms
+
+
+def decode_1m_variants(dev, stream, steps):
+    """The 1M decode step (B = 4) with the decode-time append of the block
+    its position completes (t = 1048575: block 262143 is compressed from the
+    window rows into all three caches before the indexer), and with E4M3
+    indexer keys (quantised once, outside the timing; the step quantises its
+    indexer queries)."""
+    import long_context_sparse_23_b300 as csa
+    out = {}
+    ds = DecodeStep("decode_1m", dev)
+    wl, i = ds.wl, ds.inp
+    B = ds.B
+    # append: raw indexer-key rows and gate logits of the window
+    win = {n: S.normal_bf16(wl.seed, S.TID[n], (B, wl.raw_len, wl.d_I if n in ("i_raw", "g_i") else wl.d), dev,
+                            offset=0)
+           for n in ("i_raw", "g_k", "g_v", "g_i")}
+    a = csa.layer_args(B=B, Tq=1, N=wl.N, m=wl.m, H=wl.H, d=wl.d, H_I=wl.H_I, d_I=wl.d_I, k=wl.k, W=wl.W,
+                       T_raw=wl.raw_len, k_cmp=i["k_cmp"], v_cmp=i["v_cmp"], i_cmp=i["i_cmp"], k_win=i["k_raw"],
+                       v_win=i["v_raw"], raw_base=i["raw_base"], q=i["q"], q_idx=i["q_idx"], w=i["w"],
+                       q_pos=i["q_pos"], out=ds.out, i_win=win["i_raw"], gk_win=win["g_k"], gv_win=win["g_v"],
+                       gi_win=win["g_i"])
+    need = ctypes.c_size_t(0)
+    ds.L.csa_layer_workspace(ctypes.byref(a), ctypes.byref(need))
+    ws = csa.Workspace(need.value, dev)
+
+    def step_append(st):
+        assert ds.L.csa_layer(ctypes.byref(a), ws.ptr, ws.nbytes, st) == 0
+
+    ms = _graph_ms(step_append, stream, steps)
+    assert ws.check_error() == 0
+    out["decode_1m_append"] = {"ms_per_step": ms, "queries_per_s": B / (ms * 1e-3),
+                               "appended": "block 262143 of K, V and the indexer keys, every step"}
+
+    # FP8 indexer keys
+    k8, ks = csa.csa_quantize_fp8(i["i_cmp"])
+    a8 = csa.layer_args(B=B, Tq=1, N=wl.N, m=wl.m, H=wl.H, d=wl.d, H_I=wl.H_I, d_I=wl.d_I, k=wl.k, W=wl.W,
+                        T_raw=wl.raw_len, k_cmp=i["k_cmp"], v_cmp=i["v_cmp"], i_cmp=k8, k_win=i["k_raw"],
+                        v_win=i["v_raw"], raw_base=i["raw_base"], q=i["q"], q_idx=i["q_idx"], w=i["w"],
+                        q_pos=i["q_pos"], out=ds.out, i_scale=ks)
+    ds.L.csa_layer_workspace(ctypes.byref(a8), ctypes.byref(need))
+    ws8 = csa.Workspace(need.value, dev)
+
+    def step_fp8(st):
+        assert ds.L.csa_layer(ctypes.byref(a8), ws8.ptr, ws8.nbytes, st) == 0
+
+    ev_b, ev_e = timing_events(steps, stream), timing_events(steps, stream)
+    ms8 = _graph_ms(step_fp8, stream, steps, marks=(ev_b, ev_e), L=ds.L)
+    assert ws8.check_error() == 0
+    ms_idx = sum(b_.elapsed_time(e_) for b_, e_ in zip(ev_b, ev_e)) / steps
+    peaks, _ = _peaks()
+    n_vis = B * wl.N
+    ibytes = n_vis * (wl.d_I + 4 + 4) + B * wl.H_I * (wl.d_I + 4)   # codes + key scale + score; query codes
+    sb = ibytes + B * ((wl.k + wl.W) * 2 * wl.d * 2 + 2 * wl.H * wl.d * 2)
+    out["decode_1m_fp8_indexer"] = {
+        "ms_per_step": ms8, "queries_per_s": B / (ms8 * 1e-3), "indexer_ms": ms_idx, "indexer_bytes": ibytes,
+        "indexer_frac_of_hbm": ibytes / (ms_idx * 1e-3) / 1e9 / peaks["hbm_gbs"], "step_bytes": sb,
+        "step_frac_of_hbm": sb / (ms8 * 1e-3) / 1e9 / peaks["hbm_gbs"],
+        "keys": "E4M3 codes + one fp32 power-of-two scale per entry (132 B instead of 256 B)"}
+    del ds
+    return out
+
+
+def hybrid_stack_1m(dev, stream, steps, n_pairs=7):
+    """One decode step of the hybrid stack at 1M context, B = 4: two
+    sliding-window layers, then n_pairs x (CSA, HCA) (CSA: 262144 entries at
+    m = 4, top-1024; HCA: 8192 entries at m' = 128; window 128 everywhere),
+    each layer with its own synthetic caches; one csa_stack_decode call."""
+    import long_context_sparse_23_b300 as csa
+    from long_context_sparse_23_b300 import _lib
+    L = _lib.lib()
+    wl = S.WORKLOADS["decode_1m"]
+    B, H, d, W, T_raw = wl.B, wl.H, wl.d, wl.W, wl.raw_len
+    t = wl.q_positions[0]
+    q_pos = torch.full((B, 1), t, dtype=torch.int32, device=dev)
+    raw_base = torch.full((B,), t + 1 - T_raw, dtype=torch.int32, device=dev)
+    kinds = [_lib.CSA_STACK_SWA] * 2 + [_lib.CSA_STACK_CSA, _lib.CSA_STACK_HCA] * n_pairs
+    layers = (_lib.csa_stack_layer * len(kinds))()
+    keep = []
+    N_h = (t + 1) // 128
+    for li, kind in enumerate(kinds):
+        sd = 100 + li
+        kw = S.normal_bf16(sd, S.TID["k_raw"], (B, T_raw, d), dev)
+        vw = S.normal_bf16(sd, S.TID["v_raw"], (B, T_raw, d), dev)
+        keep += [kw, vw]
+        if kind == _lib.CSA_STACK_CSA:
+            kc = S.normal_bf16(sd, S.TID["k_cmp"], (B, wl.N, d), dev)
+            vc = S.normal_bf16(sd, S.TID["v_cmp"], (B, wl.N, d), dev)
+            ic = S.normal_bf16(sd, S.TID["i_cmp"], (B, wl.N, wl.d_I), dev)
+            w = S.uniform_f32(sd, S.TID["w"], (wl.H_I,), dev)
+            keep += [kc, vc, ic, w]
+            a = csa.layer_args(B=B, Tq=1, N=wl.N, m=wl.m, H=H, d=d, H_I=wl.H_I, d_I=wl.d_I, k=wl.k, W=W,
+                               T_raw=T_raw, k_cmp=kc, v_cmp=vc, i_cmp=ic, k_win=kw, v_win=vw, raw_base=raw_base,
+                               w=w, q_pos=q_pos)
+        elif kind == _lib.CSA_STACK_HCA:
+            kc = S.normal_bf16(sd, S.TID["k_cmp"], (B, N_h, d), dev)
+            vc = S.normal_bf16(sd, S.TID["v_cmp"], (B, N_h, d), dev)
+            keep += [kc, vc]
+            a = csa.layer_args(B=B, Tq=1, N=N_h, m=128, H=H, d=d, H_I=0, d_I=0, k=0, W=W, T_raw=T_raw, k_cmp=kc,
+                               v_cmp=vc, k_win=kw, v_win=vw, raw_base=raw_base, q_pos=q_pos)
+        else:
+            a = csa.layer_args(B=B, Tq=1, N=0, m=1, H=H, d=d, H_I=0, d_I=0, k=0, W=W, T_raw=T_raw, k_win=kw,
+                               v_win=vw, raw_base=raw_base, q_pos=q_pos)
+        layers[li].kind = kind
+        layers[li].a = a
+    x = S.normal_bf16(99, S.TID["q"], (B, 1, H, d), dev)
+    y = torch.empty_like(x)
+    need = ctypes.c_size_t(0)
+    assert L.csa_stack_workspace(layers, len(kinds), ctypes.byref(need)) == 0
+    ws = csa.Workspace(need.value, dev)
+
+    def step(st):
+        assert L.csa_stack_decode(layers, len(kinds), x.data_ptr(), y.data_ptr(), 0, ws.ptr, ws.nbytes, st) == 0
+
+    ms = _graph_ms(step, stream, steps)
+    assert ws.check_error() == 0
+    return {"layers": f"2 sliding-window + {n_pairs} x (CSA, HCA)", "ms_per_token_step": ms,
+            "tokens_per_s": B / (ms * 1e-3), "B": B, "context": t + 1}
+
+
 def prefill_8k(dev, stream, steps):
     """The whole layer over an 8192-token prefill (compress -> indexer ->
     top-k -> attention): tokens/s, and the indexer's bf16 tensor-core rate
@@ -737,6 +870,10 @@ def main():
     extra["decode_128k"] = decode_also("decode_128k", dev, stream, max(10, args.steps // 4))
     torch.cuda.empty_cache()
     extra["decode_1m_tail"] = decode_also("decode_1m_tail", dev, stream, max(10, args.steps // 8))
+    torch.cuda.empty_cache()
+    extra.update(decode_1m_variants(dev, stream, max(10, args.steps // 8)))
+    torch.cuda.empty_cache()
+    extra["hybrid_stack_1m"] = hybrid_stack_1m(dev, stream, max(5, args.steps // 50))
     torch.cuda.empty_cache()
     extra["prefill_8k"] = prefill_8k(dev, stream, max(5, args.steps // 100))
     torch.cuda.empty_cache()

@@ -207,39 +207,64 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     for (int sub = lo; sub < hi; sub += kT * kRun) {
       if (sub != lo) issue_batch(sub);  // the first batch was requested before the bucket search
       bulk_wait();
-      // thread tid owns the run [sub + kRun*tid, sub + kRun*(tid+1)); its 16
-      // float4 reads start at a rotated position (fewer bank conflicts)
-      const int i0 = sub + kRun * tid;
-      unsigned long long take = 0ull, inb = 0ull;
-#pragma unroll
-      for (int jr = 0; jr < kRun / 4; ++jr) {
-        const int j = (jr + tid) & (kRun / 4 - 1);
-        const float4 fv = *reinterpret_cast<const float4*>(stage + kRun * tid + 4 * j);
+      // warp w owns the contiguous segment [w*SEG, (w+1)*SEG) of the batch and
+      // reads it as one float4 per lane (128 consecutive scores per step:
+      // conflict-free); pass 1 counts its candidates and feeds bucket beta's
+      // keys into the second-level histogram, pass 2 writes the candidates
+      // in index order after a scan over the warps' counts
+      constexpr int NWS = kT / 32, SEG = kT * kRun / NWS;
+      const int nb = min(kT * kRun, hi - sub);
+      const int s_lo = warp * SEG, s_hi = min(nb, s_lo + SEG);
+      uint32_t wcount = 0;
+      for (int base = s_lo; base < s_hi; base += 128) {
+        const int i = base + 4 * lane;
+        const float4 fv = *reinterpret_cast<const float4*>(stage + i);
         const float v4[4] = {fv.x, fv.y, fv.z, fv.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const uint32_t bin = score_key(v4[e]) >> 20;
-          const bool in = i0 + 4 * j + e < hi;
-          const unsigned long long bit = 1ull << (4 * j + e);
-          take |= (in && bin >= beta) ? bit : 0ull;
-          inb |= (in && bin == beta) ? bit : 0ull;
+          const uint32_t key = score_key(v4[e]);
+          const bool in = i + e < s_hi;
+          wcount += (in && (key >> 20) >= beta) ? 1u : 0u;
+          // bucket beta holds about k of the keys: one reduction per key of it
+          if (in && (key >> 20) == beta) atomicAdd(hist2 + ((key >> 8) & (kTopkBins - 1)), 1u);
         }
       }
-      // bucket beta holds about k of the keys: one reduction per key of it
-      for (unsigned long long m2 = inb; m2; m2 &= m2 - 1) {
-        const int p = __ffsll(static_cast<long long>(m2)) - 1;
-        atomicAdd(hist2 + ((score_key(stage[kRun * tid + p]) >> 8) & (kTopkBins - 1)), 1u);
-      }
-      const uint32_t mine = static_cast<uint32_t>(__popcll(take));
-      const uint32_t incl = block_incl_scan<kT>(mine, tmp);
-      if (tid == kT - 1) tot32 = incl;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) wcount += __shfl_xor_sync(0xffffffffu, wcount, o);
+      if (lane == 0) tmp[warp] = wcount;
       __syncthreads();
-      uint32_t pos = n_own + incl - mine;
-      while (take) {
-        const int p = __ffsll(static_cast<long long>(take)) - 1;
-        take &= take - 1;
-        gl[pos++] = make_uint2(score_key(stage[kRun * tid + p]), static_cast<uint32_t>(i0 + p));
+      uint32_t pos = n_own;
+      for (int w = 0; w < warp; ++w) pos += tmp[w];
+      if (tid == 0) {
+        uint32_t t = 0;
+        for (int w = 0; w < NWS; ++w) t += tmp[w];
+        tot32 = t;
       }
+      for (int base = s_lo; base < s_hi; base += 128) {
+        const int i = base + 4 * lane;
+        const float4 fv = *reinterpret_cast<const float4*>(stage + i);
+        const float v4[4] = {fv.x, fv.y, fv.z, fv.w};
+        uint32_t kk[4], mine = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          kk[e] = score_key(v4[e]);
+          mine |= (i + e < s_hi && (kk[e] >> 20) >= beta) ? (1u << e) : 0u;
+        }
+        // candidates of the lanes before this one, then this lane's in order
+        const uint32_t c = static_cast<uint32_t>(__popc(mine));
+        uint32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += n;
+        }
+        uint32_t at = pos + incl - c;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (mine & (1u << e)) gl[at++] = make_uint2(kk[e], static_cast<uint32_t>(sub + i + e));
+        pos += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      __syncthreads();  // tot32 written; tmp read
       n_own += tot32;
       __syncthreads();  // the stage and tot32 are rewritten by the next batch
     }

@@ -107,6 +107,15 @@ __device__ __forceinline__ Item item_of(const KParams& p, int r) {
   return it;
 }
 
+// Key tile of the item's i-th step: the item's tiles rotated by the CTA
+// index, so CTAs working on the same (L2-resident) keys at the same time read
+// different tiles, not all the same one.
+__device__ __forceinline__ int tile_at(const Item& I, int i) {
+  const int rot = static_cast<int>(blockIdx.x) % I.ntile;
+  const int j = i + rot;
+  return I.tile_lo + (j >= I.ntile ? j - I.ntile : j);
+}
+
 // Rank of this CTA's k-th item, or -1: rounds of gridDim.x ranks, taken in
 // alternating direction (snake order), so every CTA gets a similar share of
 // heavy and light items.
@@ -229,9 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(&bars->full[s], p.kh * kHalfBytes + (F8 ? kTileKeys * 4 : 0));
           char* dst = ks + s * p.kh * kHalfBytes;
           for (int h = 0; h < p.kh; ++h)
-            tma_load_3d_hint(dst + h * kHalfBytes, &tmk, &bars->full[s], h * 64, (I.tile_lo + i) * kTileKeys, I.b,
+            tma_load_3d_hint(dst + h * kHalfBytes, &tmk, &bars->full[s], h * 64, tile_at(I, i) * kTileKeys, I.b,
                              key_policy);
-          if (F8) tma_load_2d(ksc + s * kTileKeys, &tms, &bars->full[s], (I.tile_lo + i) * kTileKeys, I.b);
+          if (F8) tma_load_2d(ksc + s * kTileKeys, &tms, &bars->full[s], tile_at(I, i) * kTileKeys, I.b);
           ++gt;
         }
       }
@@ -292,7 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (gt > 0) mbar_wait(&bars->tfull[(gt - 1) & 1], ((gt - 1) >> 1) & 1, kDrainBudget, nullptr);
     }
   } else if (warp == 2) {
-    // ---- item producer: head weights, visibility and query rows
+    // ---- item producer: query rows first (the MMAs wait for them), then the
+    // head weights and visibility the epilogue needs
     if (lane == 0) tma_prefetch_desc(&tmq);
     int it = 0, q_issued = 0;
     for (int k = 0;; ++k) {
@@ -301,14 +311,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item I = item_of(p, r);
       if (I.ntile <= 0) continue;
       const int ib = it & 1;
-      // the weight buffer of parity ib was last read for item it - 2
       bool ok = true;
-      if (it >= 2 && lane == 0) ok = mbar_wait(&bars->wfree[ib], ((it - 2) >> 1) & 1, p.budget, abort_v);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        if (lane == 0) fail();
-        break;
+      if (lane == 0) {
+        // the query rows, once the MMAs of the previous item are done
+        ok = it == 0 || mbar_wait(&bars->qfree, (it - 1) & 1, p.budget, abort_v);
+        if (ok) {
+          mbar_expect_tx(&bars->qfull, p.kh * p.NC * 128);
+          const int qrow = (I.b * p.Tq + I.j0) * HI;
+          for (int h = 0; h < p.kh; ++h) tma_load_2d(qs + h * p.NC * 128, &tmq, &bars->qfull, h * 64, qrow);
+          q_issued = it + 1;
+          // the next item's query rows into L2 while this item runs
+          const int rn = rank_of(k + 1, p);
+          if (rn >= 0) {
+            const Item J = item_of(p, rn);
+            const int jn = min(p.G, p.Tq - J.j0);
+            const uint32_t bytes = static_cast<uint32_t>(jn * HI * p.q_row_bytes);
+            const char* src = static_cast<const char*>(p.q_base) +
+                              (static_cast<size_t>(J.b) * p.Tq + J.j0) * HI * p.q_row_bytes;
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+          }
+          // the weight buffer of parity ib was last read for item it - 2
+          if (it >= 2) ok = mbar_wait(&bars->wfree[ib], ((it - 2) >> 1) & 1, p.budget, abort_v);
+        }
+        if (!ok) fail();
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
       for (int i = lane; i < p.G * HI; i += 32) {
         const int jj = i / HI, h = i % HI;
         const long long qrow = static_cast<long long>(I.b) * p.Tq + I.j0 + jj;
@@ -327,31 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         nvis_s[ib][jj] = nv;
       }
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars->wfull[ib]);
-        // the query rows, once the MMAs of the previous item are done
-        ok = it == 0 || mbar_wait(&bars->qfree, (it - 1) & 1, p.budget, abort_v);
-        if (ok) {
-          mbar_expect_tx(&bars->qfull, p.kh * p.NC * 128);
-          const int qrow = (I.b * p.Tq + I.j0) * HI;
-          for (int h = 0; h < p.kh; ++h) tma_load_2d(qs + h * p.NC * 128, &tmq, &bars->qfull, h * 64, qrow);
-          q_issued = it + 1;
-          // the next item's query rows into L2 while this item runs
-          const int rn = rank_of(k + 1, p);
-          if (rn >= 0) {
-            const Item J = item_of(p, rn);
-            const int jn = min(p.G, p.Tq - J.j0);
-            const uint32_t bytes = static_cast<uint32_t>(jn * HI * p.q_row_bytes);
-            const char* src = static_cast<const char*>(p.q_base) +
-                              (static_cast<size_t>(J.b) * p.Tq + J.j0) * HI * p.q_row_bytes;
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-          }
-        } else {
-          fail();
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      if (lane == 0) mbar_arrive(&bars->wfull[ib]);
       ++it;
     }
     // drain: the last query copy has landed before the CTA may exit
@@ -400,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) fail();
         } else {
           tc_fence_after();
-          const int key = (I.tile_lo + i) * kTileKeys + row;
+          const int key = tile_at(I, i) * kTileKeys + row;
           if constexpr (HI >= 16) {
             for (int jj = 0; jj < p.G; ++jj) {
               // all of the query's head columns in flight at once, one wait

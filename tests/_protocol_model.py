@@ -105,20 +105,23 @@ def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "", 
                 gt += 1
 
     def item_producer():
+        # the query rows first (the MMAs wait for them), then the weights
         for it in range(len(live)):
             ib = it & 1
+            if it >= 1 and plant != "qfree":
+                yield (qfree, (it - 1) & 1)
+                assert mma_items_done[0] >= it, "query rows refilled before the previous item's MMAs ended"
+            if it >= 1:
+                assert mma_items_done[0] >= it or plant == "qfree"
+            q_item[0] = it
+            yield None
+            qfull.arrive()
             if it >= 2 and plant != "wfree":
                 yield (wfree[ib], ((it - 2) >> 1) & 1)
                 assert min(epi_done[ib]) >= (it - 2) // 2 + 1, "weights refilled while a group still reads them"
             w_item[ib] = it
             yield None
             wfull[ib].arrive()
-            if it >= 1 and plant != "qfree":
-                yield (qfree, (it - 1) & 1)
-                assert mma_items_done[0] >= it, "query rows refilled before the previous item's MMAs ended"
-            q_item[0] = it
-            yield None
-            qfull.arrive()
 
     def mma():
         gt = 0
