@@ -356,7 +356,13 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     }
     const unsigned ltm = lanemask_lt();
     const int p_lo = r * S_r, p_hi = p_lo + S_r;
-    for (int i = warp * RPW; i < (warp + 1) * RPW; ++i) {
+    // this warp's kept candidates take the output positions [w_lo, w_hi)
+    // (in index order); a warp whose range misses this CTA's slots has
+    // nothing to write here
+    const uint32_t w_lo = run_gt + min(run_eq, rl.k_rem);
+    const uint32_t w_hi = run_gt + wg[warp] + min(run_eq + we[warp], rl.k_rem);
+    const bool overlaps = w_lo < w_hi && static_cast<int>(w_lo) < p_hi && static_cast<int>(w_hi) > p_lo;
+    for (int i = warp * RPW; overlaps && i < (warp + 1) * RPW; ++i) {
       const int n = static_cast<int>(rcnt[i]);
       for (int base = 0; base < n; base += 32) {
         const int c = base + lane;

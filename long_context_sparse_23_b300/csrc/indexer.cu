@@ -54,6 +54,7 @@ struct KParams {
   int items_per_group;
   int tiles_per_item;
   int items;          // B * n_groups * items_per_group
+  int per_cta;        // > 0: CTA c owns the contiguous ranks [c * per_cta, (c + 1) * per_cta)
   int tmem_cols;
   uint32_t* errw;
   long long budget;
@@ -69,8 +70,8 @@ struct __align__(8) Bars {
   uint64_t empty[8];   // key stage consumed by the MMAs
   uint64_t tfull[2];   // accumulator buffer written by the MMAs
   uint64_t tempty[2];  // accumulator buffer read by its epilogue group
-  uint64_t qfull;      // the item's queries loaded
-  uint64_t qfree;      // the item's MMAs done: the query buffer may be refilled
+  uint64_t qfull;      // a query group's rows loaded (one phase per load)
+  uint64_t qfree;      // a query group's MMAs done: the query buffer may be refilled
   uint64_t wfull[2];   // head weights / visibility of an item written
   uint64_t wfree[2];   // both epilogue groups are done with an item's weights
   uint64_t sfree[8];   // FP8: the key scales of a stage read by the epilogue
@@ -116,13 +117,34 @@ __device__ __forceinline__ int tile_at(const Item& I, int i) {
   return I.tile_lo + (j >= I.ntile ? j - I.ntile : j);
 }
 
-// Rank of this CTA's k-th item, or -1: rounds of gridDim.x ranks, taken in
+// Rank of this CTA's k-th item, or -1.  Items of unequal weight (prefill:
+// causal rows of every length) go in rounds of gridDim.x ranks taken in
 // alternating direction (snake order), so every CTA gets a similar share of
-// heavy and light items.
+// heavy and light items; items of equal weight (decode: one query group per
+// sequence) go in contiguous blocks, so a CTA's consecutive items share
+// their query rows and histogram.
 __device__ __forceinline__ int rank_of(int k, const KParams& p) {
   const int n = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-  const long long r = static_cast<long long>(k) * n + ((k & 1) ? n - 1 - c : c);
+  long long r;
+  if (p.per_cta > 0) {
+    if (k >= p.per_cta) return -1;
+    r = static_cast<long long>(c) * p.per_cta + k;
+  } else {
+    r = static_cast<long long>(k) * n + ((k & 1) ? n - 1 - c : c);
+  }
   return r < p.items ? static_cast<int>(r) : -1;
+}
+
+__device__ __forceinline__ bool same_group(const Item& a, const Item& b) { return a.b == b.b && a.j0 == b.j0; }
+
+// The first item with visible tiles after this CTA's k-th item (false: none).
+__device__ __forceinline__ bool next_item(const KParams& p, int k, Item* J) {
+  for (int kk = k + 1;; ++kk) {
+    const int r = rank_of(kk, p);
+    if (r < 0) return false;
+    *J = item_of(p, r);
+    if (J->ntile > 0) return true;
+  }
 }
 
 __device__ __forceinline__ void group_bar(int g) {
@@ -254,17 +276,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = F8 ? idesc_e4m3_f32(128, p.NC) : idesc_bf16_f32(128, p.NC);
-      int gt = 0, it = 0;
+      int gt = 0, nq = 0;
       bool ok = true;
+      Item prev{-1, -1, 0, 0};
       for (int k = 0; ok; ++k) {
         const int r = rank_of(k, p);
         if (r < 0) break;
         const Item I = item_of(p, r);
         if (I.ntile <= 0) continue;
-        if (!mbar_wait(&bars->qfull, it & 1, p.budget, abort_v)) {
-          fail();
-          break;
+        if (nq == 0 || !same_group(I, prev)) {
+          // a new query group: the query buffer may be refilled once the
+          // previous group's MMAs are done, and this group's rows must be in
+          if (nq > 0) umma_commit(&bars->qfree);
+          if (!mbar_wait(&bars->qfull, nq & 1, p.budget, abort_v)) {
+            fail();
+            break;
+          }
+          ++nq;
         }
+        prev = I;
         for (int i = 0; i < I.ntile; ++i) {
           const int s = gt % p.stages;
           const uint32_t ph = (gt / p.stages) & 1;
@@ -294,8 +324,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++gt;
         }
         if (!ok) break;
-        umma_commit(&bars->qfree);  // the query buffer is free once this item's MMAs are done
-        ++it;
       }
       // drain: the last MMAs have finished reading shared memory / writing TMEM
       if (gt > 0) mbar_wait(&bars->tfull[(gt - 1) & 1], ((gt - 1) >> 1) & 1, kDrainBudget, nullptr);
@@ -304,22 +332,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- item producer: query rows first (the MMAs wait for them), then the
     // head weights and visibility the epilogue needs
     if (lane == 0) tma_prefetch_desc(&tmq);
-    int it = 0, q_issued = 0;
+    int it = 0, nq = 0;
+    Item prev{-1, -1, 0, 0};
     for (int k = 0;; ++k) {
       const int r = rank_of(k, p);
       if (r < 0) break;
       const Item I = item_of(p, r);
       if (I.ntile <= 0) continue;
       const int ib = it & 1;
+      const bool new_group = nq == 0 || !same_group(I, prev);
+      prev = I;
       bool ok = true;
-      if (lane == 0) {
-        // the query rows, once the MMAs of the previous item are done
-        ok = it == 0 || mbar_wait(&bars->qfree, (it - 1) & 1, p.budget, abort_v);
+      if (lane == 0 && new_group) {
+        // the query rows, once the MMAs of the previous query group are done
+        ok = nq == 0 || mbar_wait(&bars->qfree, (nq - 1) & 1, p.budget, abort_v);
         if (ok) {
           mbar_expect_tx(&bars->qfull, p.kh * p.NC * 128);
           const int qrow = (I.b * p.Tq + I.j0) * HI;
           for (int h = 0; h < p.kh; ++h) tma_load_2d(qs + h * p.NC * 128, &tmq, &bars->qfull, h * 64, qrow);
-          q_issued = it + 1;
           // the next item's query rows into L2 while this item runs
           const int rn = rank_of(k + 1, p);
           if (rn >= 0) {
@@ -330,13 +360,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                               (static_cast<size_t>(J.b) * p.Tq + J.j0) * HI * p.q_row_bytes;
             asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
           }
-          // the weight buffer of parity ib was last read for item it - 2
-          if (it >= 2) ok = mbar_wait(&bars->wfree[ib], ((it - 2) >> 1) & 1, p.budget, abort_v);
         }
+        if (!ok) fail();
+      }
+      if (lane == 0 && ok && it >= 2) {
+        // the weight buffer of parity ib was last read for item it - 2
+        ok = mbar_wait(&bars->wfree[ib], ((it - 2) >> 1) & 1, p.budget, abort_v);
         if (!ok) fail();
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
+      if (new_group) ++nq;
       for (int i = lane; i < p.G * HI; i += 32) {
         const int jj = i / HI, h = i % HI;
         const long long qrow = static_cast<long long>(I.b) * p.Tq + I.j0 + jj;
@@ -359,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++it;
     }
     // drain: the last query copy has landed before the CTA may exit
-    if (lane == 0 && q_issued > 0) mbar_wait(&bars->qfull, (q_issued - 1) & 1, kDrainBudget, nullptr);
+    if (lane == 0 && nq > 0) mbar_wait(&bars->qfull, (nq - 1) & 1, kDrainBudget, nullptr);
   } else {
     // ---- epilogue warps: TMEM lane quarter = warp % 4; group e handles the
     // CTA's tiles gt = e (mod 2), i.e. TMEM accumulator buffer e
@@ -459,9 +493,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this group is done with the item's weights and visibility
       group_bar(egroup);
       if ((ew & 3) == 0 && lane == 0) mbar_arrive(&bars->wfree[ib]);
-      if (p.hist) {
-        // both groups' counts of the item are in: flush them (once the
-        // histogram has been zeroed), then clear for the next item
+      Item J;
+      if (p.hist && !(next_item(p, k, &J) && same_group(I, J))) {
+        // both groups' counts of the query group are in: flush them (once
+        // the histogram has been zeroed), then clear for the next group
         epi_bar();
         if (p.after_zero && !waited_zero) {
           asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -522,9 +557,21 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   const int n_tiles_all = (a.N + kTileKeys - 1) / kTileKeys;
   const long long groups = static_cast<long long>(a.B) * p.n_groups;
   const int n_sm = sm_count();
-  // tile ranges per group: one item per SM when the groups alone cannot fill the GPU
-  int ipg = static_cast<int>(n_sm / (groups > 0 ? groups : 1));
-  ipg = ipg < 1 ? 1 : (ipg > n_tiles_all ? n_tiles_all : ipg);
+  // tile ranges per group when the groups alone cannot fill the GPU: as many
+  // that the item count is a multiple of the SM count (lcm(groups, SMs)
+  // items), or failing that (too few tiles) one item per SM
+  int ipg = 1;
+  if (groups < n_sm) {
+    long long g = groups, h = n_sm;
+    while (h != 0) {
+      const long long t = g % h;
+      g = h;
+      h = t;
+    }
+    ipg = static_cast<int>(n_sm / g);
+    if (ipg > n_tiles_all) ipg = static_cast<int>(n_sm / groups);
+    ipg = ipg < 1 ? 1 : (ipg > n_tiles_all ? n_tiles_all : ipg);
+  }
   p.tiles_per_item = (n_tiles_all + ipg - 1) / ipg;
   p.items_per_group = (n_tiles_all + p.tiles_per_item - 1) / p.tiles_per_item;
   p.errw = a.errw;
@@ -539,6 +586,10 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   if (items > 0x7fffffffLL) return cudaErrorNotSupported;
   p.items = static_cast<int>(items);
   const int grid = static_cast<int>(items < n_sm ? items : n_sm);
+  // one query group per sequence (decode): items of equal weight, in
+  // contiguous blocks per CTA; several groups per sequence (prefill, causal
+  // rows of every length): snake order
+  p.per_cta = p.n_groups == 1 ? static_cast<int>((items + grid - 1) / grid) : 0;
 
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;

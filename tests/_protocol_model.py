@@ -67,11 +67,16 @@ def named_barrier(bar: Bar, use: int):
 # (qfull, refilled once the MMAs of the previous item are done: qfree); with
 # the histogram both groups meet at every item's end (two named barriers).
 
-def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "", fp8: bool = False) -> bool:
-    """``plant`` names a wait to leave out ("qfree", "wfree", "sfree"), for the
-    tests that show the hazard checks catch a missing wait.  ``fp8``: the key
-    scales share the stage ring and a stage's scale slot is released by the
-    four warps of the epilogue group that read it (sfree)."""
+def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "", fp8: bool = False,
+            groups=None) -> bool:
+    """``items``: tile counts of the CTA's items in order (0 = nothing
+    visible, skipped); ``groups``: the query group of each item (consecutive
+    items of one group share the query rows, loaded once, and the histogram,
+    flushed once).  ``plant`` names a wait to leave out ("qfree", "wfree",
+    "sfree"), for the tests that show the hazard checks catch a missing wait.
+    ``fp8``: the key scales share the stage ring and a stage's scale slot is
+    released by the four warps of the epilogue group that read it (sfree)."""
+    groups = list(range(len(items))) if groups is None else groups
     full = [Bar(1) for _ in range(stages)]
     empty = [Bar(1) for _ in range(stages)]
     sfree = [Bar(4) for _ in range(stages)]
@@ -81,12 +86,15 @@ def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "", 
     wfull, wfree = [Bar(1), Bar(1)], [Bar(2), Bar(2)]
     group_bar = [Bar(4), Bar(4)]
     epi_bar = Bar(8)
-    live = [n for n in items if n > 0]
+    live = [(n, g) for n, g in zip(items, groups) if n > 0]
     loads = [0] * stages
-    q_item = [-1]                 # the item whose query rows the buffer holds
+    q_group = [None]              # the query group whose rows the buffer holds
     w_item = [-1, -1]             # the item whose weights each buffer holds
-    mma_items_done = [0]          # items whose MMAs have completed
+    mma_groups_done = [0]         # query groups whose MMAs have completed
     epi_done = [[0, 0], [0, 0]]   # [buffer][group]: items of that buffer parity finished by the group
+
+    def new_group(it):
+        return it == 0 or live[it][1] != live[it - 1][1]
 
     def key_producer():
         gt = 0
@@ -105,17 +113,19 @@ def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "", 
                 gt += 1
 
     def item_producer():
-        # the query rows first (the MMAs wait for them), then the weights
+        # per item: the query rows when its group is new (the MMAs wait for
+        # them), then the weights
+        nq = 0
         for it in range(len(live)):
             ib = it & 1
-            if it >= 1 and plant != "qfree":
-                yield (qfree, (it - 1) & 1)
-                assert mma_items_done[0] >= it, "query rows refilled before the previous item's MMAs ended"
-            if it >= 1:
-                assert mma_items_done[0] >= it or plant == "qfree"
-            q_item[0] = it
-            yield None
-            qfull.arrive()
+            if new_group(it):
+                if nq >= 1 and plant != "qfree":
+                    yield (qfree, (nq - 1) & 1)
+                    assert mma_groups_done[0] >= nq, "query rows refilled before the previous group's MMAs ended"
+                q_group[0] = live[it][1]
+                yield None
+                qfull.arrive()
+                nq += 1
             if it >= 2 and plant != "wfree":
                 yield (wfree[ib], ((it - 2) >> 1) & 1)
                 assert min(epi_done[ib]) >= (it - 2) // 2 + 1, "weights refilled while a group still reads them"
@@ -124,9 +134,14 @@ def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "", 
             wfull[ib].arrive()
 
     def mma():
-        gt = 0
-        for it, n in enumerate(live):
-            yield (qfull, it & 1)
+        gt = nq = 0
+        for it, (n, g) in enumerate(live):
+            if new_group(it):
+                if nq > 0:
+                    mma_groups_done[0] += 1    # the commit completes once the previous group's MMAs are done
+                    qfree.arrive()
+                yield (qfull, nq & 1)
+                nq += 1
             for _ in range(n):
                 s, ph = gt % stages, (gt // stages) & 1
                 acc, aph = gt & 1, (gt >> 1) & 1
@@ -134,17 +149,15 @@ def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "", 
                 yield (full[s], ph)
                 assert loads[s] == gt // stages + 1, "MMA read a stage that holds another tile"
                 assert tempty[acc].done >= gt >> 1, "accumulator overwritten before the epilogue read it"
-                assert q_item[0] == it, "MMA read another item's query rows"
+                assert q_group[0] == g, "MMA read another group's query rows"
                 empty[s].arrive()
                 tfull[acc].arrive()
                 gt += 1
-            mma_items_done[0] += 1    # the commit completes once these MMAs are done
-            qfree.arrive()
 
     def epilogue(group: int, first: bool):
         gt = 0
         uses = 0
-        for it, n in enumerate(live):
+        for it, (n, g) in enumerate(live):
             ib = it & 1
             yield (wfull[ib], (it >> 1) & 1)
             assert w_item[ib] == it, "epilogue read another item's weights"
@@ -164,7 +177,7 @@ def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "", 
             if first:
                 epi_done[ib][group] += 1
                 wfree[ib].arrive()
-            if hist:
+            if hist and (it + 1 == len(live) or live[it + 1][1] != g):
                 yield from named_barrier(epi_bar, uses)
                 yield from named_barrier(epi_bar, uses + 1)
                 uses += 2

@@ -21,7 +21,9 @@ def test_indexer_protocol_completes_without_hazards():
         stages = rng.choice([2, 3, 4, 5, 8])
         hist = rng.random() < 0.5
         fp8 = rng.random() < 0.5
-        assert M.indexer(items, stages, trial, hist, fp8=fp8), (items, stages, hist, fp8)
+        # consecutive items of one query group (decode blocks) or all distinct (prefill)
+        groups = sorted(rng.randint(0, 2) for _ in items) if rng.random() < 0.5 else None
+        assert M.indexer(items, stages, trial, hist, fp8=fp8, groups=groups), (items, stages, hist, fp8, groups)
 
 
 @pytest.mark.parametrize("plant", ["qfree", "wfree", "sfree"])

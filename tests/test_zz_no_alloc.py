@@ -6,8 +6,9 @@ and outputs), and latency-bound code that must never reach cudaMalloc or
 cudaFree.  csa_attend_noalloc serves them: short key lists merge their split
 partials inside a thread-block cluster, and long ones (over 131072 keys per
 query) keep them in one fixed device array inside the library.  These tests call it through the C
-ABI and check it against csa_attend, which takes a workspace, with the
-attention tolerance |err| <= 1e-2 + 1e-2 |ref| used by every attention test.
+ABI and check it against csa_attend, which takes a workspace, and against the
+oracle on sampled queries, with the attention tolerance |err| <= 1e-2 +
+1e-2 |ref| used by every attention test.
 
 The file is named so that pytest collects it last: the shared device array
 keeps whatever the previous call left in it, so the GPU test also runs after
@@ -113,8 +114,21 @@ def test_noalloc_matches_workspace_attention_twice(L):
     cases = [case(21, 2, 150000, 139264, 128, 64, 128, 4 * 150000 - 1),
              case(22, 3, 140000, 135000, 64, 32, 64, 4 * 140000 - 1),
              case(23, 4, 65536, 1024, 128, 64, 128, 262143)]
+    import oracle as O
+    from tests._parity import bits
+
     for c in cases:
         ref_o, ref_l = run(c, noalloc=False)
         got_o, got_l = run(c, noalloc=True)
         assert_attention_close(got_o, ref_o.astype(np.float64), "noalloc vs workspace output")
         np.testing.assert_allclose(got_l, ref_l, rtol=1e-4, atol=1e-4)
+        # and against the oracle itself on the first and last query of the call
+        t = int(c["qp"][0, 0])
+        for b in (0, c["B"] - 1):
+            win = O.window_rows(t, c["W"], int(c["rb"][b]), c["T_raw"])
+            o, lse = O.attend_one(O.bf16_to_f64(bits(c["q"][b, 0])), O.bf16_to_f64(bits(c["kc"][b])),
+                                  O.bf16_to_f64(bits(c["vc"][b])), c["idx"][b, 0].cpu().numpy(),
+                                  O.bf16_to_f64(bits(c["kr"][b])), O.bf16_to_f64(bits(c["vr"][b])), win,
+                                  1 / np.sqrt(c["d"]))
+            assert_attention_close(got_o[b, 0], o, f"noalloc vs oracle, H={c['H']} d={c['d']} b={b}")
+            np.testing.assert_allclose(got_l[b, 0], lse, rtol=1e-4, atol=1e-4)
