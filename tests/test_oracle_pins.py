@@ -11,6 +11,17 @@ import torch
 from scipy.special import logsumexp
 
 import oracle as O
+from oracle import ref_cpp
+
+
+@pytest.fixture(scope="module", params=["numpy", "cpp"])
+def OC(request):
+    """The oracle under test: the numpy oracle, or the C++ oracle (same call
+    signatures).  Both are held to the same pins."""
+    if request.param == "cpp":
+        ref_cpp.build()
+        return ref_cpp
+    return O
 
 
 def _rows(s):
@@ -47,95 +58,95 @@ def test_round_bf16_ties_and_single_rounding():
 
 # ---------------------------------------------------------------- (1) compression
 
-def test_compress_golden_m2(golden_dir):
+def test_compress_golden_m2(OC, golden_dir):
     for ln in _load(golden_dir, "compress_m2.txt"):
         p = [s for s in ln.split("|")]
         x = np.array([[float(v) for v in p[0].split()], [float(v) for v in p[1].split()]])
         g = np.array([[float(v) for v in p[2].split()], [float(v) for v in p[3].split()]])
         want = np.array([float(v) for v in p[4].split()])
-        got = O.compress(x, g, 2)
+        got = OC.compress(x, g, 2)
         assert got.shape == (1, 2)
         np.testing.assert_allclose(got[0], want, rtol=0, atol=1e-14)
 
 
-def test_compress_invariants():
+def test_compress_invariants(OC):
     rng = np.random.default_rng(1)
     T, D, m = 64, 8, 4
     x = rng.standard_normal((T, D))
     g = rng.standard_normal((T, D)) * 3
-    base = O.compress(x, g, m)
+    base = OC.compress(x, g, m)
     # adding one constant per (block, channel) to the gates changes nothing
     shift = np.repeat(rng.standard_normal((T // m, D)) * 50, m, axis=0)
-    np.testing.assert_allclose(O.compress(x, g + shift, m), base, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(OC.compress(x, g + shift, m), base, rtol=1e-12, atol=1e-12)
     # a stream constant within each block is reproduced exactly
     c = np.repeat(rng.standard_normal((T // m, D)), m, axis=0)
-    np.testing.assert_allclose(O.compress(c, g, m), c[::m], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(OC.compress(c, g, m), c[::m], rtol=1e-13, atol=1e-13)
     # permuting tokens inside a block (with their gates) changes nothing
     perm = np.concatenate([b * m + rng.permutation(m) for b in range(T // m)])
-    np.testing.assert_allclose(O.compress(x[perm], g[perm], m), base, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(OC.compress(x[perm], g[perm], m), base, rtol=1e-12, atol=1e-12)
     # a convex combination: inside [min, max] of the block
     X = x.reshape(T // m, m, D)
     assert np.all(base <= X.max(axis=1) + 1e-12) and np.all(base >= X.min(axis=1) - 1e-12)
     # m = 1 is the identity
-    np.testing.assert_array_equal(O.compress(x, g, 1), x)
+    np.testing.assert_array_equal(OC.compress(x, g, 1), x)
     # a trailing partial block is dropped
-    assert O.compress(x[:T - 3], g[:T - 3], m).shape == (T // m - 1, D)
+    assert OC.compress(x[:T - 3], g[:T - 3], m).shape == (T // m - 1, D)
     # one dominant gate selects its token
     g2 = np.zeros((T, D))
     g2[2::m] = 800.0
-    np.testing.assert_allclose(O.compress(x, g2, m), x[2::m], rtol=0, atol=1e-300)
+    np.testing.assert_allclose(OC.compress(x, g2, m), x[2::m], rtol=0, atol=1e-300)
 
 
 # ---------------------------------------------------------------- visibility
 
 @pytest.mark.parametrize("m", [1, 2, 4, 128])
-def test_n_visible_boundaries(m):
+def test_n_visible_boundaries(OC, m):
     N = 10
     if m >= 2:
-        assert O.n_visible(m - 2, m, N) == 0      # first block not yet complete
-    assert O.n_visible(m - 1, m, N) == 1          # first block complete at t = m-1
-    assert O.n_visible(2 * m - 2, m, N) == 1      # second block one token short
-    assert O.n_visible(2 * m - 1, m, N) == 2
-    assert O.n_visible(100 * m, m, N) == N        # capped by the blocks that exist
-    assert O.n_visible(-1, m, N) == 0
+        assert OC.n_visible(m - 2, m, N) == 0      # first block not yet complete
+    assert OC.n_visible(m - 1, m, N) == 1          # first block complete at t = m-1
+    assert OC.n_visible(2 * m - 2, m, N) == 1      # second block one token short
+    assert OC.n_visible(2 * m - 1, m, N) == 2
+    assert OC.n_visible(100 * m, m, N) == N        # capped by the blocks that exist
+    assert OC.n_visible(-1, m, N) == 0
 
 
 # ---------------------------------------------------------------- (2)+(3) indexer, top-k
 
-def test_indexer_golden_and_tie(golden_dir):
+def test_indexer_golden_and_tie(OC, golden_dir):
     lines = _load(golden_dir, "indexer_tie.txt")
     kv = dict(ln.split("=", 1) for ln in lines if "=" in ln)
     w = np.array([float(v) for v in kv["w "].split()])
     q = _rows(kv["q "])
     keys = _rows(kv["keys "])
     want_scores = np.array([float(v) for v in kv["scores "].split()])
-    np.testing.assert_array_equal(O.indexer_scores(q, keys, w, t=100, m=1), want_scores)
+    np.testing.assert_array_equal(OC.indexer_scores(q, keys, w, t=100, m=1), want_scores)
     cases = [ln for ln in lines if "=" not in ln]
     assert len(cases) == 5
     for ln in cases:
         a, b = ln.split("|")
         m, t, k = (int(v) for v in a.split())
         want = np.array([int(v) for v in b.split()])
-        S = O.indexer_scores(q, keys, w, t=t, m=m)
-        np.testing.assert_array_equal(O.topk(S, k), want)
+        S = OC.indexer_scores(q, keys, w, t=t, m=m)
+        np.testing.assert_array_equal(OC.topk(S, k), want)
 
 
-def test_indexer_homogeneity_and_positive_closed_form():
+def test_indexer_homogeneity_and_positive_closed_form(OC):
     rng = np.random.default_rng(2)
     H, d, N = 6, 16, 40
     q = rng.standard_normal((H, d))
     k = rng.standard_normal((N, d))
     w = rng.uniform(0, 1, H)
-    S = O.indexer_scores(q, k, w, t=10 ** 6, m=1)
+    S = OC.indexer_scores(q, k, w, t=10 ** 6, m=1)
     # ReLU is positively homogeneous: scaling q by a > 0 scales S by a
-    np.testing.assert_allclose(O.indexer_scores(2.5 * q, k, w, 10 ** 6, 1), 2.5 * S, rtol=1e-13)
+    np.testing.assert_allclose(OC.indexer_scores(2.5 * q, k, w, 10 ** 6, 1), 2.5 * S, rtol=1e-13)
     # with non-negative q and k every ReLU is the identity, so
     # S[b] = (sum_h w_h q_h) . k_b  -- one dot product with the weighted query
     qp, kp = np.abs(q), np.abs(k)
     closed = np.array([np.dot(w @ qp, kp[b]) for b in range(N)])
-    np.testing.assert_allclose(O.indexer_scores(qp, kp, w, 10 ** 6, 1), closed, rtol=1e-13)
+    np.testing.assert_allclose(OC.indexer_scores(qp, kp, w, 10 ** 6, 1), closed, rtol=1e-13)
     # with non-positive dots every term vanishes
-    np.testing.assert_array_equal(O.indexer_scores(qp, -kp, w, 10 ** 6, 1), np.zeros(N))
+    np.testing.assert_array_equal(OC.indexer_scores(qp, -kp, w, 10 ** 6, 1), np.zeros(N))
 
 
 def _brute_topk(S, k):
@@ -149,17 +160,17 @@ def _brute_topk(S, k):
     return out
 
 
-def test_topk_brute_force_with_ties():
+def test_topk_brute_force_with_ties(OC):
     rng = np.random.default_rng(3)
     for trial in range(300):
         n = int(rng.integers(0, 9))
         k = int(rng.integers(1, 6))
         # small integer scores force many ties; halves keep sums exact
         S = rng.integers(0, 4, n).astype(np.float64) * 0.5
-        np.testing.assert_array_equal(O.topk(S, k), _brute_topk(S, k), err_msg=str((S, k)))
+        np.testing.assert_array_equal(OC.topk(S, k), _brute_topk(S, k), err_msg=str((S, k)))
 
 
-def test_topk_never_selects_future_blocks():
+def test_topk_never_selects_future_blocks(OC):
     rng = np.random.default_rng(4)
     H, d, N, m = 4, 8, 32, 4
     q = np.abs(rng.standard_normal((H, d)))
@@ -167,7 +178,7 @@ def test_topk_never_selects_future_blocks():
     k[N // 2:] *= 1000.0                     # future blocks score far higher
     w = np.ones(H)
     for t in range(0, N * m):
-        idx = O.topk(O.indexer_scores(q, k, w, t, m), 5)
+        idx = OC.topk(OC.indexer_scores(q, k, w, t, m), 5)
         sel = idx[idx >= 0]
         assert len(sel) == min(5, (t + 1) // m)
         assert np.all((sel + 1) * m - 1 <= t)
@@ -175,19 +186,19 @@ def test_topk_never_selects_future_blocks():
 
 # ---------------------------------------------------------------- (4) attention
 
-def test_attend_golden_two_keys(golden_dir):
+def test_attend_golden_two_keys(OC, golden_dir):
     kv = dict(ln.split("=", 1) for ln in _load(golden_dir, "attend_2key.txt"))
     q = np.array([[float(v) for v in kv["q "].split()]])
     K, V = _rows(kv["K "]), _rows(kv["V "])
-    out, lse = O.attend_one(q, K, V, [0, 1], K[:0], V[:0], np.arange(0), 1 / math.sqrt(2))
+    out, lse = OC.attend_one(q, K, V, [0, 1], K[:0], V[:0], np.arange(0), 1 / math.sqrt(2))
     np.testing.assert_allclose(out[0], [float(v) for v in kv["O "].split()], rtol=0, atol=1e-15)
     np.testing.assert_allclose(lse[0], float(kv["lse "]), rtol=0, atol=1e-15)
     # the same two keys reached through the window branch give the same result
-    out2, _ = O.attend_one(q, K[:0], V[:0], [], K, V, np.arange(2), 1 / math.sqrt(2))
+    out2, _ = OC.attend_one(q, K[:0], V[:0], [], K, V, np.arange(2), 1 / math.sqrt(2))
     np.testing.assert_allclose(out2, out, rtol=0, atol=1e-15)
 
 
-def test_attend_special_cases():
+def test_attend_special_cases(OC):
     rng = np.random.default_rng(5)
     H, d = 3, 8
     q = rng.standard_normal((H, d))
@@ -195,18 +206,18 @@ def test_attend_special_cases():
     V = rng.standard_normal((5, d))
     empty = np.arange(0)
     # one key -> its value
-    o1, l1 = O.attend_one(q, K, V, [3], K[:0], V[:0], empty, 0.3)
+    o1, l1 = OC.attend_one(q, K, V, [3], K[:0], V[:0], empty, 0.3)
     np.testing.assert_allclose(o1, np.repeat(V[3:4], H, 0), rtol=0, atol=1e-15)
     np.testing.assert_allclose(l1, 0.3 * q @ K[3], rtol=1e-14)
     # equal logits (q = 0) -> mean of the values
-    o2, l2 = O.attend_one(np.zeros((H, d)), K, V, [0, 1, 2, 3, 4], K[:0], V[:0], empty, 0.3)
+    o2, l2 = OC.attend_one(np.zeros((H, d)), K, V, [0, 1, 2, 3, 4], K[:0], V[:0], empty, 0.3)
     np.testing.assert_allclose(o2, np.repeat(V.mean(0, keepdims=True), H, 0), rtol=1e-13, atol=1e-15)
     np.testing.assert_allclose(l2, np.full(H, math.log(5)), rtol=1e-14)
     # -1 entries are skipped; no keys at all -> zeros and -inf
-    o3, l3 = O.attend_one(q, K, V, [-1, -1], K[:0], V[:0], empty, 0.3)
+    o3, l3 = OC.attend_one(q, K, V, [-1, -1], K[:0], V[:0], empty, 0.3)
     assert np.all(o3 == 0) and np.all(np.isneginf(l3))
     # lse agrees with scipy's logsumexp
-    _, l4 = O.attend_one(q, K, V, [4, 0, 2], K, V, np.array([1, 2]), 0.3)
+    _, l4 = OC.attend_one(q, K, V, [4, 0, 2], K, V, np.array([1, 2]), 0.3)
     keys = np.concatenate([K[[4, 0, 2]], K[[1, 2]]])
     np.testing.assert_allclose(l4, logsumexp(0.3 * q @ keys.T, axis=1), rtol=1e-14)
 
@@ -225,7 +236,7 @@ def _bits(x):
     return O.round_bf16(x)
 
 
-def test_csa_reduces_to_causal_attention_at_m1():
+def test_csa_reduces_to_causal_attention_at_m1(OC):
     """m = 1, k >= n_vis, W = 0: CSA is textbook causal softmax attention."""
     rng = np.random.default_rng(6)
     T, H, d, HI, dI = 24, 2, 8, 2, 4
@@ -242,7 +253,7 @@ def test_csa_reduces_to_causal_attention_at_m1():
     np.testing.assert_allclose(res["out"][0], ref, rtol=1e-12, atol=1e-12)
 
 
-def test_hca_is_block_causal_dense_attention_and_csa_agrees():
+def test_hca_is_block_causal_dense_attention_and_csa_agrees(OC):
     rng = np.random.default_rng(7)
     N, m, H, d, T = 12, 4, 2, 8, 48
     q = _bits(rng.standard_normal((1, T, H, d)))
@@ -251,7 +262,7 @@ def test_hca_is_block_causal_dense_attention_and_csa_agrees():
     kr = _bits(rng.standard_normal((1, T, d)))
     pos = np.arange(T)[None]
     base = np.zeros(1, np.int64)
-    o_h, _ = O.hca_attend(q, kc, vc, kr, kr, base, pos, m, 0, 0.3)
+    o_h, _ = OC.hca_attend(q, kc, vc, kr, kr, base, pos, m, 0, 0.3)
     # (b+1)*m - 1 <= t, written as a boolean table
     mask = np.array([[(b + 1) * m - 1 <= t for b in range(N)] for t in range(T)])
     rows = mask.any(1)
@@ -261,13 +272,13 @@ def test_hca_is_block_causal_dense_attention_and_csa_agrees():
     # CSA with every visible block selected equals HCA
     idx = np.full((1, T, N), -1)
     for t in range(T):
-        nv = O.n_visible(t, m, N)
+        nv = OC.n_visible(t, m, N)
         idx[0, t, :nv] = np.arange(nv)
-    o_c, _ = O.csa_attend(q, kc, vc, idx, kr, kr, base, pos, 0, 0.3)
+    o_c, _ = OC.csa_attend(q, kc, vc, idx, kr, kr, base, pos, 0, 0.3)
     np.testing.assert_allclose(o_c, o_h, rtol=0, atol=1e-15)
 
 
-def test_window_only_is_banded_attention():
+def test_window_only_is_banded_attention(OC):
     """n_vis = 0 (t < m-1 of a huge m) leaves the sliding window alone."""
     rng = np.random.default_rng(8)
     T, H, d, W = 20, 2, 8, 5
@@ -275,7 +286,7 @@ def test_window_only_is_banded_attention():
     kr = _bits(rng.standard_normal((1, T, d)))
     vr = _bits(rng.standard_normal((1, T, d)))
     kc = _bits(np.zeros((1, 0, d)))
-    o, _ = O.hca_attend(q, kc, kc, kr, vr, np.zeros(1, np.int64), np.arange(T)[None], 128, W, 0.4)
+    o, _ = OC.hca_attend(q, kc, kc, kr, vr, np.zeros(1, np.int64), np.arange(T)[None], 128, W, 0.4)
     mask = np.array([[t - W < u <= t for u in range(T)] for t in range(T)])
     ref = _sdpa(O.bf16_to_f64(q[0]), O.bf16_to_f64(kr[0]), O.bf16_to_f64(vr[0]), mask, 0.4)
     np.testing.assert_allclose(o[0], ref, rtol=1e-12, atol=1e-12)
@@ -292,7 +303,7 @@ def _rand_bf16(rng, shape):
     return O.round_bf16(rng.standard_normal(shape))
 
 
-def test_batched_wrappers_equal_each_sequence_alone():
+def test_batched_wrappers_equal_each_sequence_alone(OC):
     """B = 3 sequences with different inputs, positions and window offsets:
     every batched wrapper returns, for sequence b, exactly what it returns for
     that sequence alone (B = 1, itself pinned by the reductions above), and
@@ -315,24 +326,24 @@ def test_batched_wrappers_equal_each_sequence_alone():
             assert t - W + 1 >= raw_base[b] and t < raw_base[b] + T_raw
     scale = 0.3
 
-    kc = O.csa_compress(x, g, m)
-    ic = O.csa_compress(xi, gi, m)
+    kc = OC.csa_compress(x, g, m)
+    ic = OC.csa_compress(xi, gi, m)
     kcb, icb = O.round_bf16(kc), O.round_bf16(ic)
-    idx, S = O.csa_index_topk(qi, icb, w, q_pos, m, k)
-    Oc, Lc = O.csa_attend(q, kcb, kcb, idx, kr, vr, raw_base, q_pos, W, scale)
-    Oh, Lh = O.hca_attend(q, kcb, kcb, kr, vr, raw_base, q_pos, m, W, scale)
+    idx, S = OC.csa_index_topk(qi, icb, w, q_pos, m, k)
+    Oc, Lc = OC.csa_attend(q, kcb, kcb, idx, kr, vr, raw_base, q_pos, W, scale)
+    Oh, Lh = OC.hca_attend(q, kcb, kcb, kr, vr, raw_base, q_pos, m, W, scale)
     for b in range(B):
         one = slice(b, b + 1)
-        np.testing.assert_array_equal(kc[b], O.csa_compress(x[one], g[one], m)[0])
-        idx1, S1 = O.csa_index_topk(qi[one], icb[one], w, q_pos[one], m, k)
+        np.testing.assert_array_equal(kc[b], OC.csa_compress(x[one], g[one], m)[0])
+        idx1, S1 = OC.csa_index_topk(qi[one], icb[one], w, q_pos[one], m, k)
         np.testing.assert_array_equal(idx[b], idx1[0])
         for j in range(2):
             np.testing.assert_array_equal(S[b][j], S1[0][j])
-        o1, l1 = O.csa_attend(q[one], kcb[one], kcb[one], idx[one], kr[one], vr[one], raw_base[one],
+        o1, l1 = OC.csa_attend(q[one], kcb[one], kcb[one], idx[one], kr[one], vr[one], raw_base[one],
                               q_pos[one], W, scale)
         np.testing.assert_array_equal(Oc[b], o1[0])
         np.testing.assert_array_equal(Lc[b], l1[0])
-        o1, l1 = O.hca_attend(q[one], kcb[one], kcb[one], kr[one], vr[one], raw_base[one], q_pos[one], m, W,
+        o1, l1 = OC.hca_attend(q[one], kcb[one], kcb[one], kr[one], vr[one], raw_base[one], q_pos[one], m, W,
                               scale)
         np.testing.assert_array_equal(Oh[b], o1[0])
         np.testing.assert_array_equal(Lh[b], l1[0])
@@ -342,7 +353,7 @@ def test_batched_wrappers_equal_each_sequence_alone():
     # output of query (1, 1) changes when only sequence 1's window rows change
     vr2 = vr.copy()
     vr2[1] = _rand_bf16(rng, (T_raw, d))
-    Oh2, _ = O.hca_attend(q, kcb, kcb, kr, vr2, raw_base, q_pos, m, W, scale)
+    Oh2, _ = OC.hca_attend(q, kcb, kcb, kr, vr2, raw_base, q_pos, m, W, scale)
     assert not np.array_equal(Oh2[1], Oh[1])
     np.testing.assert_array_equal(Oh2[0], Oh[0])
     np.testing.assert_array_equal(Oh2[2], Oh[2])
