@@ -137,13 +137,28 @@ __device__ __forceinline__ int rank_of(int k, const KParams& p) {
 
 __device__ __forceinline__ bool same_group(const Item& a, const Item& b) { return a.b == b.b && a.j0 == b.j0; }
 
-// The first item with visible tiles after this CTA's k-th item (false: none).
-__device__ __forceinline__ bool next_item(const KParams& p, int k, Item* J) {
-  for (int kk = k + 1;; ++kk) {
+// A CTA's walk over its items with visible tiles: k is the current item's
+// index in the CTA's list (-1: no more).  The first one is found before the
+// warp roles split, so no role waits on a fresh global read before its first
+// copy or MMA; each later one is fetched once the current item's work is
+// issued.
+struct Cursor {
+  int k;
+  Item I;
+};
+__device__ __forceinline__ bool advance(const KParams& p, Cursor& c) {
+  for (int kk = c.k + 1;; ++kk) {
     const int r = rank_of(kk, p);
-    if (r < 0) return false;
-    *J = item_of(p, r);
-    if (J->ntile > 0) return true;
+    if (r < 0) {
+      c.k = -1;
+      return false;
+    }
+    const Item J = item_of(p, r);
+    if (J.ntile > 0) {
+      c.k = kk;
+      c.I = J;
+      return true;
+    }
   }
 }
 
@@ -210,13 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->qfree, 1);
     mbar_fence_init();
   }
-  // does this CTA own any visible tile? (the same answer in every thread)
-  bool any = false;
-  for (int k = 0; !any; ++k) {
-    const int r = rank_of(k, p);
-    if (r < 0) break;
-    any = item_of(p, r).ntile > 0;
-  }
+  // this CTA's first item with visible tiles (the same answer in every
+  // thread; none: nothing to do)
+  Cursor first;
+  first.k = -1;
+  const bool any = advance(p, first);
   __syncthreads();
   if (!any) return;
 
@@ -244,10 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t key_policy = l2_policy_evict_first();
       int gt = 0;  // key tiles issued
       bool ok = true;
-      for (int k = 0; ok; ++k) {
-        const int r = rank_of(k, p);
-        if (r < 0) break;
-        const Item I = item_of(p, r);
+      for (Cursor c = first; ok && c.k >= 0; advance(p, c)) {
+        const Item& I = c.I;
         for (int i = 0; i < I.ntile; ++i) {
           const int s = gt % p.stages;
           const uint32_t ph = (gt / p.stages) & 1;
@@ -279,11 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int gt = 0, nq = 0;
       bool ok = true;
       Item prev{-1, -1, 0, 0};
-      for (int k = 0; ok; ++k) {
-        const int r = rank_of(k, p);
-        if (r < 0) break;
-        const Item I = item_of(p, r);
-        if (I.ntile <= 0) continue;
+      for (Cursor c = first; ok && c.k >= 0; advance(p, c)) {
+        const Item I = c.I;
         if (nq == 0 || !same_group(I, prev)) {
           // a new query group: the query buffer may be refilled once the
           // previous group's MMAs are done, and this group's rows must be in
@@ -334,11 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) tma_prefetch_desc(&tmq);
     int it = 0, nq = 0;
     Item prev{-1, -1, 0, 0};
-    for (int k = 0;; ++k) {
-      const int r = rank_of(k, p);
-      if (r < 0) break;
-      const Item I = item_of(p, r);
-      if (I.ntile <= 0) continue;
+    for (Cursor c = first; c.k >= 0; advance(p, c)) {
+      const Item I = c.I;
       const int ib = it & 1;
       const bool new_group = nq == 0 || !same_group(I, prev);
       prev = I;
@@ -351,9 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int qrow = (I.b * p.Tq + I.j0) * HI;
           for (int h = 0; h < p.kh; ++h) tma_load_2d(qs + h * p.NC * 128, &tmq, &bars->qfull, h * 64, qrow);
           // the next item's query rows into L2 while this item runs
-          const int rn = rank_of(k + 1, p);
-          if (rn >= 0) {
-            const Item J = item_of(p, rn);
+          Cursor nx = c;
+          if (advance(p, nx)) {
+            const Item& J = nx.I;
             const int jn = min(p.G, p.Tq - J.j0);
             const uint32_t bytes = static_cast<uint32_t>(jn * HI * p.q_row_bytes);
             const char* src = static_cast<const char*>(p.q_base) +
@@ -405,11 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t col0 = lane_addr + static_cast<uint32_t>(egroup * p.NC);
     int gt = 0, it = 0;
     bool waited_zero = false;
-    for (int k = 0;; ++k) {
-      const int r = rank_of(k, p);
-      if (r < 0) break;
-      const Item I = item_of(p, r);
-      if (I.ntile <= 0) continue;
+    for (Cursor c = first; c.k >= 0; advance(p, c)) {
+      const Item I = c.I;
       const int ib = it & 1;
       bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->wfull[ib], (it >> 1) & 1, p.budget, abort_v));
       if (!ok && lane == 0) fail();
@@ -493,8 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this group is done with the item's weights and visibility
       group_bar(egroup);
       if ((ew & 3) == 0 && lane == 0) mbar_arrive(&bars->wfree[ib]);
-      Item J;
-      if (p.hist && !(next_item(p, k, &J) && same_group(I, J))) {
+      Cursor nx = c;
+      if (p.hist && !(advance(p, nx) && same_group(I, nx.I))) {
         // both groups' counts of the query group are in: flush them (once
         // the histogram has been zeroed), then clear for the next group
         epi_bar();
