@@ -11,11 +11,12 @@
 //  1. CTA r scans its chunk [r*E, (r+1)*E) of the scores and keeps, in index
 //     order, every key whose bucket is >= beta, the bucket holding the k-th
 //     largest key (one float comparison per score against the bucket's
-//     lowest value; candidates in global memory);
+//     lowest value; candidates in global memory); the keys of bucket beta
+//     count into a second-level histogram of key bits 19..8;
 //  2. every CTA stages all ranks' candidates in shared memory (when they fit)
-//     and fixes the same exact rule (prefix, mask, k_rem) among the keys of
-//     bucket beta by up to three 8-bit digit passes: keys above the prefix
-//     are kept, and of the keys equal to it the k_rem with the lowest indices;
+//     and fixes the same exact rule (prefix, mask, k_rem) from that histogram
+//     and at most one 8-bit pass: keys above the prefix are kept, and of the
+//     keys equal to it the k_rem with the lowest indices;
 //  3. each CTA counts its kept candidates, learns the counts of the CTAs
 //     before it, and so the rank of each kept block in ascending order; it
 //     writes idx_out and sends (rank -> block) to the CTA that attends that
@@ -198,23 +199,28 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
   }
 
   // ---- 1. candidates of this CTA's chunk (keys in bucket beta or above), in
-  // index order
+  // index order; the keys of bucket beta also count into the second-level
+  // histogram (key bits 19..8)
   uint32_t n_own = 0;
   if (!all) {
     const uint32_t beta = static_cast<uint32_t>(b1.beta);
     uint2* gl = gl_all + static_cast<long long>(r) * E;
-    // the lowest score of bucket beta: the key map is order-preserving (and
-    // folds -0 onto +0, as the float comparison does), so a score is a
-    // candidate iff it compares >= this value (bucket 0 holds no finite
-    // lowest value: every score is a candidate then)
+    uint32_t* hist2 = a.hist2 + q * kTopkBins;
+    // the lowest scores of buckets beta and beta + 1: the key map is
+    // order-preserving (and folds -0 onto +0, as the float comparison does),
+    // so a score is a candidate iff it compares >= tb and in bucket beta iff
+    // also < tb1 (bucket 0 holds no finite lowest value: every score is a
+    // candidate then; above the top bucket nothing is)
     const float tb = beta == 0 ? -INFINITY : key_score(beta << 20);
+    const float tb1 = beta >= kTopkBins - 1 ? INFINITY : key_score((beta + 1) << 20);
     for (int sub = lo; sub < hi; sub += kT * kRun) {
       if (sub != lo) issue_batch(sub);  // the first batch was requested before the bucket search
       bulk_wait();
       // warp w owns the contiguous segment [w*SEG, (w+1)*SEG) of the batch and
       // reads it as one float4 per lane (128 consecutive scores per step:
-      // conflict-free); pass 1 counts its candidates, pass 2 writes them in
-      // index order after a scan over the warps' counts
+      // conflict-free); pass 1 counts its candidates and feeds bucket beta's
+      // keys into the second-level histogram, pass 2 writes the candidates
+      // in index order after a scan over the warps' counts
       constexpr int NWS = kT / 32, SEG = kT * kRun / NWS;
       const int nb = min(kT * kRun, hi - sub);
       const int s_lo = warp * SEG, s_hi = min(nb, s_lo + SEG);
@@ -222,8 +228,14 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
       for (int base = s_lo; base < s_hi; base += 128) {
         const int i = base + 4 * lane;
         const float4 fv = *reinterpret_cast<const float4*>(stage + i);
-        wcount += (i < s_hi && fv.x >= tb) + (i + 1 < s_hi && fv.y >= tb) + (i + 2 < s_hi && fv.z >= tb) +
-                  (i + 3 < s_hi && fv.w >= tb);
+        const float v4[4] = {fv.x, fv.y, fv.z, fv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const bool c = i + e < s_hi && v4[e] >= tb;
+          wcount += c ? 1u : 0u;
+          // bucket beta holds about k of the keys: one reduction per key of it
+          if (c && v4[e] < tb1) atomicAdd(hist2 + ((score_key(v4[e]) >> 8) & (kTopkBins - 1)), 1u);
+        }
       }
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) wcount += __shfl_xor_sync(0xffffffffu, wcount, o);
@@ -236,27 +248,24 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
         for (int w = 0; w < NWS; ++w) t += tmp[w];
         tot32 = t;
       }
+      const unsigned ltm = lanemask_lt();
       for (int base = s_lo; base < s_hi; base += 128) {
         const int i = base + 4 * lane;
         const float4 fv = *reinterpret_cast<const float4*>(stage + i);
         const float v4[4] = {fv.x, fv.y, fv.z, fv.w};
-        uint32_t mine = 0;
+        // candidates in index order: lane by lane, and within a lane element
+        // by element; one ballot per element position
+        unsigned bal[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) mine |= (i + e < s_hi && v4[e] >= tb) ? (1u << e) : 0u;
-        if (__ballot_sync(0xffffffffu, mine != 0u) == 0u) continue;
-        // candidates of the lanes before this one, then this lane's in order
-        const uint32_t c = static_cast<uint32_t>(__popc(mine));
-        uint32_t incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += n;
-        }
-        uint32_t at = pos + incl - c;
+        for (int e = 0; e < 4; ++e) bal[e] = __ballot_sync(0xffffffffu, i + e < s_hi && v4[e] >= tb);
+        const unsigned any4 = bal[0] | bal[1] | bal[2] | bal[3];
+        if (any4 == 0u) continue;
+        uint32_t at = pos + __popc(bal[0] & ltm) + __popc(bal[1] & ltm) + __popc(bal[2] & ltm) +
+                      __popc(bal[3] & ltm);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (mine & (1u << e)) gl[at++] = make_uint2(score_key(v4[e]), static_cast<uint32_t>(sub + i + e));
-        pos += __shfl_sync(0xffffffffu, incl, 31);
+          if ((bal[e] >> lane) & 1u) gl[at++] = make_uint2(score_key(v4[e]), static_cast<uint32_t>(sub + i + e));
+        pos += __popc(bal[0]) + __popc(bal[1]) + __popc(bal[2]) + __popc(bal[3]);
       }
       __syncthreads();  // tot32 written; tmp read
       n_own += tot32;
@@ -297,32 +306,34 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
       for (int i = 0; i < kC; ++i)
         if (rcnt[i]) bulk_g2s(lists + i * kCandR, gl_all + static_cast<long long>(i) * E, (rcnt[i] + 1) / 2 * 16, &bar);
     }
-    // the exact rule: keys above bucket beta are kept, and of the bucket's
-    // keys the k - above largest (equal keys: the lowest indices); found
-    // among the staged candidates by digit passes over key bits 19..12,
-    // 11..4 and 3..0 (the last pass re-reads bits 7..4, already fixed), each
-    // a 256-bin histogram of the keys that match the rule so far
-    const uint32_t k_b = static_cast<uint32_t>(k) - b1.above;
-    Rule rl{static_cast<uint32_t>(b1.beta) << 20, 0xFFF00000u, k_b, b1.hb == k_b ? 1u : 0u};
+    // the rule's top 24 bits from the second-level histogram while the lists
+    // arrive; keys above the prefix are kept, and of the keys equal to it the
+    // k_rem with the lowest indices
+    const uint32_t beta = static_cast<uint32_t>(b1.beta);
+    const uint32_t k2 = static_cast<uint32_t>(k) - b1.above;
+    const Bucket b2 = find_bucket<kT>(a.hist2 + q * kTopkBins, k2, tmp, &sb);
+    Rule rl{(beta << 20) | (static_cast<uint32_t>(b2.beta) << 8), 0xFFFFFF00u, k2 - b2.above, 0u};
+    rl.done = (b2.beta >= 0 && b2.hb == rl.k_rem) ? 1u : 0u;
     if (staged) bulk_wait();
     // candidate c of rank i
     auto cand_at = [&](int i, int c) -> uint2 {
       return staged ? lists[i * kCandR + c] : gl_all[static_cast<long long>(i) * E + c];
     };
-    __shared__ uint32_t hbin[256];
-    for (int pass = 0; pass < 3 && !rl.done; ++pass) {
-      const int shift = pass == 0 ? 12 : (pass == 1 ? 4 : 0);
+    if (!rl.done) {
+      // the last 8 bits among the keys with this 24-bit prefix (few keys)
+      __shared__ uint32_t hbin[256];
       if (tid < 256) hbin[tid] = 0u;
+      if (tid == 0) rule = rl;
       __syncthreads();
       for (int i = 0; i < kC; ++i) {
         const int n = static_cast<int>(rcnt[i]);
         for (int c = tid; c < n; c += kT) {
           const uint32_t key = cand_at(i, c).x;
-          if ((key & rl.mask) == rl.prefix) atomicAdd(&hbin[(key >> shift) & 255u], 1u);
+          if ((key & rl.mask) == rl.prefix) atomicAdd(&hbin[key & 255u], 1u);
         }
       }
       __syncthreads();
-      pick_digit<kT>(hbin, rl, shift, tmp, &rule);
+      pick_digit<kT>(hbin, rl, 0, tmp, &rule);
       rl = rule;
       __syncthreads();
     }

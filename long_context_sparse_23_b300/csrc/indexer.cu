@@ -146,6 +146,9 @@ struct Cursor {
   int k;
   Item I;
 };
+// Consecutive items of one query group whose tile ranges adjoin (a decode
+// CTA's contiguous block) are taken as one run, so the roles meet at item
+// boundaries only where the query group changes.
 __device__ __forceinline__ bool advance(const KParams& p, Cursor& c) {
   for (int kk = c.k + 1;; ++kk) {
     const int r = rank_of(kk, p);
@@ -153,8 +156,16 @@ __device__ __forceinline__ bool advance(const KParams& p, Cursor& c) {
       c.k = -1;
       return false;
     }
-    const Item J = item_of(p, r);
+    Item J = item_of(p, r);
     if (J.ntile > 0) {
+      for (;;) {
+        const int rn = rank_of(kk + 1, p);
+        if (rn < 0) break;
+        const Item Jn = item_of(p, rn);
+        if (!same_group(J, Jn) || Jn.tile_lo != J.tile_lo + J.ntile || Jn.ntile <= 0) break;
+        J.ntile += Jn.ntile;
+        ++kk;
+      }
       c.k = kk;
       c.I = J;
       return true;
@@ -233,14 +244,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (!any) return;
 
-  if (warp == 1) {
-    tmem_alloc(&tmem_base, p.tmem_cols);
-    tmem_relinquish();
+  // the TMEM address reaches the MMA and epilogue warps over a named barrier;
+  // the two producer warps need no TMEM and start copying at once
+  uint32_t tbase = 0;
+  if (warp != 0 && warp != 2) {
+    if (warp == 1) {
+      tmem_alloc(&tmem_base, p.tmem_cols);
+      tmem_relinquish();
+    }
+    tc_fence_before();
+    asm volatile("bar.sync 4, %0;" ::"r"(kThreads - 64) : "memory");
+    tc_fence_after();
+    tbase = tmem_base;
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = tmem_base;
   volatile int* abort_v = &abort_flag;
   auto fail = [&]() {
     if (!*abort_v) raise_flag(p.errw, kFlagTimeout);
