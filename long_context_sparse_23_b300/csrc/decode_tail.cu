@@ -94,6 +94,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Bulk prefetch of ``bytes`` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // KH: keys per warp per tile step (the half of S_r a warp attends is walked
 // in steps of KH keys; KH = S_r / 2 makes it one step).
 template <int D, int KH>
@@ -162,6 +167,8 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
   char* Vs = Ks + S_r * D * 2;
   const char* kc_base = static_cast<const char*>(at.k_cmp) + static_cast<size_t>(b) * at.N * D * 2;
   const char* vc_base = static_cast<const char*>(at.v_cmp) + static_cast<size_t>(b) * at.N * D * 2;
+  const char* kr_base = static_cast<const char*>(at.k_raw) + static_cast<size_t>(b) * at.T_raw * D * 2;
+  const char* vr_base = static_cast<const char*>(at.v_raw) + static_cast<size_t>(b) * at.T_raw * D * 2;
   auto gather_row = [&](int j, int row_c) {  // one lane copies compressed row row_c into slot j
 #pragma unroll
     for (int ch = 0; ch < CH; ++ch) {
@@ -169,6 +176,23 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
       cp_async16(Vs + swz<D>(j, ch), vc_base + static_cast<size_t>(row_c) * D * 2 + ch * 16, true);
     }
   };
+  // the window slots [k, k + W) of this CTA's range do not depend on the
+  // selection: their rows are requested now (rows outside the buffer or
+  // before token 0 are zero-filled; step 3 reports them)
+  const int win_lo = r < A ? max(r * S_r, k) : 0;
+  const int win_hi = r < A ? min((r + 1) * S_r, K_total) : 0;
+  if (win_lo < win_hi) {
+    const int raw_base = at.raw_base[b];
+    for (int i = tid; i < (win_hi - win_lo) * CH; i += kT) {
+      const int sl = win_lo + i / CH, ch = i % CH, rw = sl - r * S_r;
+      const int u = t - at.W + 1 + (sl - k);
+      const int rr = u - raw_base;
+      const bool valid = u >= 0 && rr >= 0 && rr < at.T_raw;
+      cp_async16(Ks + swz<D>(rw, ch), valid ? kr_base + static_cast<size_t>(rr) * D * 2 + ch * 16 : kc_base, valid);
+      cp_async16(Vs + swz<D>(rw, ch), valid ? vr_base + static_cast<size_t>(rr) * D * 2 + ch * 16 : vc_base, valid);
+    }
+    cp_async_commit();
+  }
 
   // the scores of this CTA's first batch to shared memory by bulk copy
   // (rounded up to 4 scores: the row holds ld >= N, a multiple of 4), issued
@@ -194,6 +218,7 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
       if (r == 0 && tid == 0) raise_flag(at.errw, kFlagIndex);
       if (r < A) mbar_wait(&bar_q, 0, kDrainBudget, nullptr);
       if (lo < hi) mbar_wait(&bar, 0, kDrainBudget, nullptr);
+      cp_async_wait<0>();  // the window rows requested at the start
       return;
     }
   }
@@ -264,7 +289,14 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
                       __popc(bal[3] & ltm);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if ((bal[e] >> lane) & 1u) gl[at++] = make_uint2(score_key(v4[e]), static_cast<uint32_t>(sub + i + e));
+          if ((bal[e] >> lane) & 1u) {
+            const uint32_t row_c = static_cast<uint32_t>(sub + i + e);
+            gl[at++] = make_uint2(score_key(v4[e]), row_c);
+            // the candidate's K and V rows into L2: the kept ones are
+            // gathered after the ranking and then come from L2
+            bulk_prefetch_l2(kc_base + static_cast<size_t>(row_c) * D * 2, D * 2);
+            bulk_prefetch_l2(vc_base + static_cast<size_t>(row_c) * D * 2, D * 2);
+          }
         pos += __popc(bal[0]) + __popc(bal[1]) + __popc(bal[2]) + __popc(bal[3]);
       }
       __syncthreads();  // tot32 written; tmp read
@@ -422,11 +454,10 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     }
     if (bad) raise_flag(at.errw, kFlagIndex);
     __syncthreads();
-    const char* kr_base = static_cast<const char*>(at.k_raw) + static_cast<size_t>(b) * at.T_raw * D * 2;
-    const char* vr_base = static_cast<const char*>(at.v_raw) + static_cast<size_t>(b) * at.T_raw * D * 2;
     for (int i = tid; i < S_r * CH; i += kT) {
       const int rw = i / CH, ch = i % CH;
-      if (!all && s0 + rw < k) continue;  // requested in step 2
+      if (!all && s0 + rw < k) continue;                 // requested in step 2
+      if (s0 + rw >= win_lo && s0 + rw < win_hi) continue;  // requested at the start
       const int code = codes[rw];
       const char* kp = code >= 0 ? kc_base + static_cast<size_t>(code) * D * 2
                                  : kr_base + static_cast<size_t>(code <= -2 ? -code - 2 : 0) * D * 2;
