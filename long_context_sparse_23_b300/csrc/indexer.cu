@@ -9,16 +9,19 @@
 // 128-key tile = the 128 TMEM lanes) and (query, head) pairs on N (a group of
 // G queries x H_I heads, N <= 256 columns), K = d_I.  So every epilogue thread
 // owns one key row and reduces sum_h w_h * max(acc, 0) over its own TMEM
-// columns -- no cross-thread reduction.  Warp roles per CTA (320 threads):
-//   warp 0     TMA producer: the query group once, then key tiles into an
-//              S-stage shared-memory ring (128-byte swizzle, OOB rows zero);
-//   warp 1     allocates TMEM; one lane issues tcgen05.mma (kind::f16, bf16
-//              operands, fp32 accumulators) into two TMEM accumulator buffers;
-//   warps 2-9  epilogue, two groups of four alternating tiles (group e owns
-//              TMEM accumulator buffer e): tcgen05.ld the tile's accumulators,
-//              apply ReLU and the head weights, store fp32 scores (one
-//              coalesced row per warp) and count them into the top-k bucket
-//              histogram.
+// columns -- no cross-thread reduction.  A work item is one query group
+// against a range of 128-key tiles; TMA feeds a 128-byte-swizzled shared-
+// memory ring of key tiles, one thread issues tcgen05.mma into two TMEM
+// accumulators, and two groups of four epilogue warps take alternate tiles
+// (tcgen05.ld, ReLU and the head weights, coalesced fp32 scores, the top-k
+// bucket histogram).  Two kernels:
+//   indexer_single_kernel  decode (one query group per sequence): one item
+//                          per CTA, the query rows and key tiles issued by one
+//                          producer thread at once;
+//   indexer_kernel         prefill (query groups of every causal length):
+//                          persistent, one CTA per SM walking its items
+//                          (heavy first, snake order), an item producer warp
+//                          loading each item's weights and query rows.
 // mbarriers connect the stages (full/empty per smem stage, full/empty per
 // TMEM buffer); every wait is bounded and reports CSA_FLAG_TIMEOUT instead of
 // hanging.  Tiles past the group's last visible block are never loaded.
@@ -54,7 +57,6 @@ struct KParams {
   int items_per_group;
   int tiles_per_item;
   int items;          // B * n_groups * items_per_group
-  int per_cta;        // > 0: CTA c owns the contiguous ranks [c * per_cta, (c + 1) * per_cta)
   int tmem_cols;
   uint32_t* errw;
   long long budget;
@@ -70,8 +72,8 @@ struct __align__(8) Bars {
   uint64_t empty[8];   // key stage consumed by the MMAs
   uint64_t tfull[2];   // accumulator buffer written by the MMAs
   uint64_t tempty[2];  // accumulator buffer read by its epilogue group
-  uint64_t qfull;      // a query group's rows loaded (one phase per load)
-  uint64_t qfree;      // a query group's MMAs done: the query buffer may be refilled
+  uint64_t qfull;      // the item's queries loaded
+  uint64_t qfree;      // the item's MMAs done: the query buffer may be refilled
   uint64_t wfull[2];   // head weights / visibility of an item written
   uint64_t wfree[2];   // both epilogue groups are done with an item's weights
   uint64_t sfree[8];   // FP8: the key scales of a stage read by the epilogue
@@ -117,60 +119,13 @@ __device__ __forceinline__ int tile_at(const Item& I, int i) {
   return I.tile_lo + (j >= I.ntile ? j - I.ntile : j);
 }
 
-// Rank of this CTA's k-th item, or -1.  Items of unequal weight (prefill:
-// causal rows of every length) go in rounds of gridDim.x ranks taken in
+// Rank of this CTA's k-th item, or -1: rounds of gridDim.x ranks, taken in
 // alternating direction (snake order), so every CTA gets a similar share of
-// heavy and light items; items of equal weight (decode: one query group per
-// sequence) go in contiguous blocks, so a CTA's consecutive items share
-// their query rows and histogram.
+// heavy and light items.
 __device__ __forceinline__ int rank_of(int k, const KParams& p) {
   const int n = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-  long long r;
-  if (p.per_cta > 0) {
-    if (k >= p.per_cta) return -1;
-    r = static_cast<long long>(c) * p.per_cta + k;
-  } else {
-    r = static_cast<long long>(k) * n + ((k & 1) ? n - 1 - c : c);
-  }
+  const long long r = static_cast<long long>(k) * n + ((k & 1) ? n - 1 - c : c);
   return r < p.items ? static_cast<int>(r) : -1;
-}
-
-__device__ __forceinline__ bool same_group(const Item& a, const Item& b) { return a.b == b.b && a.j0 == b.j0; }
-
-// A CTA's walk over its items with visible tiles: k is the current item's
-// index in the CTA's list (-1: no more).  The first one is found before the
-// warp roles split, so no role waits on a fresh global read before its first
-// copy or MMA; each later one is fetched once the current item's work is
-// issued.
-struct Cursor {
-  int k;
-  Item I;
-};
-// Consecutive items of one query group whose tile ranges adjoin (a decode
-// CTA's contiguous block) are taken as one run, so the roles meet at item
-// boundaries only where the query group changes.
-__device__ __forceinline__ bool advance(const KParams& p, Cursor& c) {
-  for (int kk = c.k + 1;; ++kk) {
-    const int r = rank_of(kk, p);
-    if (r < 0) {
-      c.k = -1;
-      return false;
-    }
-    Item J = item_of(p, r);
-    if (J.ntile > 0) {
-      for (;;) {
-        const int rn = rank_of(kk + 1, p);
-        if (rn < 0) break;
-        const Item Jn = item_of(p, rn);
-        if (!same_group(J, Jn) || Jn.tile_lo != J.tile_lo + J.ntile || Jn.ntile <= 0) break;
-        J.ntile += Jn.ntile;
-        ++kk;
-      }
-      c.k = kk;
-      c.I = J;
-      return true;
-    }
-  }
 }
 
 __device__ __forceinline__ void group_bar(int g) {
@@ -236,27 +191,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->qfree, 1);
     mbar_fence_init();
   }
-  // this CTA's first item with visible tiles (the same answer in every
-  // thread; none: nothing to do)
-  Cursor first;
-  first.k = -1;
-  const bool any = advance(p, first);
+  // does this CTA own any visible tile? (the same answer in every thread)
+  bool any = false;
+  for (int k = 0; !any; ++k) {
+    const int r = rank_of(k, p);
+    if (r < 0) break;
+    any = item_of(p, r).ntile > 0;
+  }
   __syncthreads();
   if (!any) return;
 
-  // the TMEM address reaches the MMA and epilogue warps over a named barrier;
-  // the two producer warps need no TMEM and start copying at once
-  uint32_t tbase = 0;
-  if (warp != 0 && warp != 2) {
-    if (warp == 1) {
-      tmem_alloc(&tmem_base, p.tmem_cols);
-      tmem_relinquish();
-    }
-    tc_fence_before();
-    asm volatile("bar.sync 4, %0;" ::"r"(kThreads - 64) : "memory");
-    tc_fence_after();
-    tbase = tmem_base;
+  if (warp == 1) {
+    tmem_alloc(&tmem_base, p.tmem_cols);
+    tmem_relinquish();
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base;
   volatile int* abort_v = &abort_flag;
   auto fail = [&]() {
     if (!*abort_v) raise_flag(p.errw, kFlagTimeout);
@@ -273,8 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t key_policy = l2_policy_evict_first();
       int gt = 0;  // key tiles issued
       bool ok = true;
-      for (Cursor c = first; ok && c.k >= 0; advance(p, c)) {
-        const Item& I = c.I;
+      for (int k = 0; ok; ++k) {
+        const int r = rank_of(k, p);
+        if (r < 0) break;
+        const Item I = item_of(p, r);
         for (int i = 0; i < I.ntile; ++i) {
           const int s = gt % p.stages;
           const uint32_t ph = (gt / p.stages) & 1;
@@ -303,22 +257,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = F8 ? idesc_e4m3_f32(128, p.NC) : idesc_bf16_f32(128, p.NC);
-      int gt = 0, nq = 0;
+      int gt = 0, it = 0;
       bool ok = true;
-      Item prev{-1, -1, 0, 0};
-      for (Cursor c = first; ok && c.k >= 0; advance(p, c)) {
-        const Item I = c.I;
-        if (nq == 0 || !same_group(I, prev)) {
-          // a new query group: the query buffer may be refilled once the
-          // previous group's MMAs are done, and this group's rows must be in
-          if (nq > 0) umma_commit(&bars->qfree);
-          if (!mbar_wait(&bars->qfull, nq & 1, p.budget, abort_v)) {
-            fail();
-            break;
-          }
-          ++nq;
+      for (int k = 0; ok; ++k) {
+        const int r = rank_of(k, p);
+        if (r < 0) break;
+        const Item I = item_of(p, r);
+        if (I.ntile <= 0) continue;
+        if (!mbar_wait(&bars->qfull, it & 1, p.budget, abort_v)) {
+          fail();
+          break;
         }
-        prev = I;
         for (int i = 0; i < I.ntile; ++i) {
           const int s = gt % p.stages;
           const uint32_t ph = (gt / p.stages) & 1;
@@ -348,6 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++gt;
         }
         if (!ok) break;
+        umma_commit(&bars->qfree);  // the query buffer is free once this item's MMAs are done
+        ++it;
       }
       // drain: the last MMAs have finished reading shared memory / writing TMEM
       if (gt > 0) mbar_wait(&bars->tfull[(gt - 1) & 1], ((gt - 1) >> 1) & 1, kDrainBudget, nullptr);
@@ -356,42 +307,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- item producer: query rows first (the MMAs wait for them), then the
     // head weights and visibility the epilogue needs
     if (lane == 0) tma_prefetch_desc(&tmq);
-    int it = 0, nq = 0;
-    Item prev{-1, -1, 0, 0};
-    for (Cursor c = first; c.k >= 0; advance(p, c)) {
-      const Item I = c.I;
+    int it = 0, q_issued = 0;
+    for (int k = 0;; ++k) {
+      const int r = rank_of(k, p);
+      if (r < 0) break;
+      const Item I = item_of(p, r);
+      if (I.ntile <= 0) continue;
       const int ib = it & 1;
-      const bool new_group = nq == 0 || !same_group(I, prev);
-      prev = I;
       bool ok = true;
-      if (lane == 0 && new_group) {
-        // the query rows, once the MMAs of the previous query group are done
-        ok = nq == 0 || mbar_wait(&bars->qfree, (nq - 1) & 1, p.budget, abort_v);
+      if (lane == 0) {
+        // the query rows, once the MMAs of the previous item are done
+        ok = it == 0 || mbar_wait(&bars->qfree, (it - 1) & 1, p.budget, abort_v);
         if (ok) {
           mbar_expect_tx(&bars->qfull, p.kh * p.NC * 128);
           const int qrow = (I.b * p.Tq + I.j0) * HI;
           for (int h = 0; h < p.kh; ++h) tma_load_2d(qs + h * p.NC * 128, &tmq, &bars->qfull, h * 64, qrow);
+          q_issued = it + 1;
           // the next item's query rows into L2 while this item runs
-          Cursor nx = c;
-          if (advance(p, nx)) {
-            const Item& J = nx.I;
+          const int rn = rank_of(k + 1, p);
+          if (rn >= 0) {
+            const Item J = item_of(p, rn);
             const int jn = min(p.G, p.Tq - J.j0);
             const uint32_t bytes = static_cast<uint32_t>(jn * HI * p.q_row_bytes);
             const char* src = static_cast<const char*>(p.q_base) +
                               (static_cast<size_t>(J.b) * p.Tq + J.j0) * HI * p.q_row_bytes;
             asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
           }
+          // the weight buffer of parity ib was last read for item it - 2
+          if (it >= 2) ok = mbar_wait(&bars->wfree[ib], ((it - 2) >> 1) & 1, p.budget, abort_v);
         }
-        if (!ok) fail();
-      }
-      if (lane == 0 && ok && it >= 2) {
-        // the weight buffer of parity ib was last read for item it - 2
-        ok = mbar_wait(&bars->wfree[ib], ((it - 2) >> 1) & 1, p.budget, abort_v);
         if (!ok) fail();
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      if (new_group) ++nq;
       for (int i = lane; i < p.G * HI; i += 32) {
         const int jj = i / HI, h = i % HI;
         const long long qrow = static_cast<long long>(I.b) * p.Tq + I.j0 + jj;
@@ -414,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++it;
     }
     // drain: the last query copy has landed before the CTA may exit
-    if (lane == 0 && nq > 0) mbar_wait(&bars->qfull, (nq - 1) & 1, kDrainBudget, nullptr);
+    if (lane == 0 && q_issued > 0) mbar_wait(&bars->qfull, (q_issued - 1) & 1, kDrainBudget, nullptr);
   } else {
     // ---- epilogue warps: TMEM lane quarter = warp % 4; group e handles the
     // CTA's tiles gt = e (mod 2), i.e. TMEM accumulator buffer e
@@ -426,8 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t col0 = lane_addr + static_cast<uint32_t>(egroup * p.NC);
     int gt = 0, it = 0;
     bool waited_zero = false;
-    for (Cursor c = first; c.k >= 0; advance(p, c)) {
-      const Item I = c.I;
+    for (int k = 0;; ++k) {
+      const int r = rank_of(k, p);
+      if (r < 0) break;
+      const Item I = item_of(p, r);
+      if (I.ntile <= 0) continue;
       const int ib = it & 1;
       bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->wfull[ib], (it >> 1) & 1, p.budget, abort_v));
       if (!ok && lane == 0) fail();
@@ -511,10 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this group is done with the item's weights and visibility
       group_bar(egroup);
       if ((ew & 3) == 0 && lane == 0) mbar_arrive(&bars->wfree[ib]);
-      Cursor nx = c;
-      if (p.hist && !(advance(p, nx) && same_group(I, nx.I))) {
-        // both groups' counts of the query group are in: flush them (once
-        // the histogram has been zeroed), then clear for the next group
+      if (p.hist) {
+        // both groups' counts of the item are in: flush them (once the
+        // histogram has been zeroed), then clear for the next item
         epi_bar();
         if (p.after_zero && !waited_zero) {
           asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -540,6 +490,268 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tbase, p.tmem_cols);
+  }
+}
+
+// One work item per CTA (decode: one query group per sequence, a range of
+// its key tiles per CTA): 320 threads, no item loop.  Warp 0 issues the query
+// rows and then the key tiles into the S-stage ring, warp 1 the MMAs, warps
+// 2-9 are the epilogue (two groups of four alternating tiles); the head
+// weights and visibility are in shared memory from the start.  The same
+// arithmetic as the persistent kernel.
+constexpr int kThreads1 = 64 + 128 * kEpiGroups;
+
+template <int HI, bool F8>
+__global__ void __launch_bounds__(kThreads1, 1)
+    indexer_single_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
+                          const __grid_constant__ CUtensorMap tms, KParams p) {
+  if (p.after_zero) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  } else {
+    pdl_wait_then_release();
+  }
+  extern __shared__ __align__(1024) char smem_raw[];
+  char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  char* qs = smem;                                      // [kh][NC][128 B]
+  char* ks = qs + p.kh * p.NC * 128;                    // [stages][kh][128][128 B]
+  float* ksc = reinterpret_cast<float*>(ks + p.stages * p.kh * kHalfBytes);  // FP8: [stages][128]
+  Bars* bars = reinterpret_cast<Bars*>(reinterpret_cast<char*>(ksc) + (F8 ? p.stages * kTileKeys * 4 : 0));
+  uint32_t* hist_s = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(bars) + sizeof(Bars));
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  __shared__ float w_s[256];      // [G][HI]
+  __shared__ int nvis_s[kMaxG];   // [G]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // this CTA's (sequence, query group, tile range); heavy first
+  const int item = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
+  const int grp = item / p.items_per_group;
+  const int sub = item % p.items_per_group;
+  const int b = grp / p.n_groups;
+  const int j0 = (grp % p.n_groups) * p.G;
+  const int n_tiles_all = (p.N + kTileKeys - 1) / kTileKeys;
+
+  for (int jj = tid; jj < p.G; jj += kThreads1) {
+    int nv = 0;
+    if (j0 + jj < p.Tq) {
+      const int t = p.q_pos[static_cast<long long>(b) * p.Tq + j0 + jj];
+      nv = t >= 0 ? (t + 1) / p.m : 0;
+      nv = nv < p.N ? nv : p.N;
+    }
+    nvis_s[jj] = nv;
+  }
+  for (int i = tid; i < p.G * HI; i += kThreads1) {
+    const int jj = i / HI, h = i % HI;
+    const long long qrow = static_cast<long long>(b) * p.Tq + j0 + jj;
+    float wv = p.w_stride == 0 ? p.w[h] : (j0 + jj < p.Tq ? p.w[qrow * p.w_stride + h] : 0.f);
+    if (F8) wv = j0 + jj < p.Tq ? wv * p.q_scale[qrow * HI + h] : 0.f;
+    w_s[i] = wv;
+  }
+  if (p.hist)
+    for (int i = tid; i < kTopkBins; i += kThreads1) hist_s[i] = 0u;
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+      mbar_init(&bars->sfree[s], 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->tfull[i], 1);
+      mbar_init(&bars->tempty[i], 4);
+    }
+    mbar_init(&bars->qfull, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  int nv_max = 0;
+  for (int jj = 0; jj < p.G; ++jj) nv_max = max(nv_max, nvis_s[jj]);
+  const int tiles_vis = (nv_max + kTileKeys - 1) / kTileKeys;
+  const int tile_lo = sub * p.tiles_per_item;
+  const int tile_hi = min(min(tile_lo + p.tiles_per_item, n_tiles_all), tiles_vis);
+  const int ntile = tile_hi - tile_lo;
+  if (ntile <= 0) return;  // uniform: nothing visible in this range
+
+  if (warp == 1) {
+    tmem_alloc(&tmem_base, p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base;
+  volatile int* abort_v = &abort_flag;
+  auto fail = [&]() {
+    if (!*abort_v) raise_flag(p.errw, kFlagTimeout);
+    *abort_v = 1;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmq);
+      if (F8) tma_prefetch_desc(&tms);
+      const int qrow = (b * p.Tq + j0) * HI;
+      // the keys are read once: evict-first, so the scores this kernel writes
+      // stay in L2 for the top-k that reads them next
+      const uint64_t key_policy = l2_policy_evict_first();
+      mbar_expect_tx(&bars->qfull, p.kh * p.NC * 128);
+      for (int h = 0; h < p.kh; ++h) tma_load_2d(qs + h * p.NC * 128, &tmq, &bars->qfull, h * 64, qrow);
+      int issued = 0;
+      for (int i = 0; i < ntile; ++i) {
+        const int s = i % p.stages;
+        const uint32_t ph = (i / p.stages) & 1;
+        if (!mbar_wait(&bars->empty[s], ph ^ 1, p.budget, abort_v) ||
+            (F8 && !mbar_wait(&bars->sfree[s], ph ^ 1, p.budget, abort_v))) {
+          fail();
+          break;
+        }
+        mbar_expect_tx(&bars->full[s], p.kh * kHalfBytes + (F8 ? kTileKeys * 4 : 0));
+        char* dst = ks + s * p.kh * kHalfBytes;
+        for (int h = 0; h < p.kh; ++h)
+          tma_load_3d_hint(dst + h * kHalfBytes, &tmk, &bars->full[s], h * 64, (tile_lo + i) * kTileKeys, b,
+                           key_policy);
+        if (F8) tma_load_2d(ksc + s * kTileKeys, &tms, &bars->full[s], (tile_lo + i) * kTileKeys, b);
+        issued = i + 1;
+      }
+      // drain: every issued copy has landed before the CTA may exit
+      for (int s = 0; s < p.stages && s < issued; ++s) {
+        const int last = issued - 1 - ((issued - 1 - s) % p.stages);
+        mbar_wait(&bars->full[s], (last / p.stages) & 1, kDrainBudget, nullptr);
+      }
+      mbar_wait(&bars->qfull, 0, kDrainBudget, nullptr);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = F8 ? idesc_e4m3_f32(128, p.NC) : idesc_bf16_f32(128, p.NC);
+      int issued = 0;
+      if (mbar_wait(&bars->qfull, 0, p.budget, abort_v)) {
+        for (int i = 0; i < ntile; ++i) {
+          const int s = i % p.stages;
+          const uint32_t ph = (i / p.stages) & 1;
+          const int acc = i & 1;
+          const uint32_t aph = (i >> 1) & 1;
+          if (!mbar_wait(&bars->tempty[acc], aph ^ 1, p.budget, abort_v) ||
+              !mbar_wait(&bars->full[s], ph, p.budget, abort_v)) {
+            fail();
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(ks + s * p.kh * kHalfBytes);
+          const uint32_t b0 = smem_u32(qs);
+          const uint32_t d = tbase + static_cast<uint32_t>(acc * p.NC);
+          for (int kk = 0; kk < p.kh * 4; ++kk) {
+            const int h = kk >> 2, w = kk & 3;
+            const uint64_t ad = sdesc_kmajor_sw128(a0 + h * kHalfBytes + w * 32);
+            const uint64_t bd = sdesc_kmajor_sw128(b0 + h * p.NC * 128 + w * 32);
+            if constexpr (F8)
+              umma_f8(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            else
+              umma_f16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&bars->empty[s]);
+          umma_commit(&bars->tfull[acc]);
+          issued = i + 1;
+        }
+      } else {
+        fail();
+      }
+      // drain: the last MMAs have finished reading shared memory / writing TMEM
+      if (issued > 0) {
+        const int i = issued - 1;
+        mbar_wait(&bars->tfull[i & 1], (i >> 1) & 1, kDrainBudget, nullptr);
+      }
+    }
+  } else {
+    // ---- epilogue warps 2..9: TMEM lane quarter = warp % 4; group e handles
+    // the tiles i = e (mod 2), i.e. TMEM accumulator buffer e
+    const int quarter = warp & 3;
+    const int egroup = (warp - 2) >> 2;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t col0 = lane_addr + static_cast<uint32_t>(egroup * p.NC);
+    const long long srow0 = static_cast<long long>(b) * p.Tq + j0;
+    for (int i = egroup; i < ntile; i += kEpiGroups) {
+      const uint32_t aph = (i >> 1) & 1;
+      const int st = i % p.stages;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->tfull[egroup], aph, p.budget, abort_v));
+      float kscale = 1.f;
+      if (F8 && ok) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->full[st], (i / p.stages) & 1, p.budget, abort_v));
+        if (ok) kscale = ksc[st * kTileKeys + row];
+      }
+      if (F8) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->sfree[st]);
+      }
+      if (!ok) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc_fence_after();
+      const int key = (tile_lo + i) * kTileKeys + row;
+      if constexpr (HI >= 16) {
+        for (int jj = 0; jj < p.G; ++jj) {
+          uint32_t rr[HI / 16][16];
+#pragma unroll
+          for (int hc = 0; hc < HI / 16; ++hc) tmem_ld16(col0 + jj * HI + hc * 16, rr[hc]);
+          tmem_ld_wait();
+          const float* wq = w_s + jj * HI;
+          float sum = 0.f;
+#pragma unroll
+          for (int hc = 0; hc < HI / 16; ++hc)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sum = fmaf(wq[hc * 16 + e], fmaxf(__uint_as_float(rr[hc][e]), 0.f), sum);
+          if (F8) sum *= kscale;
+          const bool vis = key < nvis_s[jj];
+          if (vis) p.S[(srow0 + jj) * p.ld + key] = sum;
+          if (p.hist) {
+            // bucket = top 12 bits of the order-preserving key of sum
+            uint32_t u = __float_as_uint(sum);
+            u = u == 0x80000000u ? 0u : u;
+            u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+            const unsigned am = __ballot_sync(0xffffffffu, vis);
+            if (vis) {
+              const unsigned peers = __match_any_sync(am, u >> 20);
+              if (lane == __ffs(peers) - 1) atomicAdd(&hist_s[u >> 20], static_cast<uint32_t>(__popc(peers)));
+            }
+          }
+        }
+      } else {
+        constexpr int QPC = 16 / HI;  // queries per 16-column chunk
+        for (int c0 = 0; c0 < p.NC; c0 += 16) {
+          uint32_t rr[16];
+          tmem_ld16(col0 + c0, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int qq = 0; qq < QPC; ++qq) {
+            const int jj = c0 / HI + qq;
+            const float* wq = w_s + (jj < p.G ? jj : 0) * HI;
+            float sum = 0.f;
+#pragma unroll
+            for (int e = 0; e < HI; ++e) sum = fmaf(wq[e], fmaxf(__uint_as_float(rr[qq * HI + e]), 0.f), sum);
+            if (jj < p.G && key < nvis_s[jj]) p.S[(srow0 + jj) * p.ld + key] = sum;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->tempty[egroup]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, p.tmem_cols);
+  }
+  if (p.after_zero) asm volatile("griddepcontrol.wait;" ::: "memory");  // the histogram is zeroed
+  if (p.hist) {
+    uint32_t* g = p.hist + (static_cast<long long>(b) * p.Tq + j0) * kTopkBins;
+    for (int i = tid; i < kTopkBins; i += kThreads1)
+      if (hist_s[i]) atomicAdd(g + i, hist_s[i]);
   }
 }
 
@@ -575,21 +787,9 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   const int n_tiles_all = (a.N + kTileKeys - 1) / kTileKeys;
   const long long groups = static_cast<long long>(a.B) * p.n_groups;
   const int n_sm = sm_count();
-  // tile ranges per group when the groups alone cannot fill the GPU: as many
-  // that the item count is a multiple of the SM count (lcm(groups, SMs)
-  // items), or failing that (too few tiles) one item per SM
-  int ipg = 1;
-  if (groups < n_sm) {
-    long long g = groups, h = n_sm;
-    while (h != 0) {
-      const long long t = g % h;
-      g = h;
-      h = t;
-    }
-    ipg = static_cast<int>(n_sm / g);
-    if (ipg > n_tiles_all) ipg = static_cast<int>(n_sm / groups);
-    ipg = ipg < 1 ? 1 : (ipg > n_tiles_all ? n_tiles_all : ipg);
-  }
+  // tile ranges per group: one item per SM when the groups alone cannot fill the GPU
+  int ipg = static_cast<int>(n_sm / (groups > 0 ? groups : 1));
+  ipg = ipg < 1 ? 1 : (ipg > n_tiles_all ? n_tiles_all : ipg);
   p.tiles_per_item = (n_tiles_all + ipg - 1) / ipg;
   p.items_per_group = (n_tiles_all + p.tiles_per_item - 1) / p.tiles_per_item;
   p.errw = a.errw;
@@ -604,10 +804,6 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   if (items > 0x7fffffffLL) return cudaErrorNotSupported;
   p.items = static_cast<int>(items);
   const int grid = static_cast<int>(items < n_sm ? items : n_sm);
-  // one query group per sequence (decode): items of equal weight, in
-  // contiguous blocks per CTA; several groups per sequence (prefill, causal
-  // rows of every length): snake order
-  p.per_cta = p.n_groups == 1 ? static_cast<int>((items + grid - 1) / grid) : 0;
 
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
@@ -651,6 +847,13 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   }
   const size_t smem = 1024 + q_bytes + static_cast<size_t>(stages) * (stage_bytes + (F8 ? kTileKeys * 4 : 0)) +
                      sizeof(Bars) + hist_bytes;
+  if (p.n_groups == 1) {
+    // decode (one query group per sequence): one item per CTA
+    cudaError_t e = ensure_dyn_smem<indexer_single_kernel<HI, F8>>(static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return launch_k(indexer_single_kernel<HI, F8>, dim3(static_cast<unsigned>(items)), dim3(kThreads1), smem, s, 1,
+                    tmk, tmq, tms, p);
+  }
   cudaError_t e = ensure_dyn_smem<indexer_kernel<HI, F8>>(static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   return launch_k(indexer_kernel<HI, F8>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, s, 1, tmk, tmq,

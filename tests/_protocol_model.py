@@ -188,6 +188,59 @@ def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "", 
 
 
 # ---------------------------------------------------------------------------
+# indexer_single_kernel: one item per CTA -- one producer thread issues the
+# query rows and then the key tiles into the stage ring, the MMA issuer feeds
+# two TMEM accumulators, two epilogue groups of four warps alternate tiles;
+# with FP8 keys each stage's scale slot is released by the group that read it
+
+def indexer_single(ntile: int, stages: int, seed: int, fp8: bool = False) -> bool:
+    full = [Bar(1) for _ in range(stages)]
+    empty = [Bar(1) for _ in range(stages)]
+    sfree = [Bar(4) for _ in range(stages)]
+    tfull, tempty = [Bar(1), Bar(1)], [Bar(4), Bar(4)]
+    qfull = Bar(1)
+    loads = [0] * stages
+    scale_tile = [-1] * stages
+
+    def producer():
+        qfull.arrive()
+        for i in range(ntile):
+            s, ph = i % stages, (i // stages) & 1
+            yield (empty[s], ph ^ 1)
+            assert empty[s].done >= i // stages, "stage refilled before its MMAs read it"
+            if fp8:
+                yield (sfree[s], ph ^ 1)
+                assert i < stages or sfree[s].done >= i // stages, "key scales refilled before the epilogue read them"
+                scale_tile[s] = i
+            loads[s] += 1
+            full[s].arrive()
+
+    def mma():
+        yield (qfull, 0)
+        for i in range(ntile):
+            s, ph = i % stages, (i // stages) & 1
+            acc, aph = i & 1, (i >> 1) & 1
+            yield (tempty[acc], aph ^ 1)
+            yield (full[s], ph)
+            assert loads[s] == i // stages + 1, "MMA read a stage that holds another tile"
+            assert tempty[acc].done >= i >> 1, "accumulator overwritten before the epilogue read it"
+            empty[s].arrive()
+            tfull[acc].arrive()
+
+    def epilogue(group: int):
+        for i in range(group, ntile, 2):
+            yield (tfull[group], (i >> 1) & 1)
+            if fp8:
+                s = i % stages
+                yield (full[s], (i // stages) & 1)
+                assert scale_tile[s] == i, "epilogue read another tile's key scales"
+                sfree[s].arrive()
+            tempty[group].arrive()
+
+    return run([producer(), mma()] + [epilogue(g) for g in (0, 1) for _ in range(4)], seed)
+
+
+# ---------------------------------------------------------------------------
 # attend_tc_kernel: K tiles loaded at once, a tile's buffer refilled with V
 # once its score MMAs are done (gather or TMA producers alike), per-tile
 # epilogue (two named barriers per tile among the 8 epilogue warps), output

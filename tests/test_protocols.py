@@ -21,9 +21,16 @@ def test_indexer_protocol_completes_without_hazards():
         stages = rng.choice([2, 3, 4, 5, 8])
         hist = rng.random() < 0.5
         fp8 = rng.random() < 0.5
-        # consecutive items of one query group (decode blocks) or all distinct (prefill)
-        groups = sorted(rng.randint(0, 2) for _ in items) if rng.random() < 0.5 else None
-        assert M.indexer(items, stages, trial, hist, fp8=fp8, groups=groups), (items, stages, hist, fp8, groups)
+        assert M.indexer(items, stages, trial, hist, fp8=fp8), (items, stages, hist, fp8)
+
+
+def test_indexer_single_protocol_completes_without_hazards():
+    """The one-item decode indexer, bf16 and FP8 keys."""
+    rng = random.Random(1)
+    for trial in range(300):
+        ntile = rng.choice([0, 1, 2, 3, 4, 5, 8, 13, 17])
+        stages = rng.choice([2, 3, 5, 8])
+        assert M.indexer_single(ntile, stages, trial, fp8=rng.random() < 0.5), (ntile, stages)
 
 
 @pytest.mark.parametrize("plant", ["qfree", "wfree", "sfree"])
