@@ -757,10 +757,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--workload", default=HEADLINE,
-                    choices=["decode_1m", "decode_128k", "decode_1m_tail", "hca_attend_1m", "prefill_8k"],
+                    choices=["decode_1m", "decode_128k", "decode_1m_tail", "hca_attend_1m", "prefill_8k",
+                             "decode_1m_variants", "hybrid_stack_1m"],
                     help="decode workload to time (the headline is decode_1m); with --quick also "
-                         "hca_attend_1m (only the HCA attention over given caches) and prefill_8k (the whole "
-                         "layer over an 8192-token prefill)")
+                         "hca_attend_1m (only the HCA attention over given caches), prefill_8k (the whole "
+                         "layer over an 8192-token prefill), decode_1m_variants (the 1M step with the append "
+                         "and with FP8 indexer keys) and hybrid_stack_1m (16 layers at 1M context)")
     ap.add_argument("--quick", action="store_true",
                     help="time the device step only: no stage breakdown, e2e, 128K line or CPU baseline "
                          "(the form used for kernel profiles)")
@@ -769,7 +771,7 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.workload in ("hca_attend_1m", "prefill_8k"):
+    if args.workload in ("hca_attend_1m", "prefill_8k", "decode_1m_variants", "hybrid_stack_1m"):
         if not args.quick or args.impl != "ours" or world != 1:
             raise SystemExit(f"{args.workload} is a profiling case: --quick, one GPU, --impl ours")
         torch.cuda.set_device(local)
@@ -779,6 +781,10 @@ def main():
         st = torch.cuda.Stream(device=dev)
         if args.workload == "hca_attend_1m":
             print(json.dumps(hca_attend_given(dev, st, args.steps, args.warmup)))
+        elif args.workload == "decode_1m_variants":
+            print(json.dumps(decode_1m_variants(dev, st, args.steps)))
+        elif args.workload == "hybrid_stack_1m":
+            print(json.dumps(hybrid_stack_1m(dev, st, args.steps)))
         else:
             print(json.dumps(prefill_8k(dev, st, args.steps)))
         return
