@@ -10,21 +10,21 @@
 // with a cluster barrier between them:
 //  1. CTA r scans its chunk [r*E, (r+1)*E) of the scores and keeps, in index
 //     order, every key whose bucket is >= beta, the bucket holding the k-th
-//     largest key (one float comparison per score against the bucket's
-//     lowest value; candidates in global memory); the keys of bucket beta
-//     count into a second-level histogram of key bits 19..8;
-//  2. every CTA stages all ranks' candidates in shared memory (when they fit)
-//     and fixes the same exact rule (prefix, mask, k_rem) from that histogram
-//     and at most one 8-bit pass: keys above the prefix are kept, and of the
-//     keys equal to it the k_rem with the lowest indices;
+//     largest key (candidates: in global memory, staged in shared memory when
+//     they fit);
+//  2. every CTA reads the candidates of bucket beta and fixes the same exact
+//     rule (prefix, mask, k_rem) with a histogram of key bits 19..8 and at
+//     most one 8-bit pass: keys above the prefix are kept, and of the keys
+//     equal to it the k_rem with the lowest indices;
 //  3. each CTA counts its kept candidates, learns the counts of the CTAs
 //     before it, and so the rank of each kept block in ascending order; it
-//     writes idx_out and sends (rank -> block) to the CTA that attends that
-//     rank;
-//  4. CTA r attends the virtual key slots [r*S_r, (r+1)*S_r) of the query
-//     (selected blocks by rank, then the window) for every head (8 warps:
-//     4 groups of 16 heads x 2 key halves, mma.sync), merges the halves, and
-//     sends each head's (O, max, sum) to the CTA owning that head;
+//     writes idx_out and records (rank -> block) for the ranks it attends;
+//  4. CTA r gathers the K/V rows of its virtual key slots [r*S_r, (r+1)*S_r)
+//     (selected blocks by rank, then the window; all 256 threads, 16 bytes
+//     each, consecutive threads on consecutive chunks of a row) and attends
+//     them for every head (8 warps: 4 groups of 16 heads x 2 key halves,
+//     mma.sync), merges the halves, and sends each head's (O, max, sum) to
+//     the CTA owning that head;
 //  5. each CTA folds the partials of its heads in rank order and writes the
 //     output.
 // Everything merges in a fixed order: results do not depend on scheduling.
@@ -94,16 +94,10 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
-// Bulk prefetch of ``bytes`` (a multiple of 16, 16-byte aligned) into L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // KH: keys per warp per tile step (the half of S_r a warp attends is walked
 // in steps of KH keys; KH = S_r / 2 makes it one step).
 template <int D, int KH>
 __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, int S_r) {
-  pdl_wait_then_release();
   constexpr int LDO = D + 4;
   constexpr int CH = D / 8, DT = D / 8;
   extern __shared__ __align__(128) char smem[];
@@ -124,7 +118,6 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
   float* recv_m = recv + L.hpc * kC * LDO;                // [hpc][kC]
   float* recv_l = recv_m + L.hpc * kC;                    // [hpc][kC]
   __shared__ __align__(8) uint64_t bar, bar_q;
-  __shared__ uint32_t n_own_s;                            // this rank's candidates, read by the cluster
   __shared__ uint32_t rcnt[kC], wg[kT / 32], we[kT / 32];
   uint32_t bar_phase = 0;
   if (tid == 0) {
@@ -133,6 +126,10 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     mbar_fence_init();
   }
   __syncthreads();
+  // first half of a cluster barrier: every CTA of the cluster has started
+  // before any writes another's shared memory (the wait is at the first
+  // such write)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   // wait for the bulk copies on ``bar``: bounded by the call's budget (a
   // timeout is reported), then drained, so the copies have landed before the
   // buffer is read, refilled or given up at exit
@@ -161,38 +158,19 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     bulk_g2s(qs, static_cast<const char*>(at.q) + static_cast<size_t>(q) * H * D * 2,
              static_cast<uint32_t>(H * D * 2), &bar_q);
   }
-  // K/V tile of this CTA's key slots; kept compressed rows are requested as
-  // soon as their rank is known (step 2), the rest in step 3
+  // K/V tile of this CTA's key slots (gathered in step 3)
   char* Ks = smem + L.kv;
   char* Vs = Ks + S_r * D * 2;
   const char* kc_base = static_cast<const char*>(at.k_cmp) + static_cast<size_t>(b) * at.N * D * 2;
   const char* vc_base = static_cast<const char*>(at.v_cmp) + static_cast<size_t>(b) * at.N * D * 2;
-  const char* kr_base = static_cast<const char*>(at.k_raw) + static_cast<size_t>(b) * at.T_raw * D * 2;
-  const char* vr_base = static_cast<const char*>(at.v_raw) + static_cast<size_t>(b) * at.T_raw * D * 2;
-  auto gather_row = [&](int j, int row_c) {  // one lane copies compressed row row_c into slot j
-#pragma unroll
-    for (int ch = 0; ch < CH; ++ch) {
-      cp_async16(Ks + swz<D>(j, ch), kc_base + static_cast<size_t>(row_c) * D * 2 + ch * 16, true);
-      cp_async16(Vs + swz<D>(j, ch), vc_base + static_cast<size_t>(row_c) * D * 2 + ch * 16, true);
-    }
-  };
-  // the window slots [k, k + W) of this CTA's range do not depend on the
-  // selection: their rows are requested now (rows outside the buffer or
-  // before token 0 are zero-filled; step 3 reports them)
-  const int win_lo = r < A ? max(r * S_r, k) : 0;
-  const int win_hi = r < A ? min((r + 1) * S_r, K_total) : 0;
-  if (win_lo < win_hi) {
-    const int raw_base = at.raw_base[b];
-    for (int i = tid; i < (win_hi - win_lo) * CH; i += kT) {
-      const int sl = win_lo + i / CH, ch = i % CH, rw = sl - r * S_r;
-      const int u = t - at.W + 1 + (sl - k);
-      const int rr = u - raw_base;
-      const bool valid = u >= 0 && rr >= 0 && rr < at.T_raw;
-      cp_async16(Ks + swz<D>(rw, ch), valid ? kr_base + static_cast<size_t>(rr) * D * 2 + ch * 16 : kc_base, valid);
-      cp_async16(Vs + swz<D>(rw, ch), valid ? vr_base + static_cast<size_t>(rr) * D * 2 + ch * 16 : vc_base, valid);
-    }
-    cp_async_commit();
-  }
+
+  // Everything above reads only the call's inputs (query positions and
+  // rows), which no kernel of this call writes; the kernel launched before
+  // this one's predecessor has completed when this kernel starts (each
+  // kernel releases its dependents after its own wait, the indexer after
+  // the histogram-zeroing kernel's).  The scores and histograms below are
+  // the indexer's: wait for it.
+  pdl_wait_then_release();
 
   // the scores of this CTA's first batch to shared memory by bulk copy
   // (rounded up to 4 scores: the row holds ld >= N, a multiple of 4), issued
@@ -218,93 +196,60 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
       if (r == 0 && tid == 0) raise_flag(at.errw, kFlagIndex);
       if (r < A) mbar_wait(&bar_q, 0, kDrainBudget, nullptr);
       if (lo < hi) mbar_wait(&bar, 0, kDrainBudget, nullptr);
-      cp_async_wait<0>();  // the window rows requested at the start
       return;
     }
   }
 
-  // ---- 1. candidates of this CTA's chunk (keys in bucket beta or above), in
-  // index order; the keys of bucket beta also count into the second-level
-  // histogram (key bits 19..8)
+  // ---- 1. candidates of this CTA's chunk, in index order; the keys of
+  // bucket beta also count into the second-level histogram (bits 19..8)
   uint32_t n_own = 0;
   if (!all) {
     const uint32_t beta = static_cast<uint32_t>(b1.beta);
     uint2* gl = gl_all + static_cast<long long>(r) * E;
     uint32_t* hist2 = a.hist2 + q * kTopkBins;
-    // the lowest scores of buckets beta and beta + 1: the key map is
-    // order-preserving (and folds -0 onto +0, as the float comparison does),
-    // so a score is a candidate iff it compares >= tb and in bucket beta iff
-    // also < tb1 (bucket 0 holds no finite lowest value: every score is a
-    // candidate then; above the top bucket nothing is)
-    const float tb = beta == 0 ? -INFINITY : key_score(beta << 20);
-    const float tb1 = beta >= kTopkBins - 1 ? INFINITY : key_score((beta + 1) << 20);
     for (int sub = lo; sub < hi; sub += kT * kRun) {
       if (sub != lo) issue_batch(sub);  // the first batch was requested before the bucket search
       bulk_wait();
-      // warp w owns the contiguous segment [w*SEG, (w+1)*SEG) of the batch and
-      // reads it as one float4 per lane (128 consecutive scores per step:
-      // conflict-free); pass 1 counts its candidates and feeds bucket beta's
-      // keys into the second-level histogram, pass 2 writes the candidates
-      // in index order after a scan over the warps' counts
-      constexpr int NWS = kT / 32, SEG = kT * kRun / NWS;
-      const int nb = min(kT * kRun, hi - sub);
-      const int s_lo = warp * SEG, s_hi = min(nb, s_lo + SEG);
-      uint32_t wcount = 0;
-      for (int base = s_lo; base < s_hi; base += 128) {
-        const int i = base + 4 * lane;
-        const float4 fv = *reinterpret_cast<const float4*>(stage + i);
+      // thread tid owns the run [sub + kRun*tid, sub + kRun*(tid+1)); its 16
+      // float4 reads start at a rotated position (fewer bank conflicts)
+      const int i0 = sub + kRun * tid;
+      unsigned long long take = 0ull, inb = 0ull;
+#pragma unroll
+      for (int jr = 0; jr < kRun / 4; ++jr) {
+        const int j = (jr + tid) & (kRun / 4 - 1);
+        const float4 fv = *reinterpret_cast<const float4*>(stage + kRun * tid + 4 * j);
         const float v4[4] = {fv.x, fv.y, fv.z, fv.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const bool c = i + e < s_hi && v4[e] >= tb;
-          wcount += c ? 1u : 0u;
-          // bucket beta holds about k of the keys: one reduction per key of it
-          if (c && v4[e] < tb1) atomicAdd(hist2 + ((score_key(v4[e]) >> 8) & (kTopkBins - 1)), 1u);
+          const uint32_t bin = score_key(v4[e]) >> 20;
+          const bool in = i0 + 4 * j + e < hi;
+          const unsigned long long bit = 1ull << (4 * j + e);
+          take |= (in && bin >= beta) ? bit : 0ull;
+          inb |= (in && bin == beta) ? bit : 0ull;
         }
       }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) wcount += __shfl_xor_sync(0xffffffffu, wcount, o);
-      if (lane == 0) tmp[warp] = wcount;
+      // bucket beta holds about k of the keys: one reduction per key of it
+      for (unsigned long long m2 = inb; m2; m2 &= m2 - 1) {
+        const int p = __ffsll(static_cast<long long>(m2)) - 1;
+        atomicAdd(hist2 + ((score_key(stage[kRun * tid + p]) >> 8) & (kTopkBins - 1)), 1u);
+      }
+      const uint32_t mine = static_cast<uint32_t>(__popcll(take));
+      const uint32_t incl = block_incl_scan<kT>(mine, tmp);
+      if (tid == kT - 1) tot32 = incl;
       __syncthreads();
-      uint32_t pos = n_own;
-      for (int w = 0; w < warp; ++w) pos += tmp[w];
-      if (tid == 0) {
-        uint32_t t = 0;
-        for (int w = 0; w < NWS; ++w) t += tmp[w];
-        tot32 = t;
+      uint32_t pos = n_own + incl - mine;
+      while (take) {
+        const int p = __ffsll(static_cast<long long>(take)) - 1;
+        take &= take - 1;
+        gl[pos++] = make_uint2(score_key(stage[kRun * tid + p]), static_cast<uint32_t>(i0 + p));
       }
-      const unsigned ltm = lanemask_lt();
-      for (int base = s_lo; base < s_hi; base += 128) {
-        const int i = base + 4 * lane;
-        const float4 fv = *reinterpret_cast<const float4*>(stage + i);
-        const float v4[4] = {fv.x, fv.y, fv.z, fv.w};
-        // candidates in index order: lane by lane, and within a lane element
-        // by element; one ballot per element position
-        unsigned bal[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) bal[e] = __ballot_sync(0xffffffffu, i + e < s_hi && v4[e] >= tb);
-        const unsigned any4 = bal[0] | bal[1] | bal[2] | bal[3];
-        if (any4 == 0u) continue;
-        uint32_t at = pos + __popc(bal[0] & ltm) + __popc(bal[1] & ltm) + __popc(bal[2] & ltm) +
-                      __popc(bal[3] & ltm);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if ((bal[e] >> lane) & 1u) {
-            const uint32_t row_c = static_cast<uint32_t>(sub + i + e);
-            gl[at++] = make_uint2(score_key(v4[e]), row_c);
-            // the candidate's K and V rows into L2: the kept ones are
-            // gathered after the ranking and then come from L2
-            bulk_prefetch_l2(kc_base + static_cast<size_t>(row_c) * D * 2, D * 2);
-            bulk_prefetch_l2(vc_base + static_cast<size_t>(row_c) * D * 2, D * 2);
-          }
-        pos += __popc(bal[0]) + __popc(bal[1]) + __popc(bal[2]) + __popc(bal[3]);
-      }
-      __syncthreads();  // tot32 written; tmp read
       n_own += tot32;
       __syncthreads();  // the stage and tot32 are rewritten by the next batch
     }
   }
-  if (tid == 0) n_own_s = n_own;
+  // this rank's candidate count into every CTA's table (read after the barrier)
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (tid < kC) *cluster.map_shared_rank(&rcnt[r], tid) = n_own;
   // no slot of this CTA holds a kept block until step 2 says so (with
   // consistent inputs step 2 fills every slot below k; with a histogram that
   // does not match the scores, unfilled slots stay empty instead of undefined)
@@ -325,8 +270,6 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
       }
     }
   } else {
-    if (tid < kC) rcnt[tid] = *cluster.map_shared_rank(&n_own_s, tid);
-    __syncthreads();
     bool staged = true;
     for (int i = 0; i < kC; ++i) staged = staged && rcnt[i] <= static_cast<uint32_t>(kCandR);
     uint2* lists = reinterpret_cast<uint2*>(smem + L.stage);  // [kC][kCandR]
@@ -338,9 +281,7 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
       for (int i = 0; i < kC; ++i)
         if (rcnt[i]) bulk_g2s(lists + i * kCandR, gl_all + static_cast<long long>(i) * E, (rcnt[i] + 1) / 2 * 16, &bar);
     }
-    // the rule's top 24 bits from the second-level histogram while the lists
-    // arrive; keys above the prefix are kept, and of the keys equal to it the
-    // k_rem with the lowest indices
+    // the rule's top 24 bits while the lists arrive
     const uint32_t beta = static_cast<uint32_t>(b1.beta);
     const uint32_t k2 = static_cast<uint32_t>(k) - b1.above;
     const Bucket b2 = find_bucket<kT>(a.hist2 + q * kTopkBins, k2, tmp, &sb);
@@ -415,7 +356,6 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
           const int pos = static_cast<int>(gt_b + min(eq_b, rl.k_rem));
           if (pos >= p_lo && pos < p_hi && pos < k) {  // this CTA attends that rank and reports it
             map[pos - p_lo] = static_cast<int>(cv.y);
-            gather_row(pos - p_lo, static_cast<int>(cv.y));
             if (a.idx_out) a.idx_out[q * k + pos] = static_cast<int32_t>(cv.y);
             if (a.score_out) a.score_out[q * k + pos] = key_score(cv.x);
           }
@@ -433,8 +373,7 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     const int s0 = r * S_r;
     const int raw_base = at.W > 0 ? at.raw_base[b] : 0;
     bool bad = false;
-    // slot codes: kept blocks (already requested in step 2 unless every visible
-    // block is kept), then window rows, then nothing
+    // slot codes: kept blocks, then window rows, then nothing
     for (int j = tid; j < S_r; j += kT) {
       const int s = s0 + j;
       int code = -1;
@@ -454,10 +393,10 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     }
     if (bad) raise_flag(at.errw, kFlagIndex);
     __syncthreads();
+    const char* kr_base = static_cast<const char*>(at.k_raw) + static_cast<size_t>(b) * at.T_raw * D * 2;
+    const char* vr_base = static_cast<const char*>(at.v_raw) + static_cast<size_t>(b) * at.T_raw * D * 2;
     for (int i = tid; i < S_r * CH; i += kT) {
       const int rw = i / CH, ch = i % CH;
-      if (!all && s0 + rw < k) continue;                 // requested in step 2
-      if (s0 + rw >= win_lo && s0 + rw < win_hi) continue;  // requested at the start
       const int code = codes[rw];
       const char* kp = code >= 0 ? kc_base + static_cast<size_t>(code) * D * 2
                                  : kr_base + static_cast<size_t>(code <= -2 ? -code - 2 : 0) * D * 2;

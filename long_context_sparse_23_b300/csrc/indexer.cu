@@ -11,20 +11,24 @@
 // owns one key row and reduces sum_h w_h * max(acc, 0) over its own TMEM
 // columns -- no cross-thread reduction.  A work item is one query group
 // against a range of 128-key tiles; TMA feeds a 128-byte-swizzled shared-
-// memory ring of key tiles, one thread issues tcgen05.mma into two TMEM
-// accumulators, and two groups of four epilogue warps take alternate tiles
-// (tcgen05.ld, ReLU and the head weights, coalesced fp32 scores, the top-k
-// bucket histogram).  Two kernels:
+// memory ring of key tiles, one thread issues tcgen05.mma into TMEM
+// accumulators, and two groups of four epilogue warps read them (tcgen05.ld,
+// ReLU and the head weights, coalesced fp32 scores, the top-k bucket
+// histogram).  Two kernels:
 //   indexer_single_kernel  decode (one query group per sequence): one item
-//                          per CTA, the query rows and key tiles issued by one
-//                          producer thread at once;
+//                          per CTA; the query rows and the first key tile
+//                          are requested before any global read;
 //   indexer_kernel         prefill (query groups of every causal length):
 //                          persistent, one CTA per SM walking its items
 //                          (heavy first, snake order), an item producer warp
-//                          loading each item's weights and query rows.
+//                          loading each item's weights and query rows; both
+//                          epilogue groups on every tile, half the queries
+//                          each.
 // mbarriers connect the stages (full/empty per smem stage, full/empty per
 // TMEM buffer); every wait is bounded and reports CSA_FLAG_TIMEOUT instead of
-// hanging.  Tiles past the group's last visible block are never loaded.
+// hanging.  Tiles past the group's last visible block are never loaded, but
+// for the first ring stages of a decode item, which are requested before the
+// visibility is read (such a tile lands and is left unread).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -32,7 +36,7 @@ namespace csa {
 
 namespace {
 
-constexpr int kEpiGroups = 2;                      // epilogue warp groups, alternating tiles
+constexpr int kEpiGroups = 2;                      // epilogue warp groups
 constexpr int kEpiWarp0 = 3;                       // first epilogue warp
 constexpr int kThreads = 32 * kEpiWarp0 + 128 * kEpiGroups;  // 3 role warps + 8 epilogue warps
 constexpr int kTileKeys = 128;
@@ -58,6 +62,7 @@ struct KParams {
   int tiles_per_item;
   int items;          // B * n_groups * items_per_group
   int tmem_cols;
+  int acc_shift;  // one-item kernel on E4M3 keys: 1 << acc_shift TMEM accumulators (2 or 4)
   uint32_t* errw;
   long long budget;
   uint32_t* hist;  // [B*Tq][kTopkBins] (G == 1 only), or nullptr
@@ -70,8 +75,8 @@ struct KParams {
 struct __align__(8) Bars {
   uint64_t full[8];    // key stage loaded
   uint64_t empty[8];   // key stage consumed by the MMAs
-  uint64_t tfull[2];   // accumulator buffer written by the MMAs
-  uint64_t tempty[2];  // accumulator buffer read by its epilogue group
+  uint64_t tfull[4];   // accumulator buffer written by the MMAs
+  uint64_t tempty[4];  // accumulator buffer read by its epilogue group
   uint64_t qfull;      // the item's queries loaded
   uint64_t qfree;      // the item's MMAs done: the query buffer may be refilled
   uint64_t wfull[2];   // head weights / visibility of an item written
@@ -142,7 +147,8 @@ __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 3, 256;" ::: 
 //               (double-buffered) and the query rows (TMA, one buffer, loaded
 //               once the previous item's MMAs are done; the next item's rows
 //               are prefetched into L2 meanwhile);
-//   warps 3-10  epilogue, two groups of four alternating tiles.
+//   warps 3-10  epilogue, two groups of four, both on every tile (half the
+//               queries each).
 // F8: keys and queries are E4M3 codes (one 128-byte row per key / query head,
 // one power-of-two scale per row); the MMAs are kind::f8f6f4 and the
 // epilogue applies the scales: sum_h (w_h s_q,h) ReLU(acc_h) * s_k.
@@ -179,11 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
-      mbar_init(&bars->sfree[s], 4);
+      mbar_init(&bars->sfree[s], 4 * kEpiGroups);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->tfull[i], 1);
-      mbar_init(&bars->tempty[i], 4);
+      mbar_init(&bars->tempty[i], 4 * kEpiGroups);
       mbar_init(&bars->wfull[i], 1);
       mbar_init(&bars->wfree[i], kEpiGroups);
     }
@@ -364,14 +370,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // drain: the last query copy has landed before the CTA may exit
     if (lane == 0 && q_issued > 0) mbar_wait(&bars->qfull, (q_issued - 1) & 1, kDrainBudget, nullptr);
   } else {
-    // ---- epilogue warps: TMEM lane quarter = warp % 4; group e handles the
-    // CTA's tiles gt = e (mod 2), i.e. TMEM accumulator buffer e
+    // ---- epilogue warps: TMEM lane quarter = warp % 4; both groups take
+    // every tile (TMEM accumulator gt mod 2), group e its half of the
+    // group's queries (H_I >= 16) or of the 16-column chunks (H_I < 16), so
+    // a tile's epilogue takes half as long and the MMAs into the other
+    // accumulator hide it
     const int ew = warp - kEpiWarp0;
     const int egroup = ew >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t col0 = lane_addr + static_cast<uint32_t>(egroup * p.NC);
+    const int qh = (p.G + 1) / 2;
+    const int jlo = egroup * qh, jhi = min(p.G, jlo + qh);
+    const int ch_h = (p.NC / 16 + 1) / 2;
+    const int clo = egroup * ch_h * 16, chi = min(p.NC, (egroup + 1) * ch_h * 16);
     int gt = 0, it = 0;
     bool waited_zero = false;
     for (int k = 0;; ++k) {
@@ -387,10 +399,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long srow0 = static_cast<long long>(I.b) * p.Tq + I.j0;
       for (int i = 0; i < I.ntile; ++i) {
         const int g2 = gt + i;
-        if ((g2 & 1) != egroup) continue;
+        const int acc = g2 & 1;
         const uint32_t aph = (g2 >> 1) & 1;
         const int st = g2 % p.stages;
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->tfull[egroup], aph, p.budget, abort_v));
+        const uint32_t col0 = lane_addr + static_cast<uint32_t>(acc * p.NC);
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->tfull[acc], aph, p.budget, abort_v));
         // FP8: the key's scale, read before the stage's scale slot is released
         // (the stage's load phase is complete, so this wait returns at once and
         // makes the copy's writes visible to this thread)
@@ -409,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const int key = tile_at(I, i) * kTileKeys + row;
           if constexpr (HI >= 16) {
-            for (int jj = 0; jj < p.G; ++jj) {
+            for (int jj = jlo; jj < jhi; ++jj) {
               // all of the query's head columns in flight at once, one wait
               uint32_t rr[HI / 16][16];
 #pragma unroll
@@ -438,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
             constexpr int QPC = 16 / HI;  // queries per 16-column chunk
-            for (int c0 = 0; c0 < p.NC; c0 += 16) {
+            for (int c0 = clo; c0 < chi; c0 += 16) {
               uint32_t rr[16];
               tmem_ld16(col0 + c0, rr);
               tmem_ld_wait();
@@ -456,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->tempty[egroup]);
+        if (lane == 0) mbar_arrive(&bars->tempty[acc]);
       }
       gt += I.ntile;
       // this group is done with the item's weights and visibility
@@ -494,11 +507,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // One work item per CTA (decode: one query group per sequence, a range of
-// its key tiles per CTA): 320 threads, no item loop.  Warp 0 issues the query
-// rows and then the key tiles into the S-stage ring, warp 1 the MMAs, warps
-// 2-9 are the epilogue (two groups of four alternating tiles); the head
-// weights and visibility are in shared memory from the start.  The same
-// arithmetic as the persistent kernel.
+// its key tiles per CTA): 320 threads, no item loop.  Thread 0 initialises
+// the barriers and at once requests the query rows and the first key tile
+// (they need no global read: the item follows from the block index), while
+// the other threads read the visibility and head weights; then the rest of
+// the S-stage ring is requested, warp 0 keeps it filled, warp 1 issues the
+// MMAs into two TMEM accumulators (four with E4M3 keys), warps 2-9 are the
+// epilogue (two groups of four alternating tiles).  The same arithmetic as
+// the persistent kernel.
 constexpr int kThreads1 = 64 + 128 * kEpiGroups;
 
 template <int HI, bool F8>
@@ -522,6 +538,10 @@ __global__ void __launch_bounds__(kThreads1, 1)
   __shared__ float w_s[256];      // [G][HI]
   __shared__ int nvis_s[kMaxG];   // [G]
 
+  // TMEM accumulators: with E4M3 keys four when they fit in the 512 columns
+  // (the MMAs run up to three tiles ahead of the epilogue, the longer stage
+  // there), else two; two with bf16 keys
+  const int acc_sh = F8 ? p.acc_shift : 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // this CTA's (sequence, query group, tile range); heavy first
   const int item = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
@@ -530,7 +550,48 @@ __global__ void __launch_bounds__(kThreads1, 1)
   const int b = grp / p.n_groups;
   const int j0 = (grp % p.n_groups) * p.G;
   const int n_tiles_all = (p.N + kTileKeys - 1) / kTileKeys;
-
+  const int tile_lo = sub * p.tiles_per_item;
+  // the item's tiles before the visibility cut, of which the first n_pre are
+  // requested at once
+  const int tile_cap = min(tile_lo + p.tiles_per_item, n_tiles_all);
+  const int n_pre = min(p.stages, max(tile_cap - tile_lo, 0));
+  const uint32_t stage_tx = p.kh * kHalfBytes + (F8 ? kTileKeys * 4 : 0);
+  char* const ks_c = ks;
+  uint64_t key_policy = 0;
+  auto issue_tile = [&](int i, int s) {  // key tile tile_lo + i into stage s (thread 0)
+    mbar_expect_tx(&bars->full[s], stage_tx);
+    char* dst = ks_c + s * p.kh * kHalfBytes;
+    for (int h = 0; h < p.kh; ++h)
+      tma_load_3d_hint(dst + h * kHalfBytes, &tmk, &bars->full[s], h * 64, (tile_lo + i) * kTileKeys, b,
+                       key_policy);
+    if (F8) tma_load_2d(ksc + s * kTileKeys, &tms, &bars->full[s], (tile_lo + i) * kTileKeys, b);
+  };
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+      mbar_init(&bars->sfree[s], 4);
+    }
+    for (int i = 0; i < (1 << acc_sh); ++i) {
+      mbar_init(&bars->tfull[i], 1);
+      mbar_init(&bars->tempty[i], 4);
+    }
+    mbar_init(&bars->qfull, 1);
+    mbar_fence_init();
+    // the query rows and the first key tile need no global read: they are
+    // requested before the visibility, weights and TMEM are set up; the
+    // next stages follow once those are (every stage is free at the start;
+    // a tile that turns out invisible is loaded and left unread).  Alone in
+    // flight at first, each CTA's first tile lands sooner, and the MMAs
+    // start earlier.  The keys are read once: evict-first, so the scores
+    // this kernel writes stay in L2 for the top-k that reads them next
+    key_policy = l2_policy_evict_first();
+    const int qrow = (b * p.Tq + j0) * HI;
+    mbar_expect_tx(&bars->qfull, p.kh * p.NC * 128);
+    for (int h = 0; h < p.kh; ++h) tma_load_2d(qs + h * p.NC * 128, &tmq, &bars->qfull, h * 64, qrow);
+    if (n_pre > 0) issue_tile(0, 0);
+  }
   for (int jj = tid; jj < p.G; jj += kThreads1) {
     int nv = 0;
     if (j0 + jj < p.Tq) {
@@ -549,28 +610,23 @@ __global__ void __launch_bounds__(kThreads1, 1)
   }
   if (p.hist)
     for (int i = tid; i < kTopkBins; i += kThreads1) hist_s[i] = 0u;
-  if (tid == 0) {
-    abort_flag = 0;
-    for (int s = 0; s < p.stages; ++s) {
-      mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 1);
-      mbar_init(&bars->sfree[s], 4);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->tfull[i], 1);
-      mbar_init(&bars->tempty[i], 4);
-    }
-    mbar_init(&bars->qfull, 1);
-    mbar_fence_init();
-  }
   __syncthreads();
+  if (tid == 0)
+    for (int i = 1; i < n_pre; ++i) issue_tile(i, i);  // the rest of the first ring
   int nv_max = 0;
   for (int jj = 0; jj < p.G; ++jj) nv_max = max(nv_max, nvis_s[jj]);
   const int tiles_vis = (nv_max + kTileKeys - 1) / kTileKeys;
-  const int tile_lo = sub * p.tiles_per_item;
-  const int tile_hi = min(min(tile_lo + p.tiles_per_item, n_tiles_all), tiles_vis);
+  const int tile_hi = min(tile_cap, tiles_vis);
   const int ntile = tile_hi - tile_lo;
-  if (ntile <= 0) return;  // uniform: nothing visible in this range
+  if (ntile <= 0) {
+    // uniform: nothing visible in this range; the copies requested at the
+    // start land before the CTA exits
+    if (tid == 0) {
+      for (int s = 0; s < n_pre; ++s) mbar_wait(&bars->full[s], 0, kDrainBudget, nullptr);
+      mbar_wait(&bars->qfull, 0, kDrainBudget, nullptr);
+    }
+    return;
+  }
 
   if (warp == 1) {
     tmem_alloc(&tmem_base, p.tmem_cols);
@@ -588,17 +644,8 @@ __global__ void __launch_bounds__(kThreads1, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      tma_prefetch_desc(&tmk);
-      tma_prefetch_desc(&tmq);
-      if (F8) tma_prefetch_desc(&tms);
-      const int qrow = (b * p.Tq + j0) * HI;
-      // the keys are read once: evict-first, so the scores this kernel writes
-      // stay in L2 for the top-k that reads them next
-      const uint64_t key_policy = l2_policy_evict_first();
-      mbar_expect_tx(&bars->qfull, p.kh * p.NC * 128);
-      for (int h = 0; h < p.kh; ++h) tma_load_2d(qs + h * p.NC * 128, &tmq, &bars->qfull, h * 64, qrow);
-      int issued = 0;
-      for (int i = 0; i < ntile; ++i) {
+      int issued = n_pre;
+      for (int i = n_pre; i < ntile; ++i) {
         const int s = i % p.stages;
         const uint32_t ph = (i / p.stages) & 1;
         if (!mbar_wait(&bars->empty[s], ph ^ 1, p.budget, abort_v) ||
@@ -606,12 +653,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
           fail();
           break;
         }
-        mbar_expect_tx(&bars->full[s], p.kh * kHalfBytes + (F8 ? kTileKeys * 4 : 0));
-        char* dst = ks + s * p.kh * kHalfBytes;
-        for (int h = 0; h < p.kh; ++h)
-          tma_load_3d_hint(dst + h * kHalfBytes, &tmk, &bars->full[s], h * 64, (tile_lo + i) * kTileKeys, b,
-                           key_policy);
-        if (F8) tma_load_2d(ksc + s * kTileKeys, &tms, &bars->full[s], (tile_lo + i) * kTileKeys, b);
+        issue_tile(i, s);
         issued = i + 1;
       }
       // drain: every issued copy has landed before the CTA may exit
@@ -629,8 +671,8 @@ __global__ void __launch_bounds__(kThreads1, 1)
         for (int i = 0; i < ntile; ++i) {
           const int s = i % p.stages;
           const uint32_t ph = (i / p.stages) & 1;
-          const int acc = i & 1;
-          const uint32_t aph = (i >> 1) & 1;
+          const int acc = i & ((1 << acc_sh) - 1);
+          const uint32_t aph = (i >> acc_sh) & 1;
           if (!mbar_wait(&bars->tempty[acc], aph ^ 1, p.budget, abort_v) ||
               !mbar_wait(&bars->full[s], ph, p.budget, abort_v)) {
             fail();
@@ -659,22 +701,24 @@ __global__ void __launch_bounds__(kThreads1, 1)
       // drain: the last MMAs have finished reading shared memory / writing TMEM
       if (issued > 0) {
         const int i = issued - 1;
-        mbar_wait(&bars->tfull[i & 1], (i >> 1) & 1, kDrainBudget, nullptr);
+        mbar_wait(&bars->tfull[i & ((1 << acc_sh) - 1)], (i >> acc_sh) & 1, kDrainBudget, nullptr);
       }
     }
   } else {
     // ---- epilogue warps 2..9: TMEM lane quarter = warp % 4; group e handles
-    // the tiles i = e (mod 2), i.e. TMEM accumulator buffer e
+    // the tiles i = e (mod 2), whose accumulators (i mod 2 or i mod 4) only
+    // this group reads
     const int quarter = warp & 3;
     const int egroup = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t col0 = lane_addr + static_cast<uint32_t>(egroup * p.NC);
     const long long srow0 = static_cast<long long>(b) * p.Tq + j0;
     for (int i = egroup; i < ntile; i += kEpiGroups) {
-      const uint32_t aph = (i >> 1) & 1;
+      const int acc = i & ((1 << acc_sh) - 1);
+      const uint32_t aph = (i >> acc_sh) & 1;
+      const uint32_t col0 = lane_addr + static_cast<uint32_t>(acc * p.NC);
       const int st = i % p.stages;
-      bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->tfull[egroup], aph, p.budget, abort_v));
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->tfull[acc], aph, p.budget, abort_v));
       float kscale = 1.f;
       if (F8 && ok) {
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->full[st], (i / p.stages) & 1, p.budget, abort_v));
@@ -736,7 +780,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->tempty[egroup]);
+      if (lane == 0) mbar_arrive(&bars->tempty[acc]);
     }
   }
 
@@ -771,8 +815,13 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   p.NC = ((p.G * HI + 15) / 16) * 16;
   p.kh = F8 ? 1 : (a.d_I + 63) / 64;  // 128-byte rows: 64 bf16 or 128 E4M3 values
   p.n_groups = (a.Tq + p.G - 1) / p.G;
+  // TMEM columns: two accumulators, four in the one-item kernel on E4M3 keys
+  // when they fit in the 512 columns (NC = G * H_I rounded up: up to 256)
+  const bool single = (a.Tq + p.G - 1) / p.G == 1;
+  p.acc_shift = single && F8 && 4 * p.NC <= 512 ? 2 : 1;
   int cols = 32;
-  while (cols < 2 * p.NC) cols *= 2;
+  while (cols < (1 << p.acc_shift) * p.NC) cols *= 2;
+  if (cols > 512) return cudaErrorNotSupported;
   p.tmem_cols = cols;
   const int q_bytes = p.kh * p.NC * 128;
   const int stage_bytes = p.kh * kHalfBytes;

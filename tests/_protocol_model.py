@@ -62,7 +62,8 @@ def named_barrier(bar: Bar, use: int):
 # indexer_kernel (persistent): a CTA walks a list of items (query group x tile
 # range; ntile may be 0 = nothing visible, skipped by every role).  Key
 # producer -> stage ring -> MMA -> two TMEM accumulators -> two epilogue groups
-# of four warps alternating the CTA's tiles; an item producer fills the
+# of four warps, both on every tile (each group half of the item's queries:
+# eight arrivals free an accumulator); an item producer fills the
 # double-buffered head weights (wfull / wfree) and the single query buffer
 # (qfull, refilled once the MMAs of the previous item are done: qfree); with
 # the histogram both groups meet at every item's end (two named barriers).
@@ -75,13 +76,13 @@ def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "", 
     flushed once).  ``plant`` names a wait to leave out ("qfree", "wfree",
     "sfree"), for the tests that show the hazard checks catch a missing wait.
     ``fp8``: the key scales share the stage ring and a stage's scale slot is
-    released by the four warps of the epilogue group that read it (sfree)."""
+    released by the eight epilogue warps that read it (sfree)."""
     groups = list(range(len(items))) if groups is None else groups
     full = [Bar(1) for _ in range(stages)]
     empty = [Bar(1) for _ in range(stages)]
-    sfree = [Bar(4) for _ in range(stages)]
+    sfree = [Bar(8) for _ in range(stages)]
     scale_tile = [-1] * stages    # the tile whose key scales each stage's slot holds
-    tfull, tempty = [Bar(1), Bar(1)], [Bar(4), Bar(4)]
+    tfull, tempty = [Bar(1), Bar(1)], [Bar(8), Bar(8)]
     qfull, qfree = Bar(1), Bar(1)
     wfull, wfree = [Bar(1), Bar(1)], [Bar(2), Bar(2)]
     group_bar = [Bar(4), Bar(4)]
@@ -163,15 +164,16 @@ def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "", 
             assert w_item[ib] == it, "epilogue read another item's weights"
             for i in range(n):
                 g2 = gt + i
-                if (g2 & 1) != group:
-                    continue
-                yield (tfull[group], (g2 >> 1) & 1)
+                acc = g2 & 1
+                yield (tfull[acc], (g2 >> 1) & 1)
+                assert tfull[acc].done >= (g2 >> 1) + 1 and tempty[acc].done == g2 >> 1, \
+                    "epilogue read an accumulator another tile owns"
                 if fp8:
                     st = g2 % stages
                     yield (full[st], (g2 // stages) & 1)
                     assert scale_tile[st] == g2, "epilogue read another tile's key scales"
                     sfree[st].arrive()
-                tempty[group].arrive()
+                tempty[acc].arrive()
             gt += n
             yield from named_barrier(group_bar[group], it)
             if first:
@@ -188,56 +190,91 @@ def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "", 
 
 
 # ---------------------------------------------------------------------------
-# indexer_single_kernel: one item per CTA -- one producer thread issues the
-# query rows and then the key tiles into the stage ring, the MMA issuer feeds
-# two TMEM accumulators, two epilogue groups of four warps alternate tiles;
-# with FP8 keys each stage's scale slot is released by the group that read it
+# indexer_single_kernel: one item per CTA -- thread 0 requests the query rows
+# and the first min(stages, cap) key tiles before the visibility is known
+# (cap: the item's tiles before the visibility cut; every stage is free then),
+# the producer keeps the ring filled up to the ntile visible tiles, the MMA
+# issuer feeds n_acc TMEM accumulators (2 or 4: tile i goes to i mod n_acc),
+# two epilogue groups of four warps alternate tiles (group g reads the
+# accumulators of the tiles i = g mod 2); with FP8 keys each stage's scale slot is released by the
+# group that read it.  Every issued copy lands before the CTA exits, read or
+# not (a pre-issued tile past the visible range is never read).
 
-def indexer_single(ntile: int, stages: int, seed: int, fp8: bool = False) -> bool:
+def indexer_single(ntile: int, stages: int, seed: int, fp8: bool = False, cap: Optional[int] = None,
+                   n_acc: int = 2, plant: Optional[str] = None) -> bool:
+    cap = ntile if cap is None else cap
+    assert 0 <= ntile <= cap and n_acc in (2, 4)
     full = [Bar(1) for _ in range(stages)]
     empty = [Bar(1) for _ in range(stages)]
     sfree = [Bar(4) for _ in range(stages)]
-    tfull, tempty = [Bar(1), Bar(1)], [Bar(4), Bar(4)]
+    tfull, tempty = [Bar(1) for _ in range(n_acc)], [Bar(4) for _ in range(n_acc)]
+    acc_tile = [-1] * n_acc
     qfull = Bar(1)
     loads = [0] * stages
     scale_tile = [-1] * stages
+    n_pre = min(stages, cap)
+
+    def load(i: int):
+        s = i % stages
+        if fp8:
+            scale_tile[s] = i
+        loads[s] += 1
+        full[s].arrive()
 
     def producer():
         qfull.arrive()
-        for i in range(ntile):
-            s, ph = i % stages, (i // stages) & 1
-            yield (empty[s], ph ^ 1)
-            assert empty[s].done >= i // stages, "stage refilled before its MMAs read it"
-            if fp8:
-                yield (sfree[s], ph ^ 1)
-                assert i < stages or sfree[s].done >= i // stages, "key scales refilled before the epilogue read them"
-                scale_tile[s] = i
-            loads[s] += 1
-            full[s].arrive()
+        for i in range(n_pre):       # before the role split: no wait, every stage free
+            load(i)
+        issued = n_pre
+        if ntile > 0:
+            for i in range(n_pre, ntile):
+                s, ph = i % stages, (i // stages) & 1
+                yield (empty[s], ph ^ 1)
+                assert empty[s].done >= i // stages, "stage refilled before its MMAs read it"
+                if fp8:
+                    yield (sfree[s], ph ^ 1)
+                    assert sfree[s].done >= i // stages, "key scales refilled before the epilogue read them"
+                load(i)
+                issued = i + 1
+        # drain: the last copy issued into each stage has landed
+        for s in range(min(stages, issued)):
+            last = issued - 1 - ((issued - 1 - s) % stages)
+            yield (full[s], (last // stages) & 1)
+        yield (qfull, 0)
 
     def mma():
         yield (qfull, 0)
         for i in range(ntile):
             s, ph = i % stages, (i // stages) & 1
-            acc, aph = i & 1, (i >> 1) & 1
+            acc, aph = i % n_acc, (i // n_acc) & 1
             yield (tempty[acc], aph ^ 1)
             yield (full[s], ph)
             assert loads[s] == i // stages + 1, "MMA read a stage that holds another tile"
-            assert tempty[acc].done >= i >> 1, "accumulator overwritten before the epilogue read it"
+            assert tempty[acc].done >= i // n_acc, "accumulator overwritten before the epilogue read it"
+            acc_tile[acc] = i
             empty[s].arrive()
             tfull[acc].arrive()
 
     def epilogue(group: int):
         for i in range(group, ntile, 2):
-            yield (tfull[group], (i >> 1) & 1)
+            acc = i % n_acc
+            if plant == "group_acc":       # mistake: the two-accumulator indexing kept
+                acc = group
+            yield (tfull[acc], (i // n_acc) & 1)
+            assert acc_tile[acc] == i, "epilogue read another tile's accumulator"
             if fp8:
                 s = i % stages
                 yield (full[s], (i // stages) & 1)
                 assert scale_tile[s] == i, "epilogue read another tile's key scales"
                 sfree[s].arrive()
-            tempty[group].arrive()
+            tempty[acc].arrive()
 
-    return run([producer(), mma()] + [epilogue(g) for g in (0, 1) for _ in range(4)], seed)
+    roles = [producer()]
+    if ntile > 0:   # an item with nothing visible: only thread 0's drain runs
+        roles += [mma()] + [epilogue(g) for g in (0, 1) for _ in range(4)]
+    ok = run(roles, seed)
+    # every copy issued has landed before the CTA exits
+    return ok and all(full[s].done == loads[s] for s in range(stages)) and qfull.done == 1
 
 
 # ---------------------------------------------------------------------------

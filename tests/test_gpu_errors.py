@@ -11,17 +11,28 @@ from long_context_sparse_23_b300 import _lib
 pytestmark = pytest.mark.gpu
 
 
-def test_wait_budget_runs_out_and_context_survives():
+@pytest.mark.parametrize("kernel", ["decode", "prefill"])
+def test_wait_budget_runs_out_and_context_survives(kernel):
+    """Indexer waits with a one-cycle budget.  Each CTA streams tens of key
+    tiles while every SM reads HBM, so its waits for tiles (and for the
+    accumulators of its other epilogue group) last about a tile's streaming
+    time: some wait outlasts the budget.  decode: one query per sequence (the
+    one-item kernel, whose first tiles are requested before any wait);
+    prefill: query groups of four (the persistent kernel)."""
     import long_context_sparse_23_b300 as csa
-    q = S.normal_bf16(1, 2, (2, 1, 64, 128), "cuda")
-    k = S.normal_bf16(1, 12, (2, 4096, 128), "cuda")
+    if kernel == "decode":
+        B, Tq, N = 4, 1, 262144
+    else:
+        B, Tq, N = 1, 16, 65536
+    q = S.normal_bf16(1, 2, (B, Tq, 64, 128), "cuda")
+    k = S.normal_bf16(1, 12, (B, N, 128), "cuda")
     w = S.uniform_f32(1, 9, (64,), "cuda")
-    qp = torch.tensor([[16383], [16383]], dtype=torch.int32, device="cuda")
+    qp = torch.full((B, Tq), 4 * N - 1, dtype=torch.int32, device="cuda") - torch.arange(Tq, device="cuda").int()
     ws = csa.Workspace()
     ref = csa.csa_index_scores(q, k, w, qp, 4, ws=ws)
     assert ws.check_error() == 0
     try:
-        _lib.lib().csa_set_wait_budget(1)       # one clock cycle: the first real wait gives up
+        _lib.lib().csa_set_wait_budget(1)       # one clock cycle: a wait that does not pass at once gives up
         csa.csa_index_scores(q, k, w, qp, 4, ws=ws)
         flags = ws.check_error()
     finally:
@@ -29,7 +40,10 @@ def test_wait_budget_runs_out_and_context_survives():
     assert flags & _lib.CSA_FLAG_TIMEOUT
     again = csa.csa_index_scores(q, k, w, qp, 4, ws=ws)
     assert ws.check_error() == 0
-    assert torch.equal(again, ref)
+    # query j sees its first (t_j + 1) // 4 entries; the rest of its row is not written
+    for j in range(Tq):
+        n = (4 * N - j) // 4
+        assert torch.equal(again[:, j, :n], ref[:, j, :n]), j
 
 
 def _decode_attend_inputs(seed, B, N, k, W, H=64, d=128):

@@ -25,12 +25,30 @@ def test_indexer_protocol_completes_without_hazards():
 
 
 def test_indexer_single_protocol_completes_without_hazards():
-    """The one-item decode indexer, bf16 and FP8 keys."""
+    """The one-item decode indexer, bf16 and FP8 keys, two or four TMEM
+    accumulators: the first stages are requested before the visibility is
+    known, so the visible tile count may fall short of the item's range (down
+    to nothing visible)."""
     rng = random.Random(1)
-    for trial in range(300):
-        ntile = rng.choice([0, 1, 2, 3, 4, 5, 8, 13, 17])
+    for trial in range(400):
+        cap = rng.choice([0, 1, 2, 3, 4, 5, 8, 13, 17])
+        ntile = cap if rng.random() < 0.6 else rng.randint(0, cap)
         stages = rng.choice([2, 3, 5, 8])
-        assert M.indexer_single(ntile, stages, trial, fp8=rng.random() < 0.5), (ntile, stages)
+        n_acc = rng.choice([2, 4])
+        assert M.indexer_single(ntile, stages, trial, fp8=rng.random() < 0.5, cap=cap, n_acc=n_acc), \
+            (ntile, cap, stages, n_acc)
+
+
+def test_indexer_single_wrong_accumulator_is_caught():
+    """Four accumulators read with the two-accumulator indexing (buffer =
+    epilogue group): the model stalls or reads another tile's accumulator."""
+    caught = 0
+    for t in range(200):
+        try:
+            caught += not M.indexer_single(9, 3, t, n_acc=4, plant="group_acc")
+        except AssertionError:
+            caught += 1
+    assert caught == 200
 
 
 @pytest.mark.parametrize("plant", ["qfree", "wfree", "sfree"])
