@@ -36,9 +36,9 @@ HEADLINE = "decode_1m"
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 # DRAM bytes (read + write) per launch of the indexer on the 1M decode
-# workload, from an ncu capture of this launch configuration
-# (profiles/decode_1m_step.md); valid only for the source it was measured on.
-TRAFFIC = {"indexer": {"src_sha": "7c855c7243f5815e", "bytes": 272947712}}
+# workload, from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum)
+# of this launch configuration; valid only for the source it was measured on.
+TRAFFIC = {"indexer": {"src_sha": "9a75d46bc0f91480", "bytes": 272942592}}
 
 
 def _src_sha(*names):
@@ -862,7 +862,7 @@ def main():
     achieved = ibytes / (ms_idx * 1e-3) / 1e9
     sha = _src_sha("indexer.cu", "common.cuh")
     traffic = TRAFFIC["indexer"]["bytes"] if TRAFFIC["indexer"]["src_sha"] == sha else None
-    roof = {"kernel": "indexer_kernel (tcgen05)", "bound": "hbm", "achieved": round(achieved, 1),
+    roof = {"kernel": "indexer_single_kernel (tcgen05)", "bound": "hbm", "achieved": round(achieved, 1),
             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
             "traffic": traffic, "algorithmic_bytes": ibytes, "launch_us": round(ms_idx * 1e3, 2),
             "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.4 TB/s"}
