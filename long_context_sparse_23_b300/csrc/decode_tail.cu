@@ -207,13 +207,23 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     const uint32_t beta = static_cast<uint32_t>(b1.beta);
     uint2* gl = gl_all + static_cast<long long>(r) * E;
     uint32_t* hist2 = a.hist2 + q * kTopkBins;
+    // the lowest scores of buckets beta and beta + 1: the key map is
+    // order-preserving (and folds -0 onto +0, as the float comparison does),
+    // so a finite score is a candidate iff it compares >= tb and in bucket
+    // beta iff also < tb1 (bucket 0 has no lowest value: every score is a
+    // candidate then; above the top bucket nothing is)
+    const float tb = beta == 0 ? -INFINITY : key_score(beta << 20);
+    const float tb1 = beta >= kTopkBins - 1 ? INFINITY : key_score((beta + 1) << 20);
     for (int sub = lo; sub < hi; sub += kT * kRun) {
       if (sub != lo) issue_batch(sub);  // the first batch was requested before the bucket search
       bulk_wait();
       // thread tid owns the run [sub + kRun*tid, sub + kRun*(tid+1)); its 16
-      // float4 reads start at a rotated position (fewer bank conflicts)
+      // float4 reads start at a rotated position (fewer bank conflicts); the
+      // marks are set at the read order's bit positions (constant shifts)
+      // and rotated back to index order once
       const int i0 = sub + kRun * tid;
-      unsigned long long take = 0ull, inb = 0ull;
+      const bool full_run = i0 + kRun <= hi;
+      unsigned long long take_r = 0ull, inb_r = 0ull;
 #pragma unroll
       for (int jr = 0; jr < kRun / 4; ++jr) {
         const int j = (jr + tid) & (kRun / 4 - 1);
@@ -221,13 +231,15 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
         const float v4[4] = {fv.x, fv.y, fv.z, fv.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const uint32_t bin = score_key(v4[e]) >> 20;
-          const bool in = i0 + 4 * j + e < hi;
-          const unsigned long long bit = 1ull << (4 * j + e);
-          take |= (in && bin >= beta) ? bit : 0ull;
-          inb |= (in && bin == beta) ? bit : 0ull;
+          const bool c = (full_run || i0 + 4 * j + e < hi) && v4[e] >= tb;
+          take_r |= static_cast<unsigned long long>(c) << (4 * jr + e);
+          inb_r |= static_cast<unsigned long long>(c && v4[e] < tb1) << (4 * jr + e);
         }
       }
+      // read position 4 jr + e holds element 4 ((jr + tid) mod 16) + e
+      const int rot = 4 * (tid & (kRun / 4 - 1));
+      unsigned long long take = rot ? (take_r << rot) | (take_r >> (64 - rot)) : take_r;
+      const unsigned long long inb = rot ? (inb_r << rot) | (inb_r >> (64 - rot)) : inb_r;
       // bucket beta holds about k of the keys: one reduction per key of it
       for (unsigned long long m2 = inb; m2; m2 &= m2 - 1) {
         const int p = __ffsll(static_cast<long long>(m2)) - 1;
