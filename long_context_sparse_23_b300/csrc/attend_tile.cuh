@@ -44,12 +44,24 @@ __device__ __forceinline__ int swz(int r, int ch) {
   return r * (D * 2) + ((ch ^ (r & 7)) << 4);
 }
 
+// byte offset of chunk ch of row r in a K/V tile: swizzled rows (PITCH = 0),
+// or plain rows PITCH bytes apart (PITCH = D * 2 + 16: each row contiguous,
+// so it can land by one bulk copy, and the 16-byte pad spreads the eight
+// rows of an ldmatrix phase over all banks)
+template <int D, int PITCH>
+__device__ __forceinline__ int kv_off(int r, int ch) {
+  if constexpr (PITCH == 0)
+    return swz<D>(r, ch);
+  else
+    return r * PITCH + (ch << 4);
+}
+
 // One warp's share of one staged tile: keys [key0, key0 + KW) of the K/V
-// tile (rows addressed through swz), slot codes cs[0 .. KW) (-1 = no key),
+// tile (rows addressed through kv_off), slot codes cs[0 .. KW) (-1 = no key),
 // for the warp's 16 query heads (fragments qf).  S = Q K^T on mma.sync, the
 // online softmax in the log2 domain (sl2 = scale * log2 e), then O += P V.
 // Updates the running (o, m, l) of the warp's rows g and g + 8.
-template <int D, int KW>
+template <int D, int KW, int PITCH = 0>
 __device__ __forceinline__ void tile_step(const uint32_t (&qf)[D / 16][4], const char* Kt, const char* Vt,
                                           int key0, const int* cs, float sl2, float (&o)[D / 8][4], float& m0,
                                           float& m1, float& l0, float& l1) {
@@ -71,7 +83,7 @@ __device__ __forceinline__ void tile_step(const uint32_t (&qf)[D / 16][4], const
       uint32_t r[4];
       const int key = key0 + jp * 16 + ((lane >> 4) << 3) + (lane & 7);
       const int ch = 2 * kk + ((lane >> 3) & 1);
-      ldsm_x4(r, Kt + swz<D>(key, ch));
+      ldsm_x4(r, Kt + kv_off<D, PITCH>(key, ch));
       mma_16816(s[2 * jp], qf[kk], r[0], r[1]);
       mma_16816(s[2 * jp + 1], qf[kk], r[2], r[3]);
     }
@@ -128,7 +140,7 @@ __device__ __forceinline__ void tile_step(const uint32_t (&qf)[D / 16][4], const
       uint32_t r[4];
       const int key = key0 + kk * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
       const int ch = 2 * dp + (lane >> 4);
-      ldsm_x4_t(r, Vt + swz<D>(key, ch));
+      ldsm_x4_t(r, Vt + kv_off<D, PITCH>(key, ch));
       mma_16816(o[2 * dp], af, r[0], r[1]);
       mma_16816(o[2 * dp + 1], af, r[2], r[3]);
     }

@@ -47,6 +47,9 @@ constexpr int kC = kTailCluster;  // CTAs per query (one cluster)
 constexpr int kCandR = 512;     // candidates of one rank staged in shared memory
 constexpr int kRun = 64;        // consecutive scores per thread in the candidate scan
 constexpr int kBulk = 16384;    // bytes per bulk copy
+// K/V tile rows: contiguous, 16 bytes of padding (one bulk copy per row)
+template <int D>
+constexpr int kv_pitch() { return D * 2 + 16; }
 // A wait that ran out of the call's budget is reported and then continued
 // with this budget (about one second), so that no bulk copy is still writing
 // this CTA's shared memory when the buffer is refilled or the CTA exits.
@@ -71,7 +74,7 @@ __host__ __device__ inline TailLayout tail_layout(int S_r, int H, int D, int E) 
   const int lists = kC * kCandR * 8;
   const int sel_end = scores > lists ? scores : lists;
   L.kv = (sel_end + 127) / 128 * 128;
-  L.codes = L.kv + 2 * S_r * D * 2;
+  L.codes = L.kv + 2 * S_r * (D * 2 + 16);
   const int kv_end = L.codes + S_r * 4;
   L.merge = 0;  // [2][H][ldo] o, then [2][H] m, [2][H] l, then [H][4] push weights
   const int merge_end = L.merge + (2 * H * ldo + 4 * H + 4 * H) * 4;
@@ -117,12 +120,13 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
   float* recv = reinterpret_cast<float*>(smem + L.recv);  // [hpc][kC][LDO]
   float* recv_m = recv + L.hpc * kC * LDO;                // [hpc][kC]
   float* recv_l = recv_m + L.hpc * kC;                    // [hpc][kC]
-  __shared__ __align__(8) uint64_t bar, bar_q;
+  __shared__ __align__(8) uint64_t bar, bar_q, bar_g;
   __shared__ uint32_t rcnt[kC], wg[kT / 32], we[kT / 32];
   uint32_t bar_phase = 0;
   if (tid == 0) {
     mbar_init(&bar, 1);
     mbar_init(&bar_q, 1);
+    mbar_init(&bar_g, 1);
     mbar_fence_init();
   }
   __syncthreads();
@@ -143,6 +147,7 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
 
   const int b = static_cast<int>(q / at.Tq);
   const int t = a.q_pos[q];
+  const int raw_base = at.W > 0 ? at.raw_base[b] : 0;  // read now: step 3's window slots need it
   int n_vis = t >= 0 ? (t + 1) / a.m : 0;
   n_vis = n_vis < a.N ? n_vis : a.N;
   const int k = a.k;
@@ -160,12 +165,14 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
   }
   // K/V tile of this CTA's key slots (gathered in step 3)
   char* Ks = smem + L.kv;
-  char* Vs = Ks + S_r * D * 2;
+  constexpr int PITCH = kv_pitch<D>();
+  char* Vs = Ks + S_r * PITCH;
   const char* kc_base = static_cast<const char*>(at.k_cmp) + static_cast<size_t>(b) * at.N * D * 2;
   const char* vc_base = static_cast<const char*>(at.v_cmp) + static_cast<size_t>(b) * at.N * D * 2;
 
-  // Everything above reads only the call's inputs (query positions and
-  // rows), which no kernel of this call writes; the kernel launched before
+  // Everything above reads only the call's inputs (query positions, the
+  // window's base position, the query rows), which no kernel of this call
+  // writes; the kernel launched before
   // this one's predecessor has completed when this kernel starts (each
   // kernel releases its dependents after its own wait, the indexer after
   // the histogram-zeroing kernel's).  The scores and histograms below are
@@ -383,14 +390,16 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
   if (r < A) {
     int* codes = reinterpret_cast<int*>(smem + L.codes);
     const int s0 = r * S_r;
-    const int raw_base = at.W > 0 ? at.raw_base[b] : 0;
+    const char* kr_base = static_cast<const char*>(at.k_raw) + static_cast<size_t>(b) * at.T_raw * D * 2;
+    const char* vr_base = static_cast<const char*>(at.v_raw) + static_cast<size_t>(b) * at.T_raw * D * 2;
     bool bad = false;
-    // slot codes: kept blocks, then window rows, then nothing
-    for (int j = tid; j < S_r; j += kT) {
-      const int s = s0 + j;
-      int code = -1;
+    // slot codes: kept blocks, then window rows, then nothing (one slot per
+    // thread: S_r <= kT)
+    int my_code = -1;
+    if (tid < S_r) {
+      const int s = s0 + tid;
       if (s < k) {
-        code = all ? (s < n_vis ? s : -1) : map[j];
+        my_code = all ? (s < n_vis ? s : -1) : map[tid];
       } else if (s < K_total) {
         const int u = t - at.W + 1 + (s - k);
         if (u >= 0) {
@@ -398,27 +407,34 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
           if (rr < 0 || rr >= at.T_raw)
             bad = true;
           else
-            code = -rr - 2;
+            my_code = -rr - 2;
         }
       }
-      codes[j] = code;
+      codes[tid] = my_code;
     }
     if (bad) raise_flag(at.errw, kFlagIndex);
-    __syncthreads();
-    const char* kr_base = static_cast<const char*>(at.k_raw) + static_cast<size_t>(b) * at.T_raw * D * 2;
-    const char* vr_base = static_cast<const char*>(at.v_raw) + static_cast<size_t>(b) * at.T_raw * D * 2;
-    for (int i = tid; i < S_r * CH; i += kT) {
-      const int rw = i / CH, ch = i % CH;
-      const int code = codes[rw];
-      const char* kp = code >= 0 ? kc_base + static_cast<size_t>(code) * D * 2
-                                 : kr_base + static_cast<size_t>(code <= -2 ? -code - 2 : 0) * D * 2;
-      const char* vp = code >= 0 ? vc_base + static_cast<size_t>(code) * D * 2
-                                 : vr_base + static_cast<size_t>(code <= -2 ? -code - 2 : 0) * D * 2;
-      const bool valid = code != -1;
-      cp_async16(Ks + swz<D>(rw, ch), valid ? kp + ch * 16 : kc_base, valid);
-      cp_async16(Vs + swz<D>(rw, ch), valid ? vp + ch * 16 : vc_base, valid);
+    // each slot's K and V rows by two bulk copies onto bar_g (thread 0
+    // announces the bytes of every valid slot; a copy may land before the
+    // announcement, the phase completes only after it); an empty slot's rows
+    // are zeroed (its probability is 0, and 0 * garbage could be NaN)
+    const int n_valid = __syncthreads_count(my_code != -1);
+    if (tid == 0) mbar_expect_tx(&bar_g, static_cast<uint32_t>(n_valid * 2 * D * 2));
+    if (tid < S_r) {
+      if (my_code != -1) {
+        const char* kp = my_code >= 0 ? kc_base + static_cast<size_t>(my_code) * D * 2
+                                      : kr_base + static_cast<size_t>(-my_code - 2) * D * 2;
+        const char* vp = my_code >= 0 ? vc_base + static_cast<size_t>(my_code) * D * 2
+                                      : vr_base + static_cast<size_t>(-my_code - 2) * D * 2;
+        bulk_g2s(Ks + tid * PITCH, kp, D * 2, &bar_g);
+        bulk_g2s(Vs + tid * PITCH, vp, D * 2, &bar_g);
+      } else {
+#pragma unroll
+        for (int c16 = 0; c16 < D * 2; c16 += 16) {
+          *reinterpret_cast<uint4*>(Ks + tid * PITCH + c16) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(Vs + tid * PITCH + c16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
     }
-    cp_async_commit();
     // Q fragments of head group hg (rows hg*16 + g and + 8) from shared memory
     const int hg = warp & 3, kh = warp >> 2;
     const int g = lane >> 2, c = lane & 3;
@@ -444,12 +460,15 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     for (int i = 0; i < DT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     const float sl2 = at.scale * kLog2e;
-    cp_async_wait<0>();
-    __syncthreads();
+    if (!mbar_wait(&bar_g, 0, a.budget, nullptr)) {
+      raise_flag(at.errw, kFlagTimeout);
+      mbar_wait(&bar_g, 0, kDrainBudget, nullptr);
+    }
+    __syncthreads();  // the zeroed rows too
     if (hg * 16 < H) {
       const int half = S_r / 2;
       for (int kb = 0; kb < half; kb += KH)
-        tile_step<D, KH>(qf, Ks, Vs, kh * half + kb, codes + kh * half + kb, sl2, o, m0, m1, l0, l1);
+        tile_step<D, KH, PITCH>(qf, Ks, Vs, kh * half + kb, codes + kh * half + kb, sl2, o, m0, m1, l0, l1);
     }
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
