@@ -197,13 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->qfree, 1);
     mbar_fence_init();
   }
-  // does this CTA own any visible tile? (the same answer in every thread)
-  bool any = false;
-  for (int k = 0; !any; ++k) {
-    const int r = rank_of(k, p);
-    if (r < 0) break;
-    any = item_of(p, r).ntile > 0;
-  }
+  // does this CTA own any item? (the same answer in every thread; an item
+  // with nothing visible is skipped by every role, so its visibility, a
+  // global read, is left to the roles rather than delaying the first copy)
+  const bool any = rank_of(0, p) >= 0;
   __syncthreads();
   if (!any) return;
 
