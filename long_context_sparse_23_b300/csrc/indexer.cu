@@ -413,24 +413,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->sfree[st]);
         }
+        bool released = false;
         if (!ok) {
           if (lane == 0) fail();
         } else {
           tc_fence_after();
           const int key = tile_at(I, i) * kTileKeys + row;
           if constexpr (HI >= 16) {
-            for (int jj = jlo; jj < jhi; ++jj) {
-              // all of the query's head columns in flight at once, one wait
-              uint32_t rr[HI / 16][16];
+            // this group's half of the accumulator (G / 2 queries x H_I heads
+            // = 128 columns: here G = 256 / H_I) into registers, then the
+            // accumulator is released before the reduction, so the MMAs of
+            // tile gt + 2 need not wait for it
+            constexpr int NQ = 128 / HI;
+            uint32_t rv[8][16];
 #pragma unroll
-              for (int hc = 0; hc < HI / 16; ++hc) tmem_ld16(col0 + jj * HI + hc * 16, rr[hc]);
-              tmem_ld_wait();
+            for (int c = 0; c < 8; ++c) tmem_ld16(col0 + jlo * HI + c * 16, rv[c]);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+            released = true;
+#pragma unroll
+            for (int jq = 0; jq < NQ; ++jq) {
+              const int jj = jlo + jq;
               const float* wq = wi + jj * HI;
               float sum = 0.f;
 #pragma unroll
-              for (int hc = 0; hc < HI / 16; ++hc)
-#pragma unroll
-                for (int e = 0; e < 16; ++e) sum = fmaf(wq[hc * 16 + e], fmaxf(__uint_as_float(rr[hc][e]), 0.f), sum);
+              for (int h = 0; h < HI; ++h)
+                sum = fmaf(wq[h], fmaxf(__uint_as_float(rv[(jq * HI + h) >> 4][(jq * HI + h) & 15]), 0.f), sum);
               if (F8) sum *= kscale;
               const bool vis = key < nvi[jj];
               if (vis) p.S[(srow0 + jj) * p.ld + key] = sum;
@@ -464,9 +474,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+        if (!released) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+        }
       }
       gt += I.ntile;
       // this group is done with the item's weights and visibility
