@@ -12,7 +12,7 @@
 // columns -- no cross-thread reduction.  A work item is one query group
 // against a range of 128-key tiles; TMA feeds a 128-byte-swizzled shared-
 // memory ring of key tiles, one thread issues tcgen05.mma into TMEM
-// accumulators, and two groups of four epilogue warps read them (tcgen05.ld,
+// accumulators, and groups of four epilogue warps read them (tcgen05.ld,
 // ReLU and the head weights, coalesced fp32 scores, the top-k bucket
 // histogram).  Two kernels:
 //   indexer_single_kernel  decode (one query group per sequence): one item
@@ -21,9 +21,9 @@
 //   indexer_kernel         prefill (query groups of every causal length):
 //                          persistent, one CTA per SM walking its items
 //                          (heavy first, snake order), an item producer warp
-//                          loading each item's weights and query rows; both
-//                          epilogue groups on every tile, half the queries
-//                          each.
+//                          loading each item's weights and query rows; every
+//                          epilogue group on every tile, its share of the
+//                          queries copied to registers before the reduction.
 // mbarriers connect the stages (full/empty per smem stage, full/empty per
 // TMEM buffer); every wait is bounded and reports CSA_FLAG_TIMEOUT instead of
 // hanging.  Tiles past the group's last visible block are never loaded, but
@@ -38,7 +38,12 @@ namespace {
 
 constexpr int kEpiGroups = 2;                      // epilogue warp groups
 constexpr int kEpiWarp0 = 3;                       // first epilogue warp
-constexpr int kThreads = 32 * kEpiWarp0 + 128 * kEpiGroups;  // 3 role warps + 8 epilogue warps
+// The persistent kernel's epilogue groups: four when a group's share of the
+// 256 accumulator columns (64) holds whole queries (H_I <= 64), else two.
+template <int HI>
+constexpr int epi_groups_p() { return HI <= 64 ? 4 : 2; }
+template <int HI>
+constexpr int threads_p() { return 32 * kEpiWarp0 + 128 * epi_groups_p<HI>(); }
 constexpr int kTileKeys = 128;
 constexpr int kHalfBytes = kTileKeys * 128;  // one 64-wide K half of a key tile
 constexpr int kMaxG = 64;                    // queries per group (H_I >= 4, G * H_I <= 256)
@@ -136,24 +141,25 @@ __device__ __forceinline__ int rank_of(int k, const KParams& p) {
 __device__ __forceinline__ void group_bar(int g) {
   asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
 }
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
+template <int NT>
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 5, %0;" ::"n"(NT) : "memory"); }
 
 // Persistent kernel: one CTA per SM walks its items; the key ring, the TMEM
 // accumulator pair and the item buffers run on across item boundaries.
-// Warp roles (352 threads):
+// Warp roles (608 threads for H_I <= 64, 352 for H_I = 128):
 //   warp 0      key producer: TMA key tiles into the S-stage ring;
 //   warp 1      allocates TMEM; one lane issues the MMAs;
 //   warp 2      item producer: per item, the head weights and visibility
 //               (double-buffered) and the query rows (TMA, one buffer, loaded
 //               once the previous item's MMAs are done; the next item's rows
 //               are prefetched into L2 meanwhile);
-//   warps 3-10  epilogue, two groups of four, both on every tile (half the
-//               queries each).
+//   warps 3..   epilogue, four groups of four (two for H_I = 128), all on
+//               every tile, each group its share of the group's queries.
 // F8: keys and queries are E4M3 codes (one 128-byte row per key / query head,
 // one power-of-two scale per row); the MMAs are kind::f8f6f4 and the
 // epilogue applies the scales: sum_h (w_h s_q,h) ReLU(acc_h) * s_k.
 template <int HI, bool F8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_p<HI>(), 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tms, KParams p) {
   if (p.after_zero) {
@@ -179,19 +185,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (p.hist)
-    for (int i = tid; i < kTopkBins; i += kThreads) hist_s[i] = 0u;
+    for (int i = tid; i < kTopkBins; i += threads_p<HI>()) hist_s[i] = 0u;
   if (tid == 0) {
     abort_flag = 0;
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
-      mbar_init(&bars->sfree[s], 4 * kEpiGroups);
+      mbar_init(&bars->sfree[s], 4 * epi_groups_p<HI>());
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->tfull[i], 1);
-      mbar_init(&bars->tempty[i], 4 * kEpiGroups);
+      mbar_init(&bars->tempty[i], 4 * epi_groups_p<HI>());
       mbar_init(&bars->wfull[i], 1);
-      mbar_init(&bars->wfree[i], kEpiGroups);
+      mbar_init(&bars->wfree[i], epi_groups_p<HI>());
     }
     mbar_init(&bars->qfull, 1);
     mbar_init(&bars->qfree, 1);
@@ -367,20 +373,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // drain: the last query copy has landed before the CTA may exit
     if (lane == 0 && q_issued > 0) mbar_wait(&bars->qfull, (q_issued - 1) & 1, kDrainBudget, nullptr);
   } else {
-    // ---- epilogue warps: TMEM lane quarter = warp % 4; both groups take
-    // every tile (TMEM accumulator gt mod 2), group e its half of the
+    // ---- epilogue warps: TMEM lane quarter = warp % 4; every group takes
+    // every tile (TMEM accumulator gt mod 2), group e its share of the
     // group's queries (H_I >= 16) or of the 16-column chunks (H_I < 16), so
-    // a tile's epilogue takes half as long and the MMAs into the other
+    // a tile's epilogue is split EG ways and the MMAs into the other
     // accumulator hide it
     const int ew = warp - kEpiWarp0;
     const int egroup = ew >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int qh = (p.G + 1) / 2;
-    const int jlo = egroup * qh, jhi = min(p.G, jlo + qh);
-    const int ch_h = (p.NC / 16 + 1) / 2;
-    const int clo = egroup * ch_h * 16, chi = min(p.NC, (egroup + 1) * ch_h * 16);
+    constexpr int EG = epi_groups_p<HI>();
+    const int qh = (p.G + EG - 1) / EG;
+    const int jlo = min(p.G, egroup * qh), jhi = min(p.G, jlo + qh);
+    const int ch_h = (p.NC / 16 + EG - 1) / EG;
+    const int clo = min(p.NC, egroup * ch_h * 16), chi = min(p.NC, (egroup + 1) * ch_h * 16);
     int gt = 0, it = 0;
     bool waited_zero = false;
     for (int k = 0;; ++k) {
@@ -420,14 +427,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const int key = tile_at(I, i) * kTileKeys + row;
           if constexpr (HI >= 16) {
-            // this group's half of the accumulator (G / 2 queries x H_I heads
-            // = 128 columns: here G = 256 / H_I) into registers, then the
-            // accumulator is released before the reduction, so the MMAs of
-            // tile gt + 2 need not wait for it
-            constexpr int NQ = 128 / HI;
-            uint32_t rv[8][16];
+            // this group's share of the accumulator (G / EG queries x H_I
+            // heads = 256 / EG columns: here G = 256 / H_I) into registers,
+            // then the accumulator is released before the reduction, so the
+            // MMAs of tile gt + 2 need not wait for it
+            constexpr int NQ = 256 / EG / HI;
+            constexpr int NCH = 256 / EG / 16;
+            uint32_t rv[NCH][16];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) tmem_ld16(col0 + jlo * HI + c * 16, rv[c]);
+            for (int c = 0; c < NCH; ++c) tmem_ld16(col0 + jlo * HI + c * 16, rv[c]);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
@@ -487,20 +495,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.hist) {
         // both groups' counts of the item are in: flush them (once the
         // histogram has been zeroed), then clear for the next item
-        epi_bar();
+        epi_bar<128 * EG>();
         if (p.after_zero && !waited_zero) {
           asm volatile("griddepcontrol.wait;" ::: "memory");
           waited_zero = true;
         }
         uint32_t* g = p.hist + srow0 * kTopkBins;
-        for (int i = ew * 32 + lane; i < kTopkBins; i += 32 * 4 * kEpiGroups) {
+        for (int i = ew * 32 + lane; i < kTopkBins; i += 32 * 4 * EG) {
           const uint32_t v = hist_s[i];
           if (v) {
             atomicAdd(g + i, v);
             hist_s[i] = 0u;
           }
         }
-        epi_bar();
+        epi_bar<128 * EG>();
       }
       ++it;
     }
@@ -914,7 +922,7 @@ cudaError_t launch_hi(const IndexerArgs& a, cudaStream_t s) {
   }
   cudaError_t e = ensure_dyn_smem<indexer_kernel<HI, F8>>(static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_k(indexer_kernel<HI, F8>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, s, 1, tmk, tmq,
+  return launch_k(indexer_kernel<HI, F8>, dim3(static_cast<unsigned>(grid)), dim3(threads_p<HI>()), smem, s, 1, tmk, tmq,
                   tms, p);
 }
 

@@ -69,30 +69,33 @@ def named_barrier(bar: Bar, use: int):
 # the histogram both groups meet at every item's end (two named barriers).
 
 def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "", fp8: bool = False,
-            groups=None) -> bool:
+            groups=None, epi_groups: int = 2) -> bool:
     """``items``: tile counts of the CTA's items in order (0 = nothing
     visible, skipped); ``groups``: the query group of each item (consecutive
     items of one group share the query rows, loaded once, and the histogram,
     flushed once).  ``plant`` names a wait to leave out ("qfree", "wfree",
     "sfree"), for the tests that show the hazard checks catch a missing wait.
     ``fp8``: the key scales share the stage ring and a stage's scale slot is
-    released by the eight epilogue warps that read it (sfree)."""
+    released by the epilogue warps that read it (sfree).  ``epi_groups``:
+    epilogue groups of four warps (two, or four when H_I <= 64), all on
+    every tile."""
+    nw = 4 * epi_groups
     groups = list(range(len(items))) if groups is None else groups
     full = [Bar(1) for _ in range(stages)]
     empty = [Bar(1) for _ in range(stages)]
-    sfree = [Bar(8) for _ in range(stages)]
+    sfree = [Bar(nw) for _ in range(stages)]
     scale_tile = [-1] * stages    # the tile whose key scales each stage's slot holds
-    tfull, tempty = [Bar(1), Bar(1)], [Bar(8), Bar(8)]
+    tfull, tempty = [Bar(1), Bar(1)], [Bar(nw), Bar(nw)]
     qfull, qfree = Bar(1), Bar(1)
-    wfull, wfree = [Bar(1), Bar(1)], [Bar(2), Bar(2)]
-    group_bar = [Bar(4), Bar(4)]
-    epi_bar = Bar(8)
+    wfull, wfree = [Bar(1), Bar(1)], [Bar(epi_groups), Bar(epi_groups)]
+    group_bar = [Bar(4) for _ in range(epi_groups)]
+    epi_bar = Bar(nw)
     live = [(n, g) for n, g in zip(items, groups) if n > 0]
     loads = [0] * stages
     q_group = [None]              # the query group whose rows the buffer holds
     w_item = [-1, -1]             # the item whose weights each buffer holds
     mma_groups_done = [0]         # query groups whose MMAs have completed
-    epi_done = [[0, 0], [0, 0]]   # [buffer][group]: items of that buffer parity finished by the group
+    epi_done = [[0] * epi_groups, [0] * epi_groups]  # [buffer][group]: items of that parity finished by the group
 
     def new_group(it):
         return it == 0 or live[it][1] != live[it - 1][1]
@@ -185,7 +188,7 @@ def indexer(items, stages: int, seed: int, hist: bool = False, plant: str = "", 
                 uses += 2
 
     roles = [key_producer(), item_producer(), mma()]
-    roles += [epilogue(g, w == 0) for g in (0, 1) for w in range(4)]
+    roles += [epilogue(g, w == 0) for g in range(epi_groups) for w in range(4)]
     return run(roles, seed)
 
 

@@ -21,7 +21,8 @@ def test_indexer_protocol_completes_without_hazards():
         stages = rng.choice([2, 3, 4, 5, 8])
         hist = rng.random() < 0.5
         fp8 = rng.random() < 0.5
-        assert M.indexer(items, stages, trial, hist, fp8=fp8), (items, stages, hist, fp8)
+        eg = rng.choice([2, 4])
+        assert M.indexer(items, stages, trial, hist, fp8=fp8, epi_groups=eg), (items, stages, hist, fp8, eg)
 
 
 def test_indexer_single_protocol_completes_without_hazards():
