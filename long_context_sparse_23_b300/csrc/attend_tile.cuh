@@ -46,8 +46,8 @@ __device__ __forceinline__ int swz(int r, int ch) {
 
 // byte offset of chunk ch of row r in a K/V tile: swizzled rows (PITCH = 0),
 // or plain rows PITCH bytes apart (PITCH = D * 2 + 16: each row contiguous,
-// so it can land by one bulk copy, and the 16-byte pad spreads the eight
-// rows of an ldmatrix phase over all banks)
+// and the 16-byte pad spreads the eight rows of an ldmatrix phase over all
+// banks)
 template <int D, int PITCH>
 __device__ __forceinline__ int kv_off(int r, int ch) {
   if constexpr (PITCH == 0)

@@ -47,7 +47,7 @@ constexpr int kC = kTailCluster;  // CTAs per query (one cluster)
 constexpr int kCandR = 512;     // candidates of one rank staged in shared memory
 constexpr int kRun = 64;        // consecutive scores per thread in the candidate scan
 constexpr int kBulk = 16384;    // bytes per bulk copy
-// K/V tile rows: contiguous, 16 bytes of padding (one bulk copy per row)
+// K/V tile rows: contiguous, 16 bytes of padding (conflict-free ldmatrix)
 template <int D>
 constexpr int kv_pitch() { return D * 2 + 16; }
 // A wait that ran out of the call's budget is reported and then continued
@@ -120,13 +120,12 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
   float* recv = reinterpret_cast<float*>(smem + L.recv);  // [hpc][kC][LDO]
   float* recv_m = recv + L.hpc * kC * LDO;                // [hpc][kC]
   float* recv_l = recv_m + L.hpc * kC;                    // [hpc][kC]
-  __shared__ __align__(8) uint64_t bar, bar_q, bar_g;
+  __shared__ __align__(8) uint64_t bar, bar_q;
   __shared__ uint32_t rcnt[kC], wg[kT / 32], we[kT / 32];
   uint32_t bar_phase = 0;
   if (tid == 0) {
     mbar_init(&bar, 1);
     mbar_init(&bar_q, 1);
-    mbar_init(&bar_g, 1);
     mbar_fence_init();
   }
   __syncthreads();
@@ -413,25 +412,39 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
       codes[tid] = my_code;
     }
     if (bad) raise_flag(at.errw, kFlagIndex);
-    // each slot's K and V rows by two bulk copies onto bar_g (thread 0
-    // announces the bytes of every valid slot; a copy may land before the
-    // announcement, the phase completes only after it); an empty slot's rows
-    // are zeroed (its probability is 0, and 0 * garbage could be NaN)
-    const int n_valid = __syncthreads_count(my_code != -1);
-    if (tid == 0) mbar_expect_tx(&bar_g, static_cast<uint32_t>(n_valid * 2 * D * 2));
-    if (tid < S_r) {
-      if (my_code != -1) {
-        const char* kp = my_code >= 0 ? kc_base + static_cast<size_t>(my_code) * D * 2
-                                      : kr_base + static_cast<size_t>(-my_code - 2) * D * 2;
-        const char* vp = my_code >= 0 ? vc_base + static_cast<size_t>(my_code) * D * 2
-                                      : vr_base + static_cast<size_t>(-my_code - 2) * D * 2;
-        bulk_g2s(Ks + tid * PITCH, kp, D * 2, &bar_g);
-        bulk_g2s(Vs + tid * PITCH, vp, D * 2, &bar_g);
-      } else {
+    // each slot's K and V rows: all 256 threads load 16-byte chunks
+    // (consecutive threads on consecutive chunks of a row; every load of a
+    // thread issued before the first store) and store them into the padded
+    // rows; an empty slot's rows are zeroed (its probability is 0, and
+    // 0 * garbage could be NaN)
+    __syncthreads();  // codes[] written
+    {
+      constexpr int NPT = (kTailMaxSlots * CH + kT - 1) / kT;  // chunks per thread at most
+      uint4 kv[NPT][2];
 #pragma unroll
-        for (int c16 = 0; c16 < D * 2; c16 += 16) {
-          *reinterpret_cast<uint4*>(Ks + tid * PITCH + c16) = make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(Vs + tid * PITCH + c16) = make_uint4(0u, 0u, 0u, 0u);
+      for (int u = 0; u < NPT; ++u) {
+        const int i = tid + u * kT;
+        kv[u][0] = kv[u][1] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < S_r * CH) {
+          const int rw = i / CH, ch = i % CH;
+          const int code = codes[rw];
+          if (code != -1) {
+            const char* kp = code >= 0 ? kc_base + static_cast<size_t>(code) * D * 2
+                                       : kr_base + static_cast<size_t>(-code - 2) * D * 2;
+            const char* vp = code >= 0 ? vc_base + static_cast<size_t>(code) * D * 2
+                                       : vr_base + static_cast<size_t>(-code - 2) * D * 2;
+            kv[u][0] = __ldg(reinterpret_cast<const uint4*>(kp + ch * 16));
+            kv[u][1] = __ldg(reinterpret_cast<const uint4*>(vp + ch * 16));
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < NPT; ++u) {
+        const int i = tid + u * kT;
+        if (i < S_r * CH) {
+          const int rw = i / CH, ch = i % CH;
+          *reinterpret_cast<uint4*>(Ks + rw * PITCH + ch * 16) = kv[u][0];
+          *reinterpret_cast<uint4*>(Vs + rw * PITCH + ch * 16) = kv[u][1];
         }
       }
     }
@@ -460,11 +473,7 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     for (int i = 0; i < DT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     const float sl2 = at.scale * kLog2e;
-    if (!mbar_wait(&bar_g, 0, a.budget, nullptr)) {
-      raise_flag(at.errw, kFlagTimeout);
-      mbar_wait(&bar_g, 0, kDrainBudget, nullptr);
-    }
-    __syncthreads();  // the zeroed rows too
+    __syncthreads();  // every slot's rows stored
     if (hg * 16 < H) {
       const int half = S_r / 2;
       for (int kb = 0; kb < half; kb += KH)
