@@ -751,12 +751,22 @@ __global__ void __launch_bounds__(kThreads1, 1)
       }
       tc_fence_after();
       const int key = (tile_lo + i) * kTileKeys + row;
+      bool released = false;
       if constexpr (HI >= 16) {
         for (int jj = 0; jj < p.G; ++jj) {
           uint32_t rr[HI / 16][16];
 #pragma unroll
           for (int hc = 0; hc < HI / 16; ++hc) tmem_ld16(col0 + jj * HI + hc * 16, rr[hc]);
           tmem_ld_wait();
+          if (!F8 && p.G == 1) {
+            // one query: its columns are in registers, the accumulator is
+            // released before the reduction (measured with bf16 keys; the
+            // E4M3 kernel keeps four accumulators instead)
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+            released = true;
+          }
           const float* wq = w_s + jj * HI;
           float sum = 0.f;
 #pragma unroll
@@ -795,9 +805,11 @@ __global__ void __launch_bounds__(kThreads1, 1)
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+      if (!released) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+      }
     }
   }
 
