@@ -38,7 +38,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch of the indexer on the 1M decode
 # workload, from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum)
 # of this launch configuration; valid only for the source it was measured on.
-TRAFFIC = {"indexer": {"src_sha": "9a75d46bc0f91480", "bytes": 272942592}}
+TRAFFIC = {"indexer": {"src_sha": "0fd2e310cf61bfb5", "bytes": 273218816}}
 
 
 def _src_sha(*names):
