@@ -10,8 +10,9 @@
 // with a cluster barrier between them:
 //  1. CTA r scans its chunk [r*E, (r+1)*E) of the scores and keeps, in index
 //     order, every key whose bucket is >= beta, the bucket holding the k-th
-//     largest key (candidates: in global memory, staged in shared memory when
-//     they fit);
+//     largest key (candidates: in global memory, and, when they fit, pushed
+//     by one bulk copy per CTA into every CTA's shared memory before the
+//     barrier);
 //  2. every CTA reads the candidates of bucket beta and fixes the same exact
 //     rule (prefix, mask, k_rem) with a histogram of key bits 19..8 and at
 //     most one 8-bit pass: keys above the prefix are kept, and of the keys
@@ -44,7 +45,7 @@ namespace {
 
 constexpr int kT = 256;         // threads per CTA
 constexpr int kC = kTailCluster;  // CTAs per query (one cluster)
-constexpr int kCandR = 512;     // candidates of one rank staged in shared memory
+constexpr int kCandP = 256;     // candidates of one rank pushed to every CTA of the cluster
 constexpr int kRun = 64;        // consecutive scores per thread in the candidate scan
 constexpr int kBulk = 16384;    // bytes per bulk copy
 // K/V tile rows: contiguous, 16 bytes of padding (conflict-free ldmatrix)
@@ -62,6 +63,8 @@ struct TailLayout {
   int merge;      // step 3: the two key halves' partials (overlap the above once consumed)
   int map, recv;  // persistent: rank -> block of this CTA's slots, partials of its heads
   int qs;         // persistent: the query's rows [H][D] bf16
+  int own;        // this rank's first kCandP candidates (the source of its pushes)
+  int plist;      // every rank's pushed candidates [kC][kCandP]
   int total;
   int hpc;        // heads owned per CTA
 };
@@ -71,8 +74,7 @@ __host__ __device__ inline TailLayout tail_layout(int S_r, int H, int D, int E) 
   const int ldo = D + 4;
   L.stage = 0;
   const int scores = (E < kT * kRun ? E : kT * kRun) * 4;
-  const int lists = kC * kCandR * 8;
-  const int sel_end = scores > lists ? scores : lists;
+  const int sel_end = scores;
   L.kv = (sel_end + 127) / 128 * 128;
   L.codes = L.kv + 2 * S_r * (D * 2 + 16);
   const int kv_end = L.codes + S_r * 4;
@@ -83,7 +85,9 @@ __host__ __device__ inline TailLayout tail_layout(int S_r, int H, int D, int E) 
   L.recv = L.map + (S_r * 4 + 15) / 16 * 16;
   L.hpc = (H + kC - 1) / kC;
   L.qs = L.recv + ((L.hpc * kC * ldo + 2 * L.hpc * kC) * 4 + 127) / 128 * 128;
-  L.total = L.qs + H * D * 2;
+  L.own = L.qs + H * D * 2;
+  L.plist = L.own + kCandP * 8;
+  L.total = L.plist + kC * kCandP * 8;
   return L;
 }
 
@@ -120,12 +124,13 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
   float* recv = reinterpret_cast<float*>(smem + L.recv);  // [hpc][kC][LDO]
   float* recv_m = recv + L.hpc * kC * LDO;                // [hpc][kC]
   float* recv_l = recv_m + L.hpc * kC;                    // [hpc][kC]
-  __shared__ __align__(8) uint64_t bar, bar_q;
+  __shared__ __align__(8) uint64_t bar, bar_q, bar_l;
   __shared__ uint32_t rcnt[kC], wg[kT / 32], we[kT / 32];
   uint32_t bar_phase = 0;
   if (tid == 0) {
     mbar_init(&bar, 1);
     mbar_init(&bar_q, 1);
+    mbar_init(&bar_l, 1);
     mbar_fence_init();
   }
   __syncthreads();
@@ -213,6 +218,7 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     const uint32_t beta = static_cast<uint32_t>(b1.beta);
     uint2* gl = gl_all + static_cast<long long>(r) * E;
     uint32_t* hist2 = a.hist2 + q * kTopkBins;
+    uint2* own = reinterpret_cast<uint2*>(smem + L.own);
     // the lowest scores of buckets beta and beta + 1: the key map is
     // order-preserving (and folds -0 onto +0, as the float comparison does),
     // so a finite score is a candidate iff it compares >= tb and in bucket
@@ -259,15 +265,34 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
       while (take) {
         const int p = __ffsll(static_cast<long long>(take)) - 1;
         take &= take - 1;
-        gl[pos++] = make_uint2(score_key(stage[kRun * tid + p]), static_cast<uint32_t>(i0 + p));
+        const uint2 cv = make_uint2(score_key(stage[kRun * tid + p]), static_cast<uint32_t>(i0 + p));
+        if (pos < static_cast<uint32_t>(kCandP)) own[pos] = cv;
+        gl[pos++] = cv;
       }
       n_own += tot32;
       __syncthreads();  // the stage and tot32 are rewritten by the next batch
     }
   }
-  // this rank's candidate count into every CTA's table (read after the barrier)
+  // this rank's candidate count into every CTA's table (read after the
+  // barrier), and its candidates (when they fit) into every CTA's list
+  // area by one bulk copy each, completing on that CTA's bar_l
+  fence_proxy_async();  // the own list, written by the threads, is read by the bulk copies
+  __syncthreads();
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  if (tid < kC) *cluster.map_shared_rank(&rcnt[r], tid) = n_own;
+  if (tid < kC) {
+    *cluster.map_shared_rank(&rcnt[r], tid) = n_own;
+    if (n_own > 0 && n_own <= static_cast<uint32_t>(kCandP)) {
+      uint32_t dst, mb;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                   : "=r"(dst)
+                   : "r"(smem_u32(smem + L.plist + r * kCandP * 8)), "r"(tid));
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(mb) : "r"(smem_u32(&bar_l)), "r"(tid));
+      asm volatile(
+          "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+          "r"(smem_u32(smem + L.own)), "r"((n_own + 1) / 2 * 16), "r"(mb)
+          : "memory");
+    }
+  }
   // no slot of this CTA holds a kept block until step 2 says so (with
   // consistent inputs step 2 fills every slot below k; with a histogram that
   // does not match the scores, unfilled slots stay empty instead of undefined)
@@ -288,27 +313,31 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
       }
     }
   } else {
+    // the pushed lists: every rank whose candidates fit pushed them here
+    // before the barrier; all pushes land before they are read (also when
+    // another rank's did not fit and the lists are read from global memory)
     bool staged = true;
-    for (int i = 0; i < kC; ++i) staged = staged && rcnt[i] <= static_cast<uint32_t>(kCandR);
-    uint2* lists = reinterpret_cast<uint2*>(smem + L.stage);  // [kC][kCandR]
-    if (staged && tid == 0) {
-      uint32_t total = 0;
-      for (int i = 0; i < kC; ++i) total += (rcnt[i] + 1) / 2 * 16;
-      fence_proxy_async();  // the stage held the scores, read by the threads
-      mbar_expect_tx(&bar, total);
-      for (int i = 0; i < kC; ++i)
-        if (rcnt[i]) bulk_g2s(lists + i * kCandR, gl_all + static_cast<long long>(i) * E, (rcnt[i] + 1) / 2 * 16, &bar);
+    uint32_t pushed = 0;
+    for (int i = 0; i < kC; ++i) {
+      const bool fits = rcnt[i] <= static_cast<uint32_t>(kCandP);
+      staged = staged && fits;
+      if (fits) pushed += (rcnt[i] + 1) / 2 * 16;
     }
+    if (tid == 0) mbar_expect_tx(&bar_l, pushed);
+    const uint2* lists = reinterpret_cast<const uint2*>(smem + L.plist);  // [kC][kCandP]
     // the rule's top 24 bits while the lists arrive
     const uint32_t beta = static_cast<uint32_t>(b1.beta);
     const uint32_t k2 = static_cast<uint32_t>(k) - b1.above;
     const Bucket b2 = find_bucket<kT>(a.hist2 + q * kTopkBins, k2, tmp, &sb);
     Rule rl{(beta << 20) | (static_cast<uint32_t>(b2.beta) << 8), 0xFFFFFF00u, k2 - b2.above, 0u};
     rl.done = (b2.beta >= 0 && b2.hb == rl.k_rem) ? 1u : 0u;
-    if (staged) bulk_wait();
+    if (!mbar_wait(&bar_l, 0, a.budget, nullptr)) {
+      raise_flag(at.errw, kFlagTimeout);
+      mbar_wait(&bar_l, 0, kDrainBudget, nullptr);
+    }
     // candidate c of rank i
     auto cand_at = [&](int i, int c) -> uint2 {
-      return staged ? lists[i * kCandR + c] : gl_all[static_cast<long long>(i) * E + c];
+      return staged ? lists[i * kCandP + c] : gl_all[static_cast<long long>(i) * E + c];
     };
     if (!rl.done) {
       // the last 8 bits among the keys with this 24-bit prefix (few keys)
