@@ -58,8 +58,8 @@ constexpr long long kDrainBudget = 1LL << 31;
 
 // Shared-memory layout (bytes), the same on host and device.
 struct TailLayout {
-  int stage;      // steps 1-2: a batch of scores, then the ranks' candidate lists
-  int kv, codes;  // step 3: the K/V tile and slot codes (after the lists: filled during step 2)
+  int stage;      // step 1: a batch of scores
+  int kv, codes;  // step 3: the K/V tile and slot codes
   int merge;      // step 3: the two key halves' partials (overlap the above once consumed)
   int map, recv;  // persistent: rank -> block of this CTA's slots, partials of its heads
   int qs;         // persistent: the query's rows [H][D] bf16
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     }
     if (tid == 0) mbar_expect_tx(&bar_l, pushed);
     const uint2* lists = reinterpret_cast<const uint2*>(smem + L.plist);  // [kC][kCandP]
-    // the rule's top 24 bits while the lists arrive
+    // the rule's top 24 bits from the second-level histogram (global)
     const uint32_t beta = static_cast<uint32_t>(b1.beta);
     const uint32_t k2 = static_cast<uint32_t>(k) - b1.above;
     const Bucket b2 = find_bucket<kT>(a.hist2 + q * kTopkBins, k2, tmp, &sb);
