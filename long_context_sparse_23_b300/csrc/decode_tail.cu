@@ -24,8 +24,9 @@
 //     (selected blocks by rank, then the window; all 256 threads, 16 bytes
 //     each, consecutive threads on consecutive chunks of a row) and attends
 //     them for every head (8 warps: 4 groups of 16 heads x 2 key halves,
-//     mma.sync), merges the halves, and sends each head's (O, max, sum) to
-//     the CTA owning that head;
+//     mma.sync), merges the halves in registers (the two warps of a head
+//     group meet at a named barrier), and sends each head's (O, max, sum)
+//     to the CTA owning that head;
 //  5. each CTA folds the partials of its heads in rank order and writes the
 //     output.
 // Everything merges in a fixed order: results do not depend on scheduling.
@@ -60,7 +61,7 @@ constexpr long long kDrainBudget = 1LL << 31;
 struct TailLayout {
   int stage;      // step 1: a batch of scores
   int kv, codes;  // step 3: the K/V tile and slot codes
-  int merge;      // step 3: the two key halves' partials (overlap the above once consumed)
+  int merge;      // step 3: the second key half's partials (overlap the above once consumed)
   int map, recv;  // persistent: rank -> block of this CTA's slots, partials of its heads
   int qs;         // persistent: the query's rows [H][D] bf16
   int own;        // this rank's first kCandP candidates (the source of its pushes)
@@ -78,8 +79,8 @@ __host__ __device__ inline TailLayout tail_layout(int S_r, int H, int D, int E) 
   L.kv = (sel_end + 127) / 128 * 128;
   L.codes = L.kv + 2 * S_r * (D * 2 + 16);
   const int kv_end = L.codes + S_r * 4;
-  L.merge = 0;  // [2][H][ldo] o, then [2][H] m, [2][H] l, then [H][4] push weights
-  const int merge_end = L.merge + (2 * H * ldo + 4 * H + 4 * H) * 4;
+  L.merge = 0;  // [H][ldo] o, then [H] m, [H] l of the second key half
+  const int merge_end = L.merge + (H * ldo + 2 * H) * 4;
   const int a_end = kv_end > merge_end ? kv_end : merge_end;
   L.map = (a_end + 15) / 16 * 16;
   L.recv = L.map + (S_r * 4 + 15) / 16 * 16;
@@ -513,57 +514,76 @@ __global__ void __launch_bounds__(kT, 1) decode_tail_kernel(TailArgs a, int E, i
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     __syncthreads();  // the K/V tile is consumed; the merge area overlaps it
-    float* xo = reinterpret_cast<float*>(smem + L.merge);  // [2][H][LDO]
-    float* xm = xo + 2 * H * LDO;                          // [2][H]
-    float* xl = xm + 2 * H;                                // [2][H]
-    if (hg * 16 < H) {
+    // the two key halves of head group hg merge in registers: the half-1
+    // warp leaves its (o, m, l) in shared memory, the half-0 warp (named
+    // barrier 1 + hg between the pair) merges them with its own and sends
+    // its 16 heads' partials to their owner CTAs, one float4 per lane and
+    // column block (a lane pair assembles it by one exchange)
+    float* xo = reinterpret_cast<float*>(smem + L.merge);  // [H][LDO] half-1 partials
+    float* xm = xo + H * LDO;                              // [H]
+    float* xl = xm + H;                                    // [H]
+    if (hg * 16 < H && kh == 1) {
 #pragma unroll
       for (int i = 0; i < DT; ++i) {
         const int col = 8 * i + 2 * c;
-        if (h0 < H) *reinterpret_cast<float2*>(xo + (kh * H + h0) * LDO + col) = make_float2(o[i][0], o[i][1]);
-        if (h1 < H) *reinterpret_cast<float2*>(xo + (kh * H + h1) * LDO + col) = make_float2(o[i][2], o[i][3]);
+        if (h0 < H) *reinterpret_cast<float2*>(xo + h0 * LDO + col) = make_float2(o[i][0], o[i][1]);
+        if (h1 < H) *reinterpret_cast<float2*>(xo + h1 * LDO + col) = make_float2(o[i][2], o[i][3]);
       }
       if (c == 0) {
         if (h0 < H) {
-          xm[kh * H + h0] = m0;
-          xl[kh * H + h0] = l0;
+          xm[h0] = m0;
+          xl[h0] = l0;
         }
         if (h1 < H) {
-          xm[kh * H + h1] = m1;
-          xl[kh * H + h1] = l1;
+          xm[h1] = m1;
+          xl[h1] = l1;
         }
       }
     }
-    __syncthreads();
-    // per head: the merged max and the two halves' weights
-    float* xw = xl + 2 * H;  // [H][4]: M, weight of half 0, weight of half 1, sum
-    if (tid < H) {
-      const float ma = xm[tid], mb = xm[H + tid];
-      const float M = fmaxf(ma, mb);
-      const float R = M == -INFINITY ? 0.f : M;
-      const float fa = ex2(ma - R), fb = ex2(mb - R);
-      xw[4 * tid] = M;
-      xw[4 * tid + 1] = fa;
-      xw[4 * tid + 2] = fb;
-      xw[4 * tid + 3] = fa * xl[tid] + fb * xl[H + tid];
-    }
-    __syncthreads();
-    // merge the two key halves and send each head's partial to its owner
-    for (int it = tid; it < H * (D / 4); it += kT) {
-      const int h = it / (D / 4), col = 4 * (it % (D / 4));
-      const float fa = xw[4 * h + 1], fb = xw[4 * h + 2];
-      const float4 va = *reinterpret_cast<const float4*>(xo + h * LDO + col);
-      const float4 vb = *reinterpret_cast<const float4*>(xo + (H + h) * LDO + col);
-      float4 v;
-      v.x = fa * va.x + fb * vb.x;
-      v.y = fa * va.y + fb * vb.y;
-      v.z = fa * va.z + fb * vb.z;
-      v.w = fa * va.w + fb * vb.w;
-      const int owner = h / L.hpc, hl = h - owner * L.hpc;
-      *reinterpret_cast<float4*>(cluster.map_shared_rank(recv + (hl * kC + r) * LDO + col, owner)) = v;
-      if (col == 0) {
-        *cluster.map_shared_rank(recv_m + hl * kC + r, owner) = xw[4 * h];
-        *cluster.map_shared_rank(recv_l + hl * kC + r, owner) = xw[4 * h + 3];
+    if (hg * 16 < H) asm volatile("bar.sync %0, 64;" ::"r"(1 + hg) : "memory");
+    if (hg * 16 < H && kh == 0) {
+      // per row: the merged max, the halves' weights and the merged sum
+      float fa[2], fb[2], Mx[2], Lx[2];
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int h = hr == 0 ? h0 : h1;
+        const float ma = hr == 0 ? m0 : m1, la = hr == 0 ? l0 : l1;
+        const float mb = h < H ? xm[h] : -INFINITY, lb = h < H ? xl[h] : 0.f;
+        const float M = fmaxf(ma, mb);
+        const float R = M == -INFINITY ? 0.f : M;
+        fa[hr] = ex2(ma - R);
+        fb[hr] = ex2(mb - R);
+        Mx[hr] = M;
+        Lx[hr] = fa[hr] * la + fb[hr] * lb;
+      }
+      const bool even = (c & 1) == 0;
+      // even lanes send row h0's column block 8i + 2c .. + 3, odd lanes row h1's
+      const int hs = even ? h0 : h1;
+      const int owner = hs / L.hpc, hl = hs - owner * L.hpc;
+      float* dst = cluster.map_shared_rank(recv + (hl * kC + r) * LDO, owner);
+#pragma unroll
+      for (int i = 0; i < DT; ++i) {
+        const int col = 8 * i + 2 * c;
+        const float2 b0 = h0 < H ? *reinterpret_cast<const float2*>(xo + h0 * LDO + col) : make_float2(0.f, 0.f);
+        const float2 b1 = h1 < H ? *reinterpret_cast<const float2*>(xo + h1 * LDO + col) : make_float2(0.f, 0.f);
+        const float v0 = fa[0] * o[i][0] + fb[0] * b0.x, v1 = fa[0] * o[i][1] + fb[0] * b0.y;
+        const float v2 = fa[1] * o[i][2] + fb[1] * b1.x, v3 = fa[1] * o[i][3] + fb[1] * b1.y;
+        const float s0 = __shfl_xor_sync(0xffffffffu, even ? v2 : v0, 1);
+        const float s1 = __shfl_xor_sync(0xffffffffu, even ? v3 : v1, 1);
+        if (hs < H)
+          *reinterpret_cast<float4*>(dst + (even ? col : col - 2)) =
+              even ? make_float4(v0, v1, s0, s1) : make_float4(s0, s1, v2, v3);
+      }
+      if (c == 0) {
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int h = hr == 0 ? h0 : h1;
+          if (h < H) {
+            const int ow = h / L.hpc, hl2 = h - ow * L.hpc;
+            *cluster.map_shared_rank(recv_m + hl2 * kC + r, ow) = Mx[hr];
+            *cluster.map_shared_rank(recv_l + hl2 * kC + r, ow) = Lx[hr];
+          }
+        }
       }
     }
   }
