@@ -135,21 +135,25 @@ class DecodeStep:
         """Our kernel launches in one csa_layer decode step.  Over 16384 entries
         (long rows): histogram zeroing, the indexer (which also accumulates the
         top-k histogram when Tq == 1, else a histogram kernel follows), then
-        over 65536 entries the fused top-k + attention kernel, else the select
-        and finish passes of the top-k and the attention.  Up to 16384 entries:
-        the indexer, the one-pass top-k and the attention.  The tensor-core
-        decode attention (H = 64, d = 128) adds the merge of its key ranges when
-        a query's k + W slots span more than four 128-slot tiles."""
+        over 65536 entries the fused top-k + attention kernel; up to 32768
+        entries the one-CTA-per-query top-k and the attention; in between the
+        select and finish passes of the top-k and the attention.  Up to 16384
+        entries: the indexer, the one-pass top-k and the attention.  The
+        tensor-core decode attention (H = 64, d = 128) merges the key ranges of
+        a query inside a cluster for up to eight ranges of four 128-slot tiles
+        and adds a merge kernel beyond that."""
         wl = self.wl
         fused_hist = self.Tq == 1 and wl.H_I >= 16
         attention = 1
         if self.Tq < 16 and wl.H == 64 and wl.d == 128:
             tiles = -(-(wl.k + wl.W) // 128)
-            attention += 1 if -(-tiles // 4) > 1 else 0
+            attention += 1 if -(-tiles // 4) > 8 else 0
         if wl.N <= 16384:
             return 2 + attention
         n = 2 + (0 if fused_hist else 1)      # zeroing, indexer (+ histogram pass)
-        return n + (1 if wl.N > 65536 else 2 + attention)  # fused tail, or select + finish + attention
+        if wl.N > 65536:
+            return n + 1                      # fused tail
+        return n + (1 if wl.N <= 32768 else 2) + attention  # top-k (one or two passes) + attention
 
     # algorithmic work of the indexer launch: every visible entry's d_I-wide bf16
     # key read once per sequence (the queries of a sequence share one pass over

@@ -32,14 +32,22 @@
 //      rows, each tile into its own TMEM accumulator;
 //   4. the epilogue weights the tiles by 2^(max_j - max) / L and writes the
 //      output (one range) or the range's partial (normalised O and
-//      log2-sum-exp) for the combine kernel, which merges a query's ranges in
-//      range order.
+//      log2-sum-exp).  Up to eight ranges of a query form a thread-block
+//      cluster: each CTA keeps its partial in shared memory and, after a
+//      cluster barrier, merges a share of the query's (head, column) outputs
+//      from every range's partial over distributed shared memory, in range
+//      order.  More ranges write their partials to the workspace for the
+//      combine kernel, which merges them the same way.
 // Every wait is bounded (and sleeps in hardware rather than polling); a
 // timeout raises the workspace error flag, an index or window row outside its
 // buffer raises the index flag and is skipped.
+#include <cooperative_groups.h>
+
 #include "attend_tile.cuh"
 #include "common.cuh"
 #include "kernels.h"
+
+namespace cg = cooperative_groups;
 
 namespace csa {
 
@@ -52,11 +60,13 @@ constexpr int kHalfB = kHT * 128;  // one 64-column half of a tile: 128 rows x 1
 constexpr int kThreads = 384;      // MMA warp, three producer warps, eight epilogue warps
 constexpr int kProducers = 96;
 constexpr long long kDrainBudget = 1LL << 31;
+constexpr int kTcClusterMax = 8;   // ranges of a query merged inside one cluster (portable size)
 
 struct TcParams {
   float sl2;  // scale * log2(e)
   int nsplit;
   int tpr;    // tiles per range
+  int cluster;  // 1: the nsplit ranges of a query form a cluster and merge through DSMEM
   long long budget;
 };
 
@@ -226,12 +236,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   int ntile = qt.n_tiles - j0;
   ntile = ntile < 0 ? 0 : (ntile > p.tpr ? p.tpr : ntile);
 
+  // the range's partial in shared memory when the ranges merge in the cluster:
+  // [H][kD] normalised O, then [H] log2-sum-exp (the K/V buffers, free once
+  // every MMA is done)
+  float* part_s = reinterpret_cast<float*>(kv);
   if (ntile == 0) {
     // nothing of this query in this range: an empty partial, or (one range)
     // the output of an empty key set, 0 and lse = -inf
     for (int i = tid; i < H * kD; i += kThreads) {
       const int h = i / kD, c = i % kD;
-      if (p.nsplit > 1) {
+      if (p.cluster) {
+        part_s[i] = 0.f;
+        if (c == 0) part_s[H * kD + h] = -INFINITY;
+      } else if (p.nsplit > 1) {
         float* pb = a.part + ((qi * p.nsplit + split) * H + h) * static_cast<long long>(kD + 1);
         pb[c] = 0.f;
         if (c == 0) pb[kD] = -INFINITY;
@@ -532,7 +549,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           o[4 * c4 + 3] = fmaf(w4.w, __uint_as_float(r[c4 >> 2][(4 * c4 + 3) & 15]), o[4 * c4 + 3]);
         }
       }
-      if (p.nsplit > 1) {
+      if (p.cluster) {
+        float* ps_o = part_s + (grp * HPG) * kD + i;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) ps_o[e * kD] = o[e];
+        if (quarter == 0) part_s[H * kD + grp * HPG + lane] = lse_s[grp * HPG + lane];
+      } else if (p.nsplit > 1) {
         float* pb = a.part + ((qi * p.nsplit + split) * H + grp * HPG) * static_cast<long long>(kD + 1) + i;
 #pragma unroll
         for (int e = 0; e < 32; ++e) pb[e * (kD + 1)] = o[e];
@@ -562,6 +584,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
+  }
+  if (p.cluster) {
+    // merge of the query's ranges: this CTA (cluster rank = range) takes a
+    // contiguous share of the H x kD outputs in groups of four columns and
+    // folds every range's partial in range order, as the combine kernel does
+    cg::cluster_group cl = cg::this_cluster();
+    cl.sync();  // every range's partial is in its CTA's shared memory
+    const int ns = p.nsplit;
+    const float* rp[kTcClusterMax];
+#pragma unroll
+    for (int r = 0; r < kTcClusterMax; ++r) rp[r] = r < ns ? cl.map_shared_rank(part_s, r) : part_s;
+    constexpr int kGroups = H * kD / 4;
+    const int g_lo = split * kGroups / ns, g_hi = (split + 1) * kGroups / ns;
+    for (int g = g_lo + tid; g < g_hi; g += kThreads) {
+      const int h = g / (kD / 4), c4 = (g % (kD / 4)) * 4;
+      float ls[kTcClusterMax];
+      float4 vs[kTcClusterMax];
+#pragma unroll
+      for (int r = 0; r < kTcClusterMax; ++r) {
+        if (r < ns) {
+          ls[r] = rp[r][H * kD + h];
+          vs[r] = *reinterpret_cast<const float4*>(rp[r] + h * kD + c4);
+        }
+      }
+      float M = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kTcClusterMax; ++r)
+        if (r < ns) M = fmaxf(M, ls[r]);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float den = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int r = 0; r < kTcClusterMax; ++r) {
+          if (r < ns) {
+            const float f = ex2(ls[r] - M);
+            den += f;
+            acc.x = fmaf(f, vs[r].x, acc.x);
+            acc.y = fmaf(f, vs[r].y, acc.y);
+            acc.z = fmaf(f, vs[r].z, acc.z);
+            acc.w = fmaf(f, vs[r].w, acc.w);
+          }
+        }
+      }
+      const float val[4] = {den > 0.f ? acc.x / den : 0.f, den > 0.f ? acc.y / den : 0.f,
+                            den > 0.f ? acc.z / den : 0.f, den > 0.f ? acc.w / den : 0.f};
+      const long long o = (qi * H + h) * static_cast<long long>(kD) + c4;
+      if (a.out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + o) = make_float4(val[0], val[1], val[2], val[3]);
+      } else {
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + o) =
+            make_uint2(pack_bf16x2(val[0], val[1]), pack_bf16x2(val[2], val[3]));
+      }
+      if (a.lse && c4 == 0) a.lse[qi * H + h] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
+    }
+    cl.sync();  // no CTA leaves while another still reads its shared memory
   }
 }
 
@@ -637,6 +714,7 @@ cudaError_t launch_attend_tc(const AttendArgs& a, long long budget, cudaStream_t
   p.sl2 = a.scale * 1.4426950408889634f;
   p.nsplit = pl.nsplit;
   p.tpr = pl.tpr;
+  p.cluster = pl.nsplit > 1 && pl.nsplit <= kTcClusterMax ? 1 : 0;
   p.budget = budget;
   const size_t smem = 1024 + 2 * kH * 128 + kTcTiles * (2 * kHalfB + kHT * 128) + sizeof(TcBars);
   const dim3 grid(static_cast<unsigned>(p.nsplit), static_cast<unsigned>(nq));
@@ -644,13 +722,15 @@ cudaError_t launch_attend_tc(const AttendArgs& a, long long budget, cudaStream_t
   if (csa) {
     e = ensure_dyn_smem<attend_tc_kernel<true>>(static_cast<int>(smem));
     if (e == cudaSuccess)
-      e = launch_k(attend_tc_kernel<true>, grid, dim3(kThreads), smem, s, 1, tmq, tkc, tvc, tkr, tvr, a, p);
+      e = launch_k(attend_tc_kernel<true>, grid, dim3(kThreads), smem, s, p.cluster ? p.nsplit : 1, tmq, tkc, tvc,
+                   tkr, tvr, a, p);
   } else {
     e = ensure_dyn_smem<attend_tc_kernel<false>>(static_cast<int>(smem));
     if (e == cudaSuccess)
-      e = launch_k(attend_tc_kernel<false>, grid, dim3(kThreads), smem, s, 1, tmq, tkc, tvc, tkr, tvr, a, p);
+      e = launch_k(attend_tc_kernel<false>, grid, dim3(kThreads), smem, s, p.cluster ? p.nsplit : 1, tmq, tkc, tvc,
+                   tkr, tvr, a, p);
   }
-  if (e != cudaSuccess || p.nsplit == 1) return e;
+  if (e != cudaSuccess || p.nsplit == 1 || p.cluster) return e;
   return launch_attend_combine(a, p.nsplit, s);
 }
 

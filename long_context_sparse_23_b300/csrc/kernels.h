@@ -78,6 +78,7 @@ bool indexer_fills_hist(int Tq, int H_I);
 constexpr int kTopkBins = 4096;        // buckets of 12 key bits (two levels: bits 31..20, 19..8)
 constexpr int kTopkChunk = 4096;       // keys per candidate-select CTA (long rows)
 constexpr int kTopkShortMax = 16384;   // rows up to this length are selected in shared memory
+constexpr int kTopkMidMax = 32768;     // longer rows up to this length: one CTA per query from the histogram
 constexpr int kTopkMaxN = 1 << 24;
 
 struct TopkArgs {

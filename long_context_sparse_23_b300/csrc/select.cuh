@@ -214,12 +214,22 @@ __device__ Rule digit_select(Keys keys, int n, Rule r, int first_shift, uint32_t
   return r;
 }
 
-// Write the kept indices of a row in index order: each warp owns a
-// contiguous segment, counts its kept keys, and after a scan over warps
-// writes them with ballots.  All T threads call it.
-template <int T, typename Keys>
+// Position i of a row is block index i, or (a candidate list) the block index
+// stored for it.
+struct RowIndex {
+  __device__ int operator()(int i) const { return i; }
+};
+struct ListIndex {
+  const uint32_t* idx;
+  __device__ int operator()(int i) const { return static_cast<int>(idx[i]); }
+};
+
+// Write the kept indices of a row (or of a candidate list in index order) in
+// index order: each warp owns a contiguous segment, counts its kept keys, and
+// after a scan over warps writes them with ballots.  All T threads call it.
+template <int T, typename Keys, typename Index = RowIndex>
 __device__ void compact_row(Keys keys, int n, const Rule r, int32_t* out, float* sout, uint32_t* wgt,
-                            uint32_t* weq) {
+                            uint32_t* weq, Index index = Index{}) {
   constexpr int NW = T / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int seg = ((n + NW - 1) / NW + 31) & ~31;
@@ -254,7 +264,7 @@ __device__ void compact_row(Keys keys, int n, const Rule r, int32_t* out, float*
     const uint32_t eq_before = run_eq + __popc(beq & lt);
     if (gt || (eq && eq_before < r.k_rem)) {
       const uint32_t pos = gt_before + min(eq_before, r.k_rem);
-      out[pos] = i;
+      out[pos] = index(i);
       if (sout) sout[pos] = key_score(full);
     }
     run_gt += __popc(bgt);

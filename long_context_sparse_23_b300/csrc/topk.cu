@@ -14,6 +14,9 @@
 // memory and fixes the rule with up to four 8-bit digit passes; a warp-ballot
 // compaction in index order writes the output.
 //
+// Mid rows (N <= 32768, e.g. decode at 128K context): the histogram below,
+// then one CTA per query selects from it (topk_mid_kernel).
+//
 // Long rows (decode: few queries, up to ~10^6 keys each), three grid-wide
 // steps instead of one CTA per query:
 //  1. a 4096-bin histogram of every query's keys' top 12 bits, accumulated in
@@ -80,6 +83,190 @@ __global__ void __launch_bounds__(kShortThreads) topk_short_kernel(TopkArgs a) {
   const Rule r = digit_select<kShortThreads>(SmemKeys{keys}, n_vis, Rule{0u, 0u, static_cast<uint32_t>(a.k), 0u},
                                              24, hist, tmp, &rule);
   compact_row<kShortThreads>(SmemKeys{keys}, n_vis, r, out, sout, wgt, weq);
+}
+
+// ---------------------------------------------------------------- mid rows
+// Rows of kTopkShortMax < N <= kTopkMidMax entries with the bucket histogram
+// ready (decode at 128K context: 32768 blocks): one CTA per query instead of
+// the select and finish passes, with every step spread evenly over the
+// threads:
+//  1. the row is copied to shared memory (cp.async) while the bucket beta of
+//     the k-th largest key is found from the histogram;
+//  2. candidates (bucket >= beta) by one float comparison per score against
+//     the lowest score of bucket beta (the key map is order-preserving),
+//     their indices appended to a list (warp-aggregated, any order);
+//  3. per candidate: bucket above beta -> kept (bit in a bitmap over the
+//     row), bucket beta -> a second-level histogram of key bits 19..8;
+//  4. the sub-bucket holding the rest of the k-th largest, then at most one
+//     8-bit pass, fix the exact rule; the candidates of bucket beta set their
+//     kept or tied bit;
+//  5. thread t owns bitmap word t (blocks 32t .. 32t + 31): two block scans
+//     keep the k_rem lowest-index ties and give each word's output position,
+//     and the kept indices are written in ascending order.
+// The candidate counts are checked against the histogram: a histogram that
+// does not match the scores (an indexer that gave up, non-finite scores) or
+// more candidates than the list holds (a row of near-equal scores) sends the
+// CTA to digit passes over the whole row in global memory instead, so the
+// output is the exact selection of the given scores in every case.
+constexpr int kMidThreads = 1024;
+constexpr int kMidWords = kTopkMidMax / 32;  // bitmap words, one per thread
+constexpr int kMidList = 8192;               // candidate indices staged
+static_assert(kMidWords == kMidThreads && kTopkMidMax % (4 * kMidThreads) == 0, "mid rows: layout");
+
+// dynamic shared memory of topk_mid_kernel, in 32-bit words
+constexpr int kMidSmemWords = kTopkMidMax + 2 * kMidWords + kTopkBins + kMidList;
+
+__global__ void __launch_bounds__(kMidThreads) topk_mid_kernel(TopkArgs a) {
+  pdl_wait_then_release();
+  extern __shared__ __align__(16) uint32_t msm[];
+  float* sf = reinterpret_cast<float*>(msm);  // [kTopkMidMax] the row's scores
+  uint32_t* bm = msm + kTopkMidMax;           // [kMidWords] kept for sure
+  uint32_t* eqm = bm + kMidWords;             // [kMidWords] equal to the rule's prefix
+  uint32_t* h2 = eqm + kMidWords;             // [kTopkBins] bucket beta: key bits 19..8
+  uint32_t* list = h2 + kTopkBins;            // [kMidList] candidate indices
+  __shared__ uint32_t h3[256], tmp[32], wgt[32], weq[32];
+  __shared__ Rule rule;
+  __shared__ Bucket sb, sb2;
+  __shared__ uint32_t n_list, n_gt;
+  const long long q = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int n_vis = visible(a, q);
+  int32_t* out = a.idx_out + q * a.k;
+  float* sout = a.score_out ? a.score_out + q * a.k : nullptr;
+  const float* row = a.scores + q * a.ld;
+  if (n_vis <= a.k) {
+    keep_all(a, row, n_vis, out, sout);
+    return;
+  }
+  const uint32_t k = static_cast<uint32_t>(a.k);
+  constexpr int R = kTopkMidMax / (4 * kMidThreads);  // float4 rounds per thread
+  // (1) the row: whole vectors by cp.async (past the row: zero-filled, never read as scores)
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int i = 4 * (tid + kMidThreads * r);
+    cp_async16(sf + i, row + (i + 3 < n_vis ? i : 0), i + 3 < n_vis);
+  }
+  cp_async_commit();
+  for (int i = tid; i < 2 * kMidWords + kTopkBins; i += kMidThreads) bm[i] = 0u;  // bm, eqm, h2
+  if (tid == 0) {
+    n_list = 0u;
+    n_gt = 0u;
+  }
+  const Bucket bk = find_bucket<kMidThreads>(a.hist + q * kTopkBins, k, tmp, &sb);
+  cp_async_wait<0>();
+  if ((n_vis & 3) && ((n_vis >> 2) % kMidThreads) == tid) {
+    const int i = n_vis & ~3;  // the partial last vector
+    for (int e = 0; i + e < n_vis; ++e) sf[i + e] = row[i + e];
+  }
+  __syncthreads();
+  const uint32_t beta = static_cast<uint32_t>(bk.beta);
+  // lowest score of bucket beta (NaN -- nothing compares true -- when there
+  // is no bucket or it holds no finite score)
+  const float lo_b = bk.beta >= 0 ? key_score(beta << 20) : __uint_as_float(0x7fc00000u);
+  // (2) candidates, each thread's in its own bit mask
+  uint32_t mc = 0;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int i = 4 * (tid + kMidThreads * r);
+    const float4 v = *reinterpret_cast<const float4*>(sf + i);
+    mc |= (i < n_vis && v.x >= lo_b ? 1u : 0u) << (4 * r);
+    mc |= (i + 1 < n_vis && v.y >= lo_b ? 1u : 0u) << (4 * r + 1);
+    mc |= (i + 2 < n_vis && v.z >= lo_b ? 1u : 0u) << (4 * r + 2);
+    mc |= (i + 3 < n_vis && v.w >= lo_b ? 1u : 0u) << (4 * r + 3);
+  }
+  {
+    const uint32_t c = static_cast<uint32_t>(__popc(mc));
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    uint32_t base = 0;
+    if (lane == 31) base = atomicAdd(&n_list, incl);
+    uint32_t pos = __shfl_sync(0xffffffffu, base, 31) + incl - c;
+    while (mc) {
+      const int j = __ffs(mc) - 1;
+      mc &= mc - 1;
+      if (pos < static_cast<uint32_t>(kMidList)) list[pos] = static_cast<uint32_t>(4 * (tid + kMidThreads * (j >> 2)) + (j & 3));
+      ++pos;
+    }
+  }
+  __syncthreads();
+  const uint32_t C = n_list;
+  bool whole_row = bk.beta < 0 || C > static_cast<uint32_t>(kMidList);
+  if (!whole_row) {
+    // (3) keys above bucket beta are kept; bucket beta's keys feed the second level
+    uint32_t g = 0;
+    for (uint32_t e = tid; e < C; e += kMidThreads) {
+      const uint32_t i = list[e];
+      const uint32_t key = score_key(sf[i]);
+      if ((key >> 20) > beta) {
+        atomicOr(&bm[i >> 5], 1u << (i & 31));
+        ++g;
+      } else {
+        atomicAdd(&h2[(key >> 8) & (kTopkBins - 1)], 1u);
+      }
+    }
+    g = __reduce_add_sync(0xffffffffu, g);
+    if (lane == 0 && g) atomicAdd(&n_gt, g);
+  }
+  __syncthreads();
+  // the candidates must be exactly the histogram's keys in buckets >= beta
+  if (!whole_row) whole_row = n_gt != bk.above || C != bk.above + bk.hb;
+  if (whole_row) {
+    const Rule r = digit_select<kMidThreads>(GlobalKeys{row}, n_vis, Rule{0u, 0u, k, 0u}, 24, h3, tmp, &rule);
+    compact_row<kMidThreads>(GlobalKeys{row}, n_vis, r, out, sout, wgt, weq);
+    return;
+  }
+  // (4) the rule: sub-bucket of bits 19..8 from the second level, then at most one 8-bit pass
+  const Bucket b2 = find_bucket<kMidThreads>(h2, k - bk.above, tmp, &sb2);
+  Rule r{(beta << 20) | (static_cast<uint32_t>(b2.beta) << 8), 0xffffff00u, k - bk.above - b2.above,
+         b2.hb == k - bk.above - b2.above ? 1u : 0u};
+  if (!r.done) {
+    if (tid < 256) h3[tid] = 0u;
+    __syncthreads();
+    for (uint32_t e = tid; e < C; e += kMidThreads) {
+      const uint32_t key = score_key(sf[list[e]]);
+      if ((key & r.mask) == r.prefix) atomicAdd(&h3[key & 255u], 1u);
+    }
+    __syncthreads();
+    pick_digit<kMidThreads>(h3, r, 0, tmp, &rule);
+    r = rule;
+  }
+  for (uint32_t e = tid; e < C; e += kMidThreads) {
+    const uint32_t i = list[e];
+    const uint32_t key = score_key(sf[i]);
+    if ((key >> 20) == beta) {
+      const uint32_t mk = key & r.mask;
+      if (mk > r.prefix) atomicOr(&bm[i >> 5], 1u << (i & 31));
+      else if (mk == r.prefix) atomicOr(&eqm[i >> 5], 1u << (i & 31));
+    }
+  }
+  __syncthreads();
+  // (5) word tid: the k_rem lowest-index ties overall, then the output position
+  uint32_t wq = eqm[tid];
+  const uint32_t ne = static_cast<uint32_t>(__popc(wq));
+  const uint32_t eq_before = block_incl_scan<kMidThreads>(ne, tmp) - ne;
+  uint32_t take = r.k_rem > eq_before ? min(ne, r.k_rem - eq_before) : 0u;
+  uint32_t wk = bm[tid];
+  for (; take > 0; --take) {
+    const uint32_t low = wq & (0u - wq);
+    wk |= low;
+    wq ^= low;
+  }
+  const uint32_t nk = static_cast<uint32_t>(__popc(wk));
+  uint32_t pos = block_incl_scan<kMidThreads>(nk, tmp) - nk;
+  while (wk) {
+    const int bit = __ffs(wk) - 1;
+    wk &= wk - 1;
+    const int i = 32 * tid + bit;
+    if (pos < k) {
+      out[pos] = i;
+      if (sout) sout[pos] = key_score(score_key(sf[i]));
+    }
+    ++pos;
+  }
 }
 
 // ---------------------------------------------------------------- long rows
@@ -504,6 +691,13 @@ cudaError_t launch_topk(const TopkArgs& a, bool hist_ready, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     e = launch_k(topk_hist_kernel, grid, dim3(kSelThreads), 0, s, 1, a);
     if (e != cudaSuccess) return e;
+  }
+  if (a.N <= kTopkMidMax) {
+    // one CTA per query: the row's keys and bucket beta's keys in shared memory
+    const size_t smem = static_cast<size_t>(kMidSmemWords) * 4;
+    e = ensure_dyn_smem<topk_mid_kernel>(static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return launch_k(topk_mid_kernel, dim3(static_cast<unsigned>(nq)), dim3(kMidThreads), smem, s, 1, a);
   }
   e = launch_k(topk_select_kernel, grid, dim3(kSelThreads), 0, s, 1, a);
   if (e != cudaSuccess) return e;

@@ -2,14 +2,14 @@
 queries per sequence) against the oracle, |err| <= 1e-2 + 1e-2 |ref| and lse to
 1e-4.
 
-Dense HCA (TMA key tiles): one key range (output written directly), many
-ranges with partials merged by the combine kernel (some ranges empty for the
-shorter query), entries that are not a whole number of 128-key tiles, the
+Dense HCA (TMA key tiles): one key range (output written directly), up to
+eight ranges merged inside their thread-block cluster and more ranges merged
+by the combine kernel (some ranges empty for the shorter query), entries that are not a whole number of 128-key tiles, the
 window clipped at token 0, the window alone, no window, an empty key set, and
 window rows outside the raw buffer.
 
 CSA (gathered rows): ragged index lists with holes, lists spanning several
-ranges, the window alone (k = 0), an empty key set, and indices outside the
+ranges (cluster merge, and the combine kernel beyond eight), the window alone (k = 0), an empty key set, and indices outside the
 entries (flagged and skipped)."""
 import math
 
@@ -38,6 +38,15 @@ def test_hca_tc_many_ranges_with_empty_ones():
     kernel; the second query sees half of them (its later ranges are empty)."""
     pos = np.array([[139999, 70000]])
     _attn_case(33, 1, 2, 140000, 64, 128, 0, 128, 1, pos, 140000, 0, hca=True)
+
+
+def test_hca_tc_cluster_merged_ranges_with_empty_ones():
+    """2000 entries at m = 1 with W = 128: 16 + 1 tiles, 5 ranges merged inside
+    their cluster; the second query sees 301 entries (its later ranges are
+    empty), the third only its window; bf16 and fp32 outputs."""
+    pos = np.array([[1999, 300, 0]])
+    _attn_case(37, 1, 3, 2000, 64, 128, 0, 128, 1, pos, 4000, 0, hca=True)
+    _attn_case(38, 1, 3, 2000, 64, 128, 0, 128, 1, pos, 4000, 0, hca=True, out_dtype=torch.float32)
 
 
 def test_hca_tc_no_window_and_empty_key_set():
@@ -88,10 +97,12 @@ def test_csa_tc_ragged_lists_with_holes_one_range():
 
 
 def test_csa_tc_many_ranges():
-    """k = 2000, W = 128: 17 tiles -> 5 ranges of at most 4 tiles, merged by the
-    combine kernel, for 3 queries of one sequence."""
+    """k = 2000, W = 128: 17 tiles -> 5 ranges of at most 4 tiles, merged inside
+    their cluster, for 3 queries of one sequence; k = 4500: 37 tiles -> 10
+    ranges, merged by the combine kernel."""
     pos = np.array([[131071, 100000, 9000]])
     _attn_case(43, 1, 3, 32768, 64, 128, 2000, 128, 4, pos, 140000, 0, holes=True)
+    _attn_case(47, 1, 3, 32768, 64, 128, 4500, 128, 4, pos, 140000, 0, holes=True, out_dtype=torch.float32)
 
 
 def test_csa_tc_window_only_and_empty():

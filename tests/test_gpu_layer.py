@@ -143,12 +143,15 @@ def test_layer_decode_fused_tail_matches_separate_calls():
     assert_attention_close(out_l.cpu().numpy(), out_s.double().cpu().numpy(), "fused vs separate")
 
 
-def test_layer_decode_tail_ties_and_short_visibility():
-    """The fused decode tail on degenerate inputs: every score equal (the
-    lowest indices win; the tie bucket is too large to stage), scores tied in
-    groups of eight (ties at the threshold), and a query that sees fewer
-    blocks than k (everything visible kept, -1 padding)."""
-    B, N, m, H, d, H_I, d_I, k, W = 3, 70000, 4, 64, 128, 64, 128, 1024, 128
+@pytest.mark.parametrize("N", [70000, 30000], ids=["fused_tail", "mid_rows"])
+def test_layer_decode_tail_ties_and_short_visibility(N):
+    """The decode top-k on degenerate inputs, in the fused decode tail (rows
+    over 65536 entries) and in the one-CTA-per-query selection (rows up to
+    32768): every score equal (the lowest indices win; the tie bucket is too
+    large to stage), scores tied in groups of eight (ties at the threshold),
+    and a query that sees fewer blocks than k (everything visible kept, -1
+    padding)."""
+    B, m, H, d, H_I, d_I, k, W = 3, 4, 64, 128, 64, 128, 1024, 128
     wl = S.WORKLOADS["decode_128k"].replace(B=B, T=N * m, positions=(N * m - 1,), raw_len=256)
     g = S.make_inputs(wl, "cuda")
     g["q_idx"][0].zero_()                                      # sequence 0: all scores 0

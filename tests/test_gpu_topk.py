@@ -98,3 +98,31 @@ def test_topk_bucket_overflow_falls_back():
     N, m, k = 100000, 4, 1024
     s = (1000.0 + rng.integers(0, 512, (2, 1, N)) / 4096.0).astype(np.float32)
     _check(s, np.array([[4 * N - 1], [4 * N - 1]]), N, m, k)
+
+
+@pytest.mark.parametrize("N", [16385, 24001, 32768])
+def test_topk_mid_rows(N):
+    """Rows of 16385..32768 entries: one CTA per query finishes the selection
+    from the bucket histogram.  Visible lengths of the whole row, odd lengths
+    (scalar loads at the end of the row), just above k and equal to k."""
+    rng = np.random.default_rng(100 + N)
+    m = 4
+    q_pos = np.array([[4 * N - 1], [4 * N - 2], [4 * N - 7], [4 * 1025 - 1], [4 * 1024 - 1], [2 * N + 5]])
+    for k in (1, 1024, 4096):
+        _check(_normal_scores(rng, 6, 1, N), q_pos, N, m, k)
+
+
+def test_topk_mid_rows_ties_and_full_buckets():
+    """Mid rows with ties inside the k-th score's bucket (kept by lowest
+    index), every score equal and a narrow score range (the bucket holds more
+    keys than the CTA stages: digit passes over the whole row), and -0 / +0."""
+    rng = np.random.default_rng(7)
+    N, m, k = 30000, 4, 1024
+    s = np.empty((5, 1, N), np.float32)
+    s[0, 0] = rng.integers(0, 4, N)                                  # four values, ~7500 each
+    s[1, 0] = 5.0                                                    # every score equal
+    s[2, 0, ::2] = -0.0
+    s[2, 0, 1::2] = 0.0
+    s[3, 0] = 1000.0 + rng.integers(0, 512, N) / 4096.0              # one bucket holds the row
+    s[4, 0] = np.round((rng.standard_normal(N) * 30 + 150) * 4) / 4  # quarter grid
+    _check(s, np.full((5, 1), 4 * N - 1), N, m, k)
