@@ -140,14 +140,14 @@ class DecodeStep:
         select and finish passes of the top-k and the attention.  Up to 16384
         entries: the indexer, the one-pass top-k and the attention.  The
         tensor-core decode attention (H = 64, d = 128) merges the key ranges of
-        a query inside a cluster for up to eight ranges of four 128-slot tiles
+        a query inside a cluster for up to eight ranges of five 128-slot tiles
         and adds a merge kernel beyond that."""
         wl = self.wl
         fused_hist = self.Tq == 1 and wl.H_I >= 16
         attention = 1
         if self.Tq < 16 and wl.H == 64 and wl.d == 128:
             tiles = -(-(wl.k + wl.W) // 128)
-            attention += 1 if -(-tiles // 4) > 8 else 0
+            attention += 1 if -(-tiles // 5) > 8 else 0
         if wl.N <= 16384:
             return 2 + attention
         n = 2 + (0 if fused_hist else 1)      # zeroing, indexer (+ histogram pass)

@@ -11,8 +11,9 @@
 //   window = {k_raw[u - raw_base] : t-W < u <= t, u >= 0},
 //   out[h] = sum_{x in J} softmax_x(scale * q[h] . K_x) V_x    (one softmax over J)
 //
-// Design.  A CTA owns one query and a range of up to kTcTiles tiles of 128
-// key slots, all 64 heads at once (the K/V rows are read once per range):
+// Design.  A CTA owns one query and a range of up to kTcTiles (CSA; HCA:
+// kTcTilesHca) tiles of 128 key slots, all 64 heads at once (the K/V rows are
+// read once per range):
 //   * keys: HCA tiles are contiguous rows, one TMA box per 64-column half
 //     (128-byte swizzle); CSA tiles are gathered row by row with 16-byte
 //     cp.async into the same swizzled layout by three producer warps, which
@@ -26,10 +27,13 @@
 //      heads) take each tile's exact per-head max (warp butterfly
 //      reduce-scatter, then the four quarters in shared memory) as soon as the
 //      tile's scores are ready, write P^T = 2^(s - max) as bf16 rows
-//      [key][head] (128-byte swizzle) and sum them per head in fp32;
+//      [key][head] (128-byte swizzle; two P buffers in turn, a buffer
+//      rewritten once the MMAs that read it are done) and sum them per head
+//      in fp32;
 //   3. O_j^T = V^T P^T on tcgen05 per tile (M = d = 128 lanes, N = 64 heads,
 //      K = keys), both operands MN-major straight from the V tile and the P
-//      rows, each tile into its own TMEM accumulator;
+//      rows, each tile into its own TMEM accumulator: the columns of the
+//      tile's scores, free once its P rows are written;
 //   4. the epilogue weights the tiles by 2^(max_j - max) / L and writes the
 //      output (one range) or the range's partial (normalised O and
 //      log2-sum-exp).  Up to eight ranges of a query form a thread-block
@@ -60,6 +64,7 @@ constexpr int kHalfB = kHT * 128;  // one 64-column half of a tile: 128 rows x 1
 constexpr int kThreads = 384;      // MMA warp, three producer warps, eight epilogue warps
 constexpr int kProducers = 96;
 constexpr long long kDrainBudget = 1LL << 31;
+constexpr int kPSlots = 2;         // P^T buffers, used by tiles in turn
 constexpr int kTcClusterMax = 8;   // ranges of a query merged inside one cluster (portable size)
 
 struct TcParams {
@@ -76,6 +81,7 @@ struct __align__(8) TcBars {
   uint64_t sdone[kTcTiles];
   uint64_t vfull[kTcTiles];
   uint64_t pfull[kTcTiles];
+  uint64_t pempty[2];  // P buffer read by the MMAs of its last tile
   uint64_t ofull;
 };
 
@@ -175,15 +181,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kQBytes = 2 * H * 128;     // two 64-column halves of the query rows
   constexpr int kTileB = 2 * kHalfB;       // K (then V) tile
   constexpr int kPB = kHT * 128;           // P^T rows of one tile
-  constexpr uint32_t kTmemCols = 512;      // per tile: H score columns and H output columns
-  constexpr uint32_t kOCol = kTcTiles * H;
-  static_assert(2 * kTcTiles * H <= static_cast<int>(kTmemCols), "TMEM columns");
+  constexpr uint32_t kTmemCols = 512;      // per tile: H score columns, then the tile's H output columns
+  static_assert(kTcTiles * H <= static_cast<int>(kTmemCols), "TMEM columns");
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   char* qs = smem;                             // [2][H][128 B]
   char* kv = qs + kQBytes;                     // [kTcTiles][2][128][128 B]
-  char* ps = kv + kTcTiles * kTileB;           // [kTcTiles][128][128 B]
-  TcBars* bars = reinterpret_cast<TcBars*>(ps + kTcTiles * kPB);
+  char* ps = kv + kTcTiles * kTileB;           // [kPSlots][128][128 B]
+  TcBars* bars = reinterpret_cast<TcBars*>(ps + kPSlots * kPB);
+  // P^T rows of tile jj: a buffer per tile for ranges of up to four tiles
+  // (ps, then the unused fifth K/V buffer); two buffers in turn for five
+  const bool pring = p.tpr > kTcTilesHca;
+  auto pbuf = [&](int jj) -> char* {
+    if (pring) return ps + (jj % kPSlots) * kPB;
+    return jj < kPSlots ? ps + jj * kPB : kv + (kTcTiles - 1) * kTileB + (jj - kPSlots) * kPB;
+  };
+  static_assert(kTcTilesHca - kPSlots <= kTileB / kPB, "P buffers of four tiles");
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   // per tile: the four lane quarters' per-head max of the raw scores and sum
@@ -209,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->vfull[j], 1);
       mbar_init(&bars->pfull[j], 8);
     }
+    for (int j = 0; j < kPSlots; ++j) mbar_init(&bars->pempty[j], 1);
     mbar_init(&bars->ofull, 1);
     mbar_fence_init();
     tma_prefetch_desc(&tmq);
@@ -290,14 +304,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t a0 = smem_u32(kv + jj * kTileB), b0 = smem_u32(ps + jj * kPB);
+        const uint32_t a0 = smem_u32(kv + jj * kTileB), b0 = smem_u32(pbuf(jj));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           // 16 keys = two 8-row groups of the V tile (A = V^T, d on M) and of
           // the P^T rows (B = P^T, heads on N); tile jj accumulates alone
-          umma_f16(tbase + kOCol + static_cast<uint32_t>(jj * H), sdesc_mnmajor_sw128(a0 + kk * 2048, kHalfB, 1024),
+          umma_f16(tbase + static_cast<uint32_t>(jj * H), sdesc_mnmajor_sw128(a0 + kk * 2048, kHalfB, 1024),
                    sdesc_mnmajor_sw128(b0 + kk * 2048, 1024, 1024), idesc_o, kk > 0 ? 1u : 0u);
         }
+        umma_commit(&bars->pempty[jj % kPSlots]);  // the P buffer is free once these MMAs are done
       }
       if (!ok) {
         if (!*abort_v) raise_flag(a.errw, kFlagTimeout);
@@ -482,18 +497,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           v[e] = p0;
           v[e + 1] = p1;
         }
-        char* row = ps + jj * kPB + i * 128;
+        // the P buffer's previous tile has been read by its MMAs
+        if (pring && jj >= kPSlots)
+          ok = __all_sync(0xffffffffu, mbar_wait_sleep(&bars->pempty[jj % kPSlots],
+                                                       static_cast<uint32_t>(jj / kPSlots - 1) & 1u, p.budget,
+                                                       abort_v));
+        char* row = pbuf(jj) + i * 128;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           const int ch = grp * 4 + cc;
-          *reinterpret_cast<uint4*>(row + ((ch ^ (i & 7)) << 4)) =
-              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+          if (ok)
+            *reinterpret_cast<uint4*>(row + ((ch ^ (i & 7)) << 4)) =
+                make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
         }
         fence_proxy_async();  // the rows are read by the tensor cores
       } else {
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = 0.f;
       }
+      // the tile's score columns are read: the MMAs may write its output there
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->pfull[jj]);
       l_part[jj][quarter][grp * HPG + lane] = warp_reduce_scatter32<false>(v, lane);
@@ -537,8 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       for (int jj = 0; jj < ntile; ++jj) {
         uint32_t r[2][16];
-        tmem_ld16(lane_addr + kOCol + jj * H + grp * HPG, r[0]);
-        tmem_ld16(lane_addr + kOCol + jj * H + grp * HPG + 16, r[1]);
+        tmem_ld16(lane_addr + jj * H + grp * HPG, r[0]);
+        tmem_ld16(lane_addr + jj * H + grp * HPG + 16, r[1]);
         tmem_ld_wait();
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
@@ -651,11 +674,15 @@ int attend_tc_tiles(bool csa, int N, int k, int W) {
   return t > 0x7fffffffLL ? 0x7fffffff : static_cast<int>(t);
 }
 
-TcPlan attend_tc_plan(int n_tiles) {
+TcPlan attend_tc_plan(int n_tiles, bool csa) {
   // the split depends on the key count only (never on the batch), so a
-  // sequence gives identical results alone or in any batch
+  // sequence gives identical results alone or in any batch.  Gathered (CSA)
+  // ranges take up to five tiles (decode at 128K: 1024 + 128 slots = 9 tiles
+  // in two ranges, one wave of CTAs for 64 queries); contiguous (HCA) ranges
+  // up to four (1M context: 65 tiles in 17 ranges of 4)
+  const int mt = csa ? kTcTiles : kTcTilesHca;
   TcPlan p;
-  p.nsplit = n_tiles > 0 ? (n_tiles + kTcTiles - 1) / kTcTiles : 1;
+  p.nsplit = n_tiles > 0 ? (n_tiles + mt - 1) / mt : 1;
   p.tpr = n_tiles > 0 ? (n_tiles + p.nsplit - 1) / p.nsplit : 1;
   return p;
 }
@@ -670,11 +697,12 @@ bool attend_tc_supported(bool csa, int Tq, long long nq, int N, int T_raw, int k
   } else {
     if (N <= 0 || (W > 0 && T_raw <= 0)) return false;
   }
-  return attend_tc_plan(attend_tc_tiles(csa, N, k, W)).nsplit <= 65535;
+  return attend_tc_plan(attend_tc_tiles(csa, N, k, W), csa).nsplit <= 65535;
 }
 
 size_t attend_tc_part_bytes(long long nq, int H, int d, const TcPlan& p) {
-  return p.nsplit > 1 ? static_cast<size_t>(nq) * p.nsplit * H * (d + 1) * sizeof(float) : 0;
+  // up to kTcClusterMax ranges merge inside their cluster: no partials
+  return p.nsplit > kTcClusterMax ? static_cast<size_t>(nq) * p.nsplit * H * (d + 1) * sizeof(float) : 0;
 }
 
 cudaError_t launch_attend_tc(const AttendArgs& a, long long budget, cudaStream_t s) {
@@ -709,14 +737,14 @@ cudaError_t launch_attend_tc(const AttendArgs& a, long long budget, cudaStream_t
     if (a.W > 0 && (!rows_map(&tkr, a.k_raw, a.T_raw) || !rows_map(&tvr, a.v_raw, a.T_raw)))
       return cudaErrorInvalidValue;
   }
-  const TcPlan pl = attend_tc_plan(attend_tc_tiles(csa, a.N, a.k, a.W));
+  const TcPlan pl = attend_tc_plan(attend_tc_tiles(csa, a.N, a.k, a.W), csa);
   TcParams p;
   p.sl2 = a.scale * 1.4426950408889634f;
   p.nsplit = pl.nsplit;
   p.tpr = pl.tpr;
   p.cluster = pl.nsplit > 1 && pl.nsplit <= kTcClusterMax ? 1 : 0;
   p.budget = budget;
-  const size_t smem = 1024 + 2 * kH * 128 + kTcTiles * (2 * kHalfB + kHT * 128) + sizeof(TcBars);
+  const size_t smem = 1024 + 2 * kH * 128 + kTcTiles * 2 * kHalfB + kPSlots * kHT * 128 + sizeof(TcBars);
   const dim3 grid(static_cast<unsigned>(p.nsplit), static_cast<unsigned>(nq));
   cudaError_t e;
   if (csa) {

@@ -143,7 +143,7 @@ size_t attn_part_bytes(bool csa_mode, int B, int Tq, int N, int k, int W, int H,
   const size_t gen = attend_part_bytes(B, Tq, (csa_mode ? k : N) + W, H, d);
   const long long nq = static_cast<long long>(B) * Tq;
   if (!csa::attend_tc_supported(csa_mode, Tq, nq, N, 1, k, H, d, W)) return gen;
-  const csa::TcPlan p = csa::attend_tc_plan(csa::attend_tc_tiles(csa_mode, N, k, W));
+  const csa::TcPlan p = csa::attend_tc_plan(csa::attend_tc_tiles(csa_mode, N, k, W), csa_mode);
   const size_t tc = align_up(csa::attend_tc_part_bytes(nq, H, d, p), kAlignWs);
   return gen > tc ? gen : tc;
 }

@@ -145,15 +145,17 @@ cudaError_t launch_attend_combine(const AttendArgs& a, int nsplit, cudaStream_t 
 // ---- decode attention on tcgen05 (H = 64, d = 128, Tq < 16) -----------------
 // CSA (a.idx != nullptr): the k listed rows and the W window rows, gathered
 // with cp.async; HCA (a.idx == nullptr): every visible entry and the window as
-// TMA tiles.  One CTA per (query, range of up to kTcTiles 128-key tiles); the
-// ranges of a query merge through workspace partials when there are several.
-constexpr int kTcTiles = 4;
+// TMA tiles.  One CTA per (query, range of up to kTcTiles (CSA) or
+// kTcTilesHca (HCA) 128-key tiles); the ranges of a query merge inside their
+// cluster (up to eight) or through workspace partials.
+constexpr int kTcTiles = 5;
+constexpr int kTcTilesHca = 4;
 struct TcPlan {
   int nsplit;  // ranges per query
   int tpr;     // tiles per range
 };
 int attend_tc_tiles(bool csa, int N, int k, int W);  // tiles of the longest key list
-TcPlan attend_tc_plan(int n_tiles);
+TcPlan attend_tc_plan(int n_tiles, bool csa);
 bool attend_tc_supported(bool csa, int Tq, long long nq, int N, int T_raw, int k, int H, int d, int W);
 size_t attend_tc_part_bytes(long long nq, int H, int d, const TcPlan& p);
 cudaError_t launch_attend_tc(const AttendArgs& a, long long wait_budget, cudaStream_t s);

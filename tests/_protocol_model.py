@@ -284,17 +284,27 @@ def indexer_single(ntile: int, stages: int, seed: int, fp8: bool = False, cap: O
 # attend_tc_kernel: K tiles loaded at once, a tile's buffer refilled with V
 # once its score MMAs are done (gather or TMA producers alike), per-tile
 # epilogue (two named barriers per tile among the 8 epilogue warps), output
-# MMAs after every tile's P rows and V rows, one final commit
+# MMAs after every tile's P rows and V rows, one final commit.  A tile's output
+# accumulates in the TMEM columns of its scores (written once every epilogue
+# warp has read them: pfull); ranges of five tiles write their P rows into two
+# buffers in turn (pempty: the output MMAs of the buffer's previous tile are
+# done), shorter ranges into one buffer per tile.
 
-def attend_tc(ntile: int, seed: int) -> bool:
+def attend_tc(ntile: int, seed: int, plant: str = "") -> bool:
     q = Bar(1)
     kfull = [Bar(1) for _ in range(ntile)]
     vfull = [Bar(1) for _ in range(ntile)]
     sdone = [Bar(1) for _ in range(ntile)]
     pfull = [Bar(8) for _ in range(ntile)]
+    pempty = [Bar(1) for _ in range(2)]
     ofull = Bar(1)
     epi_bar = Bar(8)
     buffer = ["empty"] * ntile
+    ring = ntile > 4
+    slot = (lambda j: j % 2) if ring else (lambda j: j)
+    p_owner = [None] * ntile        # tile whose P rows a buffer holds
+    p_read = [True] * ntile         # ... and whether its output MMAs have read them
+    s_reads = [0] * ntile           # epilogue warps that have read tile j's score columns
 
     def producer():
         q.arrive()
@@ -317,13 +327,24 @@ def attend_tc(ntile: int, seed: int) -> bool:
             yield (pfull[j], 0)
             yield (vfull[j], 0)
             assert buffer[j] == "V"
+            assert s_reads[j] == 8, "output written over scores not yet read"
+            assert p_owner[slot(j)] == j, "P rows of another tile"
+            p_read[slot(j)] = True
+            pempty[j % 2].arrive()
         ofull.arrive()
 
     def epilogue(me: int):
         for j in range(ntile):
             yield (sdone[j], 0)
+            s_reads[j] += 1
             yield from named_barrier(epi_bar, 2 * j)      # the quarters' maxima
             yield from named_barrier(epi_bar, 2 * j + 1)  # the per-head offsets
+            if ring and j >= 2 and plant != "pempty":
+                yield (pempty[j % 2], (j // 2 - 1) & 1)
+            s = slot(j)
+            if p_owner[s] != j:
+                assert p_read[s], "P rows written over rows still being read"
+                p_owner[s], p_read[s] = j, False
             pfull[j].arrive()
         yield from named_barrier(epi_bar, 2 * ntile)      # the sums
         yield from named_barrier(epi_bar, 2 * ntile + 1)  # the coefficients

@@ -56,11 +56,15 @@ def test_workspace_sizes(L):
     assert need.value == 256                       # short rows: selected in shared memory
     assert L.csa_index_topk_workspace(1, 1, 5, 64, 128, 4, ctypes.byref(need)) == 0
     assert need.value == 256 + 256                # 8 floats rounded up to 256 bytes
-    # decode, H = 64, d = 128 (tensor-core kernel): 1024 + 128 slots = 9 tiles -> 3
-    # ranges of 3 tiles, H x (d + 1) floats of partials per range
+    # decode, H = 64, d = 128 (tensor-core kernel): 1024 + 128 slots = 9 tiles -> 2
+    # ranges, merged inside their cluster: no partials
     assert L.csa_attend_workspace(64, 1, 64, 128, 1024, 128, ctypes.byref(need)) == 0
-    assert need.value == 256 + (64 * 3 * 64 * 129 * 4 + 255) // 256 * 256
-    # one range (up to 4 tiles): no partials
+    assert need.value == 256
+    # 5200 + 128 slots = 42 tiles -> 9 ranges of 5 tiles, beyond a cluster:
+    # H x (d + 1) floats of partials per range
+    assert L.csa_attend_workspace(64, 1, 64, 128, 5200, 128, ctypes.byref(need)) == 0
+    assert need.value == 256 + (64 * 9 * 64 * 129 * 4 + 255) // 256 * 256
+    # one range (up to 5 tiles): no partials
     assert L.csa_attend_workspace(64, 1, 64, 128, 384, 128, ctypes.byref(need)) == 0
     assert need.value == 256
     # other head counts: the general decode kernel merges its splits inside a cluster
@@ -94,17 +98,20 @@ def test_workspace_sizes(L):
 def test_layer_workspace_holds_the_attention_partials(L):
     """csa_layer's workspace = header + scores + top-k scratch + index lists +
     attention partials; only the last part depends on H.  At the 128K decode
-    shape (B = 64, 32768 entries, top-1024, W = 128) H = 64, d = 128 runs the
-    tensor-core attention with 3 ranges per query; H = 32 merges its splits
-    inside a cluster and needs none."""
-    def size(H):
+    shape (B = 64, 32768 entries, W = 128) H = 64, d = 128 runs the
+    tensor-core attention: top-1024 gives 2 ranges per query, merged inside
+    their cluster (no partials), top-5200 gives 9 ranges, which keep their
+    partials in the workspace; H = 32 merges its splits inside a cluster and
+    needs none."""
+    def size(H, k):
         la = _lib.csa_layer_args()
-        for name, v in dict(B=64, Tq=1, N=32768, m=4, H=H, d=128, H_I=64, d_I=128, k=1024, W=128).items():
+        for name, v in dict(B=64, Tq=1, N=32768, m=4, H=H, d=128, H_I=64, d_I=128, k=k, W=128).items():
             setattr(la, name, v)
         need = ctypes.c_size_t(0)
         assert L.csa_layer_workspace(ctypes.byref(la), ctypes.byref(need)) == 0
         return need.value
-    assert size(64) - size(32) == (64 * 3 * 64 * 129 * 4 + 255) // 256 * 256
+    assert size(64, 1024) == size(32, 1024)
+    assert size(64, 5200) - size(32, 5200) == (64 * 9 * 64 * 129 * 4 + 255) // 256 * 256
 
 
 def test_validation_before_any_launch(L):

@@ -22,7 +22,7 @@ def test_decode_1m_step_is_zeroing_indexer_and_fused_tail():
 
 
 def test_decode_128k_step_is_one_pass_topk_and_cluster_merged_attention():
-    # 32768 entries: one top-k kernel; 1024 + 128 slots = 9 tiles -> 3 ranges,
+    # 32768 entries: one top-k kernel; 1024 + 128 slots = 9 tiles -> 2 ranges,
     # merged inside their cluster (no merge kernel)
     assert _launches("decode_128k") == 2 + 1 + 1
 
@@ -32,7 +32,8 @@ def test_mid_and_long_rows_and_many_ranges():
     count = lambda **kw: bench.DecodeStep.kernels_per_step(SimpleNamespace(wl=wl.replace(**kw), Tq=1))
     assert count(T=4 * 40000) == 2 + 2 + 1              # select + finish between 32768 and 65536 entries
     assert count(T=4 * 16384) == 2 + 1                  # short rows: indexer, one-pass top-k, attention
-    assert count(T=4 * 40000, k=4096) == 2 + 2 + 1 + 1  # 33 tiles -> 9 ranges: the merge kernel too
+    assert count(T=4 * 40000, k=4096) == 2 + 2 + 1      # 33 tiles -> 7 ranges: merged in the cluster
+    assert count(T=4 * 40000, k=5200) == 2 + 2 + 1 + 1  # 42 tiles -> 9 ranges: the merge kernel too
 
 
 def test_tail_queries_need_the_histogram_pass():

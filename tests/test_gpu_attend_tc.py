@@ -2,14 +2,15 @@
 queries per sequence) against the oracle, |err| <= 1e-2 + 1e-2 |ref| and lse to
 1e-4.
 
-Dense HCA (TMA key tiles): one key range (output written directly), up to
-eight ranges merged inside their thread-block cluster and more ranges merged
-by the combine kernel (some ranges empty for the shorter query), entries that are not a whole number of 128-key tiles, the
+Dense HCA (TMA key tiles, ranges of up to four tiles): one key range (output
+written directly), up to eight ranges merged inside their thread-block
+cluster and more ranges merged by the combine kernel (some ranges empty for the shorter query), entries that are not a whole number of 128-key tiles, the
 window clipped at token 0, the window alone, no window, an empty key set, and
 window rows outside the raw buffer.
 
-CSA (gathered rows): ragged index lists with holes, lists spanning several
-ranges (cluster merge, and the combine kernel beyond eight), the window alone (k = 0), an empty key set, and indices outside the
+CSA (gathered rows, ranges of up to five tiles): ragged index lists with
+holes, lists spanning several ranges (cluster merge, and the combine kernel
+beyond eight), the window alone (k = 0), an empty key set, and indices outside the
 entries (flagged and skipped)."""
 import math
 
@@ -47,6 +48,14 @@ def test_hca_tc_cluster_merged_ranges_with_empty_ones():
     pos = np.array([[1999, 300, 0]])
     _attn_case(37, 1, 3, 2000, 64, 128, 0, 128, 1, pos, 4000, 0, hca=True)
     _attn_case(38, 1, 3, 2000, 64, 128, 0, 128, 1, pos, 4000, 0, hca=True, out_dtype=torch.float32)
+
+
+def test_hca_tc_two_ranges_of_three_tiles():
+    """600 entries at m = 1 with W = 128: 5 + 1 tiles -> 2 ranges of 3 tiles
+    merged inside their cluster; queries that see all, some and none of the
+    entries."""
+    pos = np.array([[599, 200, 0, 383]])
+    _attn_case(39, 1, 4, 600, 64, 128, 0, 128, 1, pos, 1200, 0, hca=True)
 
 
 def test_hca_tc_no_window_and_empty_key_set():
@@ -97,12 +106,21 @@ def test_csa_tc_ragged_lists_with_holes_one_range():
 
 
 def test_csa_tc_many_ranges():
-    """k = 2000, W = 128: 17 tiles -> 5 ranges of at most 4 tiles, merged inside
-    their cluster, for 3 queries of one sequence; k = 4500: 37 tiles -> 10
-    ranges, merged by the combine kernel."""
+    """k = 2000, W = 128: 17 tiles -> 4 ranges of at most 5 tiles (two P
+    buffers in turn), merged inside their cluster, for 3 queries of one
+    sequence; k = 5200: 42 tiles -> 9 ranges, merged by the combine kernel."""
     pos = np.array([[131071, 100000, 9000]])
     _attn_case(43, 1, 3, 32768, 64, 128, 2000, 128, 4, pos, 140000, 0, holes=True)
-    _attn_case(47, 1, 3, 32768, 64, 128, 4500, 128, 4, pos, 140000, 0, holes=True, out_dtype=torch.float32)
+    _attn_case(47, 1, 3, 32768, 64, 128, 5200, 128, 4, pos, 140000, 0, holes=True, out_dtype=torch.float32)
+
+
+def test_csa_tc_decode_128k_shape_two_ranges():
+    """k = 1000, W = 128 (the shape of decode at 128K context): 9 tiles -> ranges
+    of 5 and 4 tiles merged inside their cluster; 2 sequences, ragged lists
+    with holes, a query that sees fewer entries than k."""
+    pos = np.array([[131071, 3000], [100000, 131071]])
+    _attn_case(48, 2, 2, 32768, 64, 128, 1000, 128, 4, pos, 140000, 0, holes=True)
+    _attn_case(49, 2, 2, 32768, 64, 128, 1000, 128, 4, pos, 140000, 0, holes=True, out_dtype=torch.float32)
 
 
 def test_csa_tc_window_only_and_empty():

@@ -66,8 +66,9 @@ def _decode_attend_inputs(seed, B, N, k, W, H=64, d=128):
 @pytest.mark.parametrize("mode", ["csa_gather", "hca_tiles"])
 def test_tensor_core_attention_wait_budget_runs_out(mode):
     """The tcgen05 decode attention (H = 64, d = 128, more than four 128-key
-    tiles per query: the CSA case's 3 ranges merge inside their cluster, the
-    HCA case's 9 in a second kernel) with a one-cycle wait budget: CSA_FLAG_TIMEOUT is set, the kernel drains its copies and
+    tiles per query: the CSA case's 2 ranges of 5 and 4 tiles merge inside
+    their cluster, the HCA case's 9 in a second kernel) with a one-cycle wait
+    budget: CSA_FLAG_TIMEOUT is set, the kernel drains its copies and
     frees its tensor memory, and the next call with the default budget gives
     the reference result bit for bit."""
     import long_context_sparse_23_b300 as csa

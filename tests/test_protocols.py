@@ -66,9 +66,17 @@ def test_indexer_missing_item_waits_are_caught(plant):
 
 
 def test_attend_tc_protocol_completes_without_hazards():
-    for ntile in range(1, 5):   # a range with no tile writes its empty result and uses no barrier
+    for ntile in range(1, 6):   # a range with no tile writes its empty result and uses no barrier
         for trial in range(100):
             assert M.attend_tc(ntile, trial), ntile
+
+
+def test_attend_tc_missing_p_buffer_wait_is_caught():
+    # five tiles share two P buffers: without the wait for the output MMAs of
+    # a buffer's previous tile, some interleaving overwrites rows still unread
+    with pytest.raises(AssertionError):
+        for t in range(2000):
+            M.attend_tc(5, t, plant="pempty")
 
 
 def test_planted_mistakes_are_caught(monkeypatch):
