@@ -66,6 +66,25 @@ constexpr int kProducers = 96;
 constexpr long long kDrainBudget = 1LL << 31;
 constexpr int kPSlots = 2;         // P^T buffers, used by tiles in turn
 constexpr int kTcClusterMax = 8;   // ranges of a query merged inside one cluster (portable size)
+// cluster merge buffers in the K/V region (free once every MMA is done):
+// the range's partial [H][kD] + [H] at 0, the shares received after it
+constexpr int kRecvOff = 34 * 1024;
+constexpr int kRecvBytes = 33 * 1024;  // >= ns * ceil(H * kD / 4 / ns) * 16 for 2 <= ns <= 8
+static_assert(kRecvOff >= (kH * kD + kH) * 4, "partial before the receive buffers");
+static_assert(kRecvOff + kRecvBytes + kTcClusterMax * kH * 4 <= kTcTiles * 2 * kHalfB,
+              "merge buffers inside the K/V region");
+
+// One bulk copy from this CTA's shared memory into CTA ``rank`` of the
+// cluster, to the same offset as ``dst``, completing on that CTA's mbarrier
+// at the offset of ``bar``.
+__device__ __forceinline__ void bulk_to_rank(void* dst, const void* src, uint32_t bytes, uint64_t* bar, int rank) {
+  uint32_t d, mb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_u32(dst)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(mb) : "r"(smem_u32(bar)), "r"(rank));
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(d),
+               "r"(smem_u32(src)), "r"(bytes), "r"(mb)
+               : "memory");
+}
 
 struct TcParams {
   float sl2;  // scale * log2(e)
@@ -83,6 +102,7 @@ struct __align__(8) TcBars {
   uint64_t pfull[kTcTiles];
   uint64_t pempty[2];  // P buffer read by the MMAs of its last tile
   uint64_t ofull;
+  uint64_t mrecv;      // cluster merge: every range's share of the partial has landed
 };
 
 // Shared-memory descriptor of an MN-major operand in the 128-byte swizzle
@@ -224,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int j = 0; j < kPSlots; ++j) mbar_init(&bars->pempty[j], 1);
     mbar_init(&bars->ofull, 1);
+    mbar_init(&bars->mrecv, 1);
     mbar_fence_init();
     tma_prefetch_desc(&tmq);
     if (!kGather) {
@@ -609,26 +630,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tbase, kTmemCols);
   }
   if (p.cluster) {
-    // merge of the query's ranges: this CTA (cluster rank = range) takes a
-    // contiguous share of the H x kD outputs in groups of four columns and
-    // folds every range's partial in range order, as the combine kernel does
-    cg::cluster_group cl = cg::this_cluster();
-    cl.sync();  // every range's partial is in its CTA's shared memory
-    const int ns = p.nsplit;
-    const float* rp[kTcClusterMax];
-#pragma unroll
-    for (int r = 0; r < kTcClusterMax; ++r) rp[r] = r < ns ? cl.map_shared_rank(part_s, r) : part_s;
+    // merge of the query's ranges: the cluster rank (= range) r owns a
+    // contiguous share [g_lo, g_hi) of the H x kD outputs in groups of four
+    // columns.  Once every CTA of the cluster is past its main loop, each
+    // pushes every share of its partial, and its log2-sum-exps, into the
+    // owner's receive buffer by bulk copies completing on the owner's mrecv;
+    // each owner folds the ranges' partials of its share in range order, as
+    // the combine kernel does
     constexpr int kGroups = H * kD / 4;
+    const int ns = p.nsplit;
+    const int cap = (kGroups + ns - 1) / ns;  // groups of one share, at most
     const int g_lo = split * kGroups / ns, g_hi = (split + 1) * kGroups / ns;
-    for (int g = g_lo + tid; g < g_hi; g += kThreads) {
+    float4* recv = reinterpret_cast<float4*>(kv + kRecvOff);               // [ns][cap]
+    float* recv_l = reinterpret_cast<float*>(kv + kRecvOff + kRecvBytes);  // [ns][H]
+    fence_proxy_async();  // the partial, written by the threads, is read by bulk copies
+    cg::this_cluster().sync();  // every receive buffer of the cluster is free
+    if (tid == 0) {
+      mbar_expect_tx(&bars->mrecv, static_cast<uint32_t>(ns * ((g_hi - g_lo) * 16 + H * 4)));
+      for (int o = 0; o < ns; ++o) {
+        const int olo = o * kGroups / ns, ohi = (o + 1) * kGroups / ns;
+        bulk_to_rank(recv + split * cap, part_s + 4 * olo, static_cast<uint32_t>((ohi - olo) * 16), &bars->mrecv, o);
+        bulk_to_rank(recv_l + split * H, part_s + H * kD, H * 4, &bars->mrecv, o);
+      }
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+    bool got = mbar_wait_sleep(&bars->mrecv, 0, p.budget, abort_v);
+    if (!got) {
+      // reported, then waited out: no copy may still be writing this CTA's
+      // shared memory when it exits
+      if (tid == 0) raise_flag(a.errw, kFlagTimeout);
+      mbar_wait_sleep(&bars->mrecv, 0, kDrainBudget, nullptr);
+    }
+    for (int g = g_lo + tid; got && g < g_hi; g += kThreads) {
       const int h = g / (kD / 4), c4 = (g % (kD / 4)) * 4;
       float ls[kTcClusterMax];
       float4 vs[kTcClusterMax];
 #pragma unroll
       for (int r = 0; r < kTcClusterMax; ++r) {
         if (r < ns) {
-          ls[r] = rp[r][H * kD + h];
-          vs[r] = *reinterpret_cast<const float4*>(rp[r] + h * kD + c4);
+          ls[r] = recv_l[r * H + h];
+          vs[r] = recv[r * cap + (g - g_lo)];
         }
       }
       float M = -INFINITY;
@@ -661,7 +702,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (a.lse && c4 == 0) a.lse[qi * H + h] = den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
     }
-    cl.sync();  // no CTA leaves while another still reads its shared memory
+    // this CTA's partial has been read by every copy before it exits
+    if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   }
 }
 
