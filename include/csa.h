@@ -223,12 +223,13 @@ csa_status csa_index_topk(const void* q_idx, const void* k_idx, const float* w,
  * with CSA_FLAG_INDEX.  bf16 MMAs, fp32 softmax and accumulation.
  * Workspace: the error word and the split partials of long key lists.
  * Decode-shaped calls (Tq < 16) with H = 64 and d = 128 run on the tcgen05
- * tensor cores and cut each query's k + W slots into n_r = ceil(n_t / 4)
- * ranges of 128-slot tiles, n_t = ceil((k + W) / 128); with n_r > 1 they
- * need B * Tq * n_r * H * (d + 1) * 4 bytes of partials (e.g. k = 1024,
- * W = 128: 3 ranges, 99 KB per query).  Other shapes need partials only for
- * k + W > 131072.  The split depends on k + W only, never on B, so a
- * sequence gives the same result alone or in any batch.
+ * tensor cores and cut each query's k + W slots into n_r = ceil(n_t / 5)
+ * ranges of 128-slot tiles, n_t = ceil((k + W) / 128); up to 8 ranges merge
+ * inside a thread-block cluster (e.g. k = 1024, W = 128: 2 ranges, no
+ * partials), more need B * Tq * n_r * H * (d + 1) * 4 bytes of partials
+ * (e.g. k = 5200, W = 128: 9 ranges, 297 KB per query).  Other shapes need
+ * partials only for k + W > 131072.  The split depends on k + W only, never
+ * on B, so a sequence gives the same result alone or in any batch.
  * ------------------------------------------------------------------------ */
 csa_status csa_attend_workspace(int B, int Tq, int H, int d, int k, int W, size_t* bytes);
 csa_status csa_attend(const void* q, const void* k_cmp, const void* v_cmp, const int32_t* idx,
@@ -279,8 +280,10 @@ csa_status csa_attend_noalloc(const void* q, const void* k_cmp, const void* v_cm
  * densely with no selection, plus the same sliding window.  As csa_attend
  * with J's first part = every visible entry b < min(N, floor((t+1)/m)).
  * Decode-shaped calls with H = 64 and d = 128 load the entries as TMA tiles
- * on the tcgen05 path; there n_t = ceil(N / 128) + ceil(W / 128) (e.g.
- * N = 8192, W = 128: 17 ranges, 561 KB of partials per query).
+ * on the tcgen05 path, in ranges of up to 4 tiles; there
+ * n_t = ceil(N / 128) + ceil(W / 128) and n_r = ceil(n_t / 4) (e.g.
+ * N = 8192, W = 128: 17 ranges, 561 KB of partials per query; up to 8
+ * ranges merge inside a cluster and need none).
  * ------------------------------------------------------------------------ */
 csa_status hca_attend_workspace(int B, int Tq, int N, int H, int d, int W, size_t* bytes);
 csa_status hca_attend(const void* q, const void* k_cmp, const void* v_cmp,
