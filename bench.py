@@ -136,7 +136,7 @@ class DecodeStep:
         (long rows): histogram zeroing, the indexer (which also accumulates the
         top-k histogram when Tq == 1, else a histogram kernel follows), then
         over 65536 entries the fused top-k + attention kernel; up to 32768
-        entries the one-CTA-per-query top-k and the attention; in between the
+        entries the two-CTA-per-query top-k and the attention; in between the
         select and finish passes of the top-k and the attention.  Up to 16384
         entries: the indexer, the one-pass top-k and the attention.  The
         tensor-core decode attention (H = 64, d = 128) merges the key ranges of

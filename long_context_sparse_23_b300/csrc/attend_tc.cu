@@ -661,34 +661,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid == 0) raise_flag(a.errw, kFlagTimeout);
       mbar_wait_sleep(&bars->mrecv, 0, kDrainBudget, nullptr);
     }
+    // (loops over the ranges kept rolled: this code runs once per CTA, and a
+    // short body is fetched sooner than eight unrolled copies)
     for (int g = g_lo + tid; got && g < g_hi; g += kThreads) {
       const int h = g / (kD / 4), c4 = (g % (kD / 4)) * 4;
-      float ls[kTcClusterMax];
-      float4 vs[kTcClusterMax];
-#pragma unroll
-      for (int r = 0; r < kTcClusterMax; ++r) {
-        if (r < ns) {
-          ls[r] = recv_l[r * H + h];
-          vs[r] = recv[r * cap + (g - g_lo)];
-        }
-      }
       float M = -INFINITY;
-#pragma unroll
-      for (int r = 0; r < kTcClusterMax; ++r)
-        if (r < ns) M = fmaxf(M, ls[r]);
+#pragma unroll 1
+      for (int r = 0; r < ns; ++r) M = fmaxf(M, recv_l[r * H + h]);
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       float den = 0.f;
       if (M != -INFINITY) {
-#pragma unroll
-        for (int r = 0; r < kTcClusterMax; ++r) {
-          if (r < ns) {
-            const float f = ex2(ls[r] - M);
-            den += f;
-            acc.x = fmaf(f, vs[r].x, acc.x);
-            acc.y = fmaf(f, vs[r].y, acc.y);
-            acc.z = fmaf(f, vs[r].z, acc.z);
-            acc.w = fmaf(f, vs[r].w, acc.w);
-          }
+#pragma unroll 1
+        for (int r = 0; r < ns; ++r) {
+          const float f = ex2(recv_l[r * H + h] - M);
+          const float4 v = recv[r * cap + (g - g_lo)];
+          den += f;
+          acc.x = fmaf(f, v.x, acc.x);
+          acc.y = fmaf(f, v.y, acc.y);
+          acc.z = fmaf(f, v.z, acc.z);
+          acc.w = fmaf(f, v.w, acc.w);
         }
       }
       const float val[4] = {den > 0.f ? acc.x / den : 0.f, den > 0.f ? acc.y / den : 0.f,

@@ -15,7 +15,7 @@
 // compaction in index order writes the output.
 //
 // Mid rows (N <= 32768, e.g. decode at 128K context): the histogram below,
-// then one CTA per query selects from it (topk_mid_kernel).
+// then a cluster of two CTAs per query selects from it (topk_mid_kernel).
 //
 // Long rows (decode: few queries, up to ~10^6 keys each), three grid-wide
 // steps instead of one CTA per query:
@@ -32,9 +32,13 @@
 //     in index order.  When the candidates would not fit (a bucket holding
 //     very many near-equal scores), the finish kernel selects from the whole
 //     row in global memory instead (slower, same result).
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "select.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace csa {
 
@@ -87,64 +91,84 @@ __global__ void __launch_bounds__(kShortThreads) topk_short_kernel(TopkArgs a) {
 
 // ---------------------------------------------------------------- mid rows
 // Rows of kTopkShortMax < N <= kTopkMidMax entries with the bucket histogram
-// ready (decode at 128K context: 32768 blocks): one CTA per query instead of
-// the select and finish passes, with every step spread evenly over the
+// ready (decode at 128K context: 32768 blocks): a cluster of two CTAs per
+// query instead of the select and finish passes, rank r holding the entries
+// [r E, (r + 1) E), E = kTopkMidMax / 2, every step spread evenly over its
 // threads:
-//  1. the row is copied to shared memory (cp.async) while the bucket beta of
-//     the k-th largest key is found from the histogram;
+//  1. the half row is copied to shared memory (cp.async) while the bucket
+//     beta of the k-th largest key is found from the histogram;
 //  2. candidates (bucket >= beta) by one float comparison per score against
 //     the lowest score of bucket beta (the key map is order-preserving),
 //     their indices appended to a list (warp-aggregated, any order);
 //  3. per candidate: bucket above beta -> kept (bit in a bitmap over the
-//     row), bucket beta -> a second-level histogram of key bits 19..8;
+//     half row), bucket beta -> a second-level histogram of key bits 19..8;
+//     each rank pushes its counts and second level into the other rank's
+//     shared memory, and after a cluster barrier both hold the totals;
 //  4. the sub-bucket holding the rest of the k-th largest, then at most one
-//     8-bit pass, fix the exact rule; the candidates of bucket beta set their
+//     8-bit pass (its histogram exchanged the same way), fix the exact rule,
+//     identically in both ranks; the candidates of bucket beta set their
 //     kept or tied bit;
-//  5. thread t owns bitmap word t (blocks 32t .. 32t + 31): two block scans
-//     keep the k_rem lowest-index ties and give each word's output position,
-//     and the kept indices are written in ascending order.
+//  5. rank 0 pushes its tie and kept counts to rank 1; thread t owns bitmap
+//     word t (blocks 32t .. 32t + 31 of its half): a block scan of the words'
+//     (kept, tied) counts keeps the k_rem lowest-index ties of the row and
+//     gives each word's output position, and the kept indices are written in
+//     ascending order.
 // The candidate counts are checked against the histogram: a histogram that
 // does not match the scores (an indexer that gave up, non-finite scores) or
-// more candidates than the list holds (a row of near-equal scores) sends the
-// CTA to digit passes over the whole row in global memory instead, so the
+// more candidates than a list holds (a row of near-equal scores) sends rank
+// 0 to digit passes over the whole row in global memory instead, so the
 // output is the exact selection of the given scores in every case.
-constexpr int kMidThreads = 1024;
-constexpr int kMidWords = kTopkMidMax / 32;  // bitmap words, one per thread
-constexpr int kMidList = 8192;               // candidate indices staged
-static_assert(kMidWords == kMidThreads && kTopkMidMax % (4 * kMidThreads) == 0, "mid rows: layout");
+constexpr int kMidRanks = 2;                      // CTAs per query (one cluster)
+constexpr int kMidThreads = 512;
+constexpr int kMidHalf = kTopkMidMax / kMidRanks;  // entries per CTA
+constexpr int kMidWords = kMidHalf / 32;           // bitmap words, one per thread
+constexpr int kMidList = 8192;                     // candidate indices staged per CTA
+static_assert(kMidWords == kMidThreads && kMidHalf % (4 * kMidThreads) == 0, "mid rows: layout");
 
 // dynamic shared memory of topk_mid_kernel, in 32-bit words
-constexpr int kMidSmemWords = kTopkMidMax + 2 * kMidWords + kTopkBins + kMidList;
+constexpr int kMidSmemWords = kMidHalf + 2 * kMidWords + 2 * kTopkBins + kMidList;
 
 __global__ void __launch_bounds__(kMidThreads) topk_mid_kernel(TopkArgs a) {
+  // every CTA of the cluster has started before any writes another's shared
+  // memory (the wait is before the first such write)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   pdl_wait_then_release();
   extern __shared__ __align__(16) uint32_t msm[];
-  float* sf = reinterpret_cast<float*>(msm);  // [kTopkMidMax] the row's scores
-  uint32_t* bm = msm + kTopkMidMax;           // [kMidWords] kept for sure
+  float* sf = reinterpret_cast<float*>(msm);  // [kMidHalf] this half of the row's scores
+  uint32_t* bm = msm + kMidHalf;              // [kMidWords] kept for sure
   uint32_t* eqm = bm + kMidWords;             // [kMidWords] equal to the rule's prefix
-  uint32_t* h2 = eqm + kMidWords;             // [kTopkBins] bucket beta: key bits 19..8
-  uint32_t* list = h2 + kTopkBins;            // [kMidList] candidate indices
-  __shared__ uint32_t h3[256], tmp[32], wgt[32], weq[32];
+  uint32_t* h2 = eqm + kMidWords;             // [kTopkBins] bucket beta, key bits 19..8: this half's
+  uint32_t* h2p = h2 + kTopkBins;             // [kTopkBins] ... the other half's, then both
+  uint32_t* list = h2p + kTopkBins;           // [kMidList] candidate indices (in the half)
+  __shared__ uint32_t h3[256], h3p[256], tmp[32], wgt[32], weq[32];
   __shared__ Rule rule;
   __shared__ Bucket sb, sb2;
   __shared__ uint32_t n_list, n_gt;
-  const long long q = blockIdx.x;
+  __shared__ uint32_t peer_c, peer_g;    // the other rank's candidate and above-beta counts
+  __shared__ uint32_t off_eq, off_kept;  // rank 1: rank 0's tied and kept-for-sure counts
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = static_cast<int>(cl.block_rank()), peer = rank ^ 1;
+  const long long q = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31;
   const int n_vis = visible(a, q);
   int32_t* out = a.idx_out + q * a.k;
   float* sout = a.score_out ? a.score_out + q * a.k : nullptr;
   const float* row = a.scores + q * a.ld;
-  if (n_vis <= a.k) {
-    keep_all(a, row, n_vis, out, sout);
+  if (n_vis <= a.k) {  // both ranks (no cluster barrier follows)
+    if (rank == 0) keep_all(a, row, n_vis, out, sout);
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
     return;
   }
   const uint32_t k = static_cast<uint32_t>(a.k);
-  constexpr int R = kTopkMidMax / (4 * kMidThreads);  // float4 rounds per thread
-  // (1) the row: whole vectors by cp.async (past the row: zero-filled, never read as scores)
+  const int base = rank * kMidHalf;
+  const int n_loc = min(max(n_vis - base, 0), kMidHalf);  // entries of this half
+  const float* rowl = row + base;
+  constexpr int R = kMidHalf / (4 * kMidThreads);  // float4 rounds per thread
+  // (1) the half row: whole vectors by cp.async (past it: zero-filled, never read as scores)
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const int i = 4 * (tid + kMidThreads * r);
-    cp_async16(sf + i, row + (i + 3 < n_vis ? i : 0), i + 3 < n_vis);
+    cp_async16(sf + i, rowl + (i + 3 < n_loc ? i : 0), i + 3 < n_loc);
   }
   cp_async_commit();
   for (int i = tid; i < 2 * kMidWords + kTopkBins; i += kMidThreads) bm[i] = 0u;  // bm, eqm, h2
@@ -154,9 +178,9 @@ __global__ void __launch_bounds__(kMidThreads) topk_mid_kernel(TopkArgs a) {
   }
   const Bucket bk = find_bucket<kMidThreads>(a.hist + q * kTopkBins, k, tmp, &sb);
   cp_async_wait<0>();
-  if ((n_vis & 3) && ((n_vis >> 2) % kMidThreads) == tid) {
-    const int i = n_vis & ~3;  // the partial last vector
-    for (int e = 0; i + e < n_vis; ++e) sf[i + e] = row[i + e];
+  if ((n_loc & 3) && ((n_loc >> 2) % kMidThreads) == tid) {
+    const int i = n_loc & ~3;  // the partial last vector
+    for (int e = 0; i + e < n_loc; ++e) sf[i + e] = rowl[i + e];
   }
   __syncthreads();
   const uint32_t beta = static_cast<uint32_t>(bk.beta);
@@ -169,10 +193,10 @@ __global__ void __launch_bounds__(kMidThreads) topk_mid_kernel(TopkArgs a) {
   for (int r = 0; r < R; ++r) {
     const int i = 4 * (tid + kMidThreads * r);
     const float4 v = *reinterpret_cast<const float4*>(sf + i);
-    mc |= (i < n_vis && v.x >= lo_b ? 1u : 0u) << (4 * r);
-    mc |= (i + 1 < n_vis && v.y >= lo_b ? 1u : 0u) << (4 * r + 1);
-    mc |= (i + 2 < n_vis && v.z >= lo_b ? 1u : 0u) << (4 * r + 2);
-    mc |= (i + 3 < n_vis && v.w >= lo_b ? 1u : 0u) << (4 * r + 3);
+    mc |= (i < n_loc && v.x >= lo_b ? 1u : 0u) << (4 * r);
+    mc |= (i + 1 < n_loc && v.y >= lo_b ? 1u : 0u) << (4 * r + 1);
+    mc |= (i + 2 < n_loc && v.z >= lo_b ? 1u : 0u) << (4 * r + 2);
+    mc |= (i + 3 < n_loc && v.w >= lo_b ? 1u : 0u) << (4 * r + 3);
   }
   {
     const uint32_t c = static_cast<uint32_t>(__popc(mc));
@@ -182,20 +206,21 @@ __global__ void __launch_bounds__(kMidThreads) topk_mid_kernel(TopkArgs a) {
       const uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += n;
     }
-    uint32_t base = 0;
-    if (lane == 31) base = atomicAdd(&n_list, incl);
-    uint32_t pos = __shfl_sync(0xffffffffu, base, 31) + incl - c;
+    uint32_t b0 = 0;
+    if (lane == 31) b0 = atomicAdd(&n_list, incl);
+    uint32_t pos = __shfl_sync(0xffffffffu, b0, 31) + incl - c;
     while (mc) {
       const int j = __ffs(mc) - 1;
       mc &= mc - 1;
-      if (pos < static_cast<uint32_t>(kMidList)) list[pos] = static_cast<uint32_t>(4 * (tid + kMidThreads * (j >> 2)) + (j & 3));
+      if (pos < static_cast<uint32_t>(kMidList))
+        list[pos] = static_cast<uint32_t>(4 * (tid + kMidThreads * (j >> 2)) + (j & 3));
       ++pos;
     }
   }
   __syncthreads();
   const uint32_t C = n_list;
-  bool whole_row = bk.beta < 0 || C > static_cast<uint32_t>(kMidList);
-  if (!whole_row) {
+  const bool fits = bk.beta >= 0 && C <= static_cast<uint32_t>(kMidList);
+  if (fits) {
     // (3) keys above bucket beta are kept; bucket beta's keys feed the second level
     uint32_t g = 0;
     for (uint32_t e = tid; e < C; e += kMidThreads) {
@@ -212,18 +237,34 @@ __global__ void __launch_bounds__(kMidThreads) topk_mid_kernel(TopkArgs a) {
     if (lane == 0 && g) atomicAdd(&n_gt, g);
   }
   __syncthreads();
+  // push this half's counts and second level into the other rank
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  {
+    uint32_t* rp = cl.map_shared_rank(h2p, peer);
+    for (int i = tid; i < kTopkBins; i += kMidThreads) rp[i] = h2[i];
+    if (tid == 0) {
+      *cl.map_shared_rank(&peer_c, peer) = fits ? C : 0xffffffffu;  // a list that overflowed poisons the total
+      *cl.map_shared_rank(&peer_g, peer) = n_gt;
+    }
+  }
+  cl.sync();  // both halves' counts and second levels are here
   // the candidates must be exactly the histogram's keys in buckets >= beta
-  if (!whole_row) whole_row = n_gt != bk.above || C != bk.above + bk.hb;
+  const bool whole_row = !fits || peer_c == 0xffffffffu || n_gt + peer_g != bk.above ||
+                         C + peer_c != bk.above + bk.hb;
   if (whole_row) {
-    const Rule r = digit_select<kMidThreads>(GlobalKeys{row}, n_vis, Rule{0u, 0u, k, 0u}, 24, h3, tmp, &rule);
-    compact_row<kMidThreads>(GlobalKeys{row}, n_vis, r, out, sout, wgt, weq);
+    if (rank == 0) {
+      const Rule r = digit_select<kMidThreads>(GlobalKeys{row}, n_vis, Rule{0u, 0u, k, 0u}, 24, h3, tmp, &rule);
+      compact_row<kMidThreads>(GlobalKeys{row}, n_vis, r, out, sout, wgt, weq);
+    }
     return;
   }
+  for (int i = tid; i < kTopkBins; i += kMidThreads) h2p[i] += h2[i];
+  __syncthreads();
   // (4) the rule: sub-bucket of bits 19..8 from the second level, then at most one 8-bit pass
-  const Bucket b2 = find_bucket<kMidThreads>(h2, k - bk.above, tmp, &sb2);
+  const Bucket b2 = find_bucket<kMidThreads>(h2p, k - bk.above, tmp, &sb2);
   Rule r{(beta << 20) | (static_cast<uint32_t>(b2.beta) << 8), 0xffffff00u, k - bk.above - b2.above,
          b2.hb == k - bk.above - b2.above ? 1u : 0u};
-  if (!r.done) {
+  if (!r.done) {  // the same in both ranks
     if (tid < 256) h3[tid] = 0u;
     __syncthreads();
     for (uint32_t e = tid; e < C; e += kMidThreads) {
@@ -231,7 +272,11 @@ __global__ void __launch_bounds__(kMidThreads) topk_mid_kernel(TopkArgs a) {
       if ((key & r.mask) == r.prefix) atomicAdd(&h3[key & 255u], 1u);
     }
     __syncthreads();
-    pick_digit<kMidThreads>(h3, r, 0, tmp, &rule);
+    if (tid < 256) cl.map_shared_rank(h3p, peer)[tid] = h3[tid];
+    cl.sync();  // both halves' last digit counts are here
+    if (tid < 256) h3p[tid] += h3[tid];
+    __syncthreads();
+    pick_digit<kMidThreads>(h3p, r, 0, tmp, &rule);
     r = rule;
   }
   for (uint32_t e = tid; e < C; e += kMidThreads) {
@@ -244,25 +289,36 @@ __global__ void __launch_bounds__(kMidThreads) topk_mid_kernel(TopkArgs a) {
     }
   }
   __syncthreads();
-  // (5) word tid: the k_rem lowest-index ties overall, then the output position
-  uint32_t wq = eqm[tid];
-  const uint32_t ne = static_cast<uint32_t>(__popc(wq));
-  const uint32_t eq_before = block_incl_scan<kMidThreads>(ne, tmp) - ne;
+  // (5) word tid: kept-for-sure and tied counts; prefix sums of both in one
+  // scan (each total below 2^16)
+  uint32_t wk = bm[tid], wq = eqm[tid];
+  const uint32_t ng = static_cast<uint32_t>(__popc(wk)), ne = static_cast<uint32_t>(__popc(wq));
+  const uint32_t incl = block_incl_scan<kMidThreads>(ng | (ne << 16), tmp);
+  if (rank == 0 && tid == kMidThreads - 1) {  // rank 1's words follow rank 0's
+    *cl.map_shared_rank(&off_kept, 1) = incl & 0xffffu;
+    *cl.map_shared_rank(&off_eq, 1) = incl >> 16;
+  }
+  if (rank == 0 && tid == 0) {
+    off_kept = 0u;
+    off_eq = 0u;
+  }
+  cl.sync();  // rank 0's counts are in rank 1
+  const uint32_t excl = incl - (ng | (ne << 16));
+  const uint32_t eq_before = off_eq + (excl >> 16);  // ties in lower blocks of the whole row
+  const uint32_t kept_before = off_kept + (excl & 0xffffu) + min(eq_before, r.k_rem);
   uint32_t take = r.k_rem > eq_before ? min(ne, r.k_rem - eq_before) : 0u;
-  uint32_t wk = bm[tid];
   for (; take > 0; --take) {
     const uint32_t low = wq & (0u - wq);
     wk |= low;
     wq ^= low;
   }
-  const uint32_t nk = static_cast<uint32_t>(__popc(wk));
-  uint32_t pos = block_incl_scan<kMidThreads>(nk, tmp) - nk;
+  uint32_t pos = kept_before;
   while (wk) {
     const int bit = __ffs(wk) - 1;
     wk &= wk - 1;
     const int i = 32 * tid + bit;
     if (pos < k) {
-      out[pos] = i;
+      out[pos] = base + i;
       if (sout) sout[pos] = key_score(score_key(sf[i]));
     }
     ++pos;
@@ -697,7 +753,8 @@ cudaError_t launch_topk(const TopkArgs& a, bool hist_ready, cudaStream_t s) {
     const size_t smem = static_cast<size_t>(kMidSmemWords) * 4;
     e = ensure_dyn_smem<topk_mid_kernel>(static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    return launch_k(topk_mid_kernel, dim3(static_cast<unsigned>(nq)), dim3(kMidThreads), smem, s, 1, a);
+    return launch_k(topk_mid_kernel, dim3(kMidRanks, static_cast<unsigned>(nq)), dim3(kMidThreads), smem, s,
+                    kMidRanks, a);
   }
   e = launch_k(topk_select_kernel, grid, dim3(kSelThreads), 0, s, 1, a);
   if (e != cudaSuccess) return e;
