@@ -126,3 +126,19 @@ def test_topk_mid_rows_ties_and_full_buckets():
     s[3, 0] = 1000.0 + rng.integers(0, 512, N) / 4096.0              # one bucket holds the row
     s[4, 0] = np.round((rng.standard_normal(N) * 30 + 150) * 4) / 4  # quarter grid
     _check(s, np.full((5, 1), 4 * N - 1), N, m, k)
+
+
+def test_topk_mid_rows_one_half_overflows():
+    """The two halves of a mid row are selected by the two CTAs of a cluster:
+    a first half of equal top scores overflows its candidate list alone (the
+    whole row is then selected by digit passes: the lowest indices win), and
+    ties at the threshold that straddle the two halves keep the lowest
+    indices of the whole row."""
+    rng = np.random.default_rng(8)
+    N, m, k = 32768, 4, 1024
+    s = (rng.standard_normal((3, 1, N)) * 30 + 150).astype(np.float32)
+    s[0, 0, :16384] = 1000.0                       # 16384 equal keys in the first half
+    s[1, 0, 16000:16800] = 400.0                   # 800 tied top keys across the halves,
+    s[1, 0, 100:400] = 400.0                       # 300 more in the first half: 1100 ties > k
+    s[2, 0, 16384:16384 + 2000] = 900.0            # the top 2000, all in the second half
+    _check(s, np.full((3, 1), 4 * N - 1), N, m, k)
