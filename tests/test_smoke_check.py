@@ -53,3 +53,49 @@ def test_smoke_check_catches_a_wrong_selection(case):
         g["idx"][0, t, :] = np.arange(wl.k, dtype=np.int32) if n >= wl.k else -1
     with pytest.raises(AssertionError):
         E.smoke_check(wl, c, ref, g)
+
+
+# ---- the decode-shaped half of smoke(): two sequences over 3000 cached
+# entries (the smoke itself runs 20000 and 70000 on the GPU)
+
+@pytest.fixture(scope="module")
+def decode_case():
+    import math
+
+    import torch
+
+    import oracle as O
+    wl = E.smoke_decode_workload(3000)
+    inp = S.make_inputs(wl, "cpu")
+    c = {k: (S.bf16_bits(v) if v.dtype == torch.bfloat16 else v.numpy()) for k, v in inp.items()}
+    B, Tq = c["q_pos"].shape
+    idx = np.empty((B, Tq, wl.k), np.int32)
+    out = np.empty((B, Tq, wl.H, wl.d), np.float32)
+    for b in range(B):
+        kc, vc, ic = (O.bf16_to_f64(c[key][b]) for key in ("k_cmp", "v_cmp", "i_cmp"))
+        kr, vr = O.bf16_to_f64(c["k_raw"][b]), O.bf16_to_f64(c["v_raw"][b])
+        for j in range(Tq):
+            t = int(c["q_pos"][b, j])
+            s_ref = O.indexer_scores(O.bf16_to_f64(c["q_idx"][b, j]), ic, c["w"].astype(np.float64), t, wl.m)
+            idx[b, j] = O.topk(s_ref, wl.k)
+            win = O.window_rows(t, wl.W, int(c["raw_base"][b]), kr.shape[0])
+            out[b, j], _ = O.attend_one(O.bf16_to_f64(c["q"][b, j]), kc, vc, idx[b, j], kr, vr, win,
+                                        1 / math.sqrt(wl.d))
+    return wl, c, idx, out
+
+
+def test_smoke_decode_check_accepts_the_oracles_own_results(decode_case):
+    wl, c, idx, out = decode_case
+    assert E.smoke_decode_check(wl, c, idx, out) == 2
+
+
+def test_smoke_decode_check_catches_planted_mistakes(decode_case):
+    wl, c, idx, out = decode_case
+    bad_out = out.copy()
+    bad_out[1, 0, 63, 127] += 0.05
+    with pytest.raises(AssertionError):
+        E.smoke_decode_check(wl, c, idx, bad_out)
+    bad_idx = idx.copy()
+    bad_idx[0, 0] = np.arange(wl.k, dtype=np.int32)   # the lowest blocks instead of the best
+    with pytest.raises(AssertionError):
+        E.smoke_decode_check(wl, c, bad_idx, out)
